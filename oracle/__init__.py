@@ -1,0 +1,202 @@
+"""fp64 CPU oracle for the fused GAT neighbour aggregation (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the smoke check in
+``__graft_entry__`` and by the CPU-baseline leg of ``bench.py``; never by the
+product package.  It shares no code with the CUDA library.  See
+``gat_oracle.c`` for what it computes and which passages it follows.
+
+Arrays: ``h`` and ``dout`` are float32 ``[N, H, D]``, uint16 bit patterns of
+bfloat16 ``[N, H, D]``, or float64 (finite-difference checks); ``a_src`` /
+``a_dst`` ``[H, D]`` (float32 or float64).
+Every result is float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gat_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` (gcc, OpenMP) next to this file when stale."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared",
+                           _SRC, "-o", tmp, "-lm"])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    P, i64, i32, f64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    common = [i64, P, P, i32, i32, i32, P, P, P, f64]
+    lib.oracle_gat_forward.argtypes = common + [i64, P, P, P, P, P]
+    lib.oracle_gat_forward.restype = i32
+    lib.oracle_gat_node_stats.argtypes = common + [P, i64, P, P, P, P]
+    lib.oracle_gat_node_stats.restype = i32
+    lib.oracle_gat_backward.argtypes = common + [P, P, P, P, P, P]
+    lib.oracle_gat_backward.restype = i32
+    lib.oracle_gat_backward_rows.argtypes = common + [P, i64, P, P, P]
+    lib.oracle_gat_backward_rows.restype = i32
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = i32
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(_LIB)
+        return _lib
+
+
+def compile_variant(source_text: str, out_path: str) -> str:
+    """Compile a modified copy of the oracle source (used by tests that plant a
+    mistake in the oracle to show that the pins catch it)."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(source_text)
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared",
+                           src, "-o", out_path, "-lm"])
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+class Oracle:
+    """The oracle's entry points bound to one compiled library."""
+
+    def __init__(self, path: str | None = None):
+        self._path = path
+
+    @property
+    def lib(self):
+        if self._path is None:
+            return _load()
+        if not hasattr(self, "_lib"):
+            self._lib = _bind(self._path)
+        return self._lib
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def forward(self, row_ptr, col, h, a_src, a_dst, slope, sel=None, with_mag=False, with_alpha_sum=False):
+        row_ptr, col, h, a_src, a_dst, n, H, D, dt = _prep(row_ptr, col, h, a_src, a_dst)
+        sel = _sel(sel)
+        m = n if sel is None else len(sel)
+        out = np.empty((m, H, D), np.float64)
+        lse = np.empty((m, H), np.float64)
+        mag = np.empty((m, H, D), np.float64) if with_mag else None
+        asum = np.empty((m, H), np.float64) if with_alpha_sum else None
+        rc = self.lib.oracle_gat_forward(n, _p(row_ptr), _p(col), H, D, dt, _p(h), _p(a_src), _p(a_dst),
+                                        float(slope), 0 if sel is None else len(sel), _p(sel),
+                                        _p(out), _p(lse), _p(mag), _p(asum))
+        _check(rc, "forward")
+        return dict(out=out, lse=lse, out_mag=mag, alpha_sum=asum)
+
+    def node_stats(self, row_ptr, col, h, a_src, a_dst, slope, dout, sel=None):
+        """lse, Delta (= sum_j alpha_ij dout_i . h_j) and ds_dst per (node, head)."""
+        row_ptr, col, h, a_src, a_dst, n, H, D, dt = _prep(row_ptr, col, h, a_src, a_dst)
+        dout = np.ascontiguousarray(dout)
+        assert dout.shape == h.shape and dout.dtype == h.dtype
+        sel = _sel(sel)
+        m = n if sel is None else len(sel)
+        lse, delta, ds = (np.empty((m, H), np.float64) for _ in range(3))
+        rc = self.lib.oracle_gat_node_stats(n, _p(row_ptr), _p(col), H, D, dt, _p(h), _p(a_src),
+                                           _p(a_dst), float(slope), _p(dout),
+                                           0 if sel is None else len(sel), _p(sel),
+                                           _p(lse), _p(delta), _p(ds))
+        _check(rc, "node_stats")
+        return dict(lse=lse, delta=delta, ds_dst=ds)
+
+    def backward(self, row_ptr, col, h, a_src, a_dst, slope, dout, with_mag=False):
+        row_ptr, col, h, a_src, a_dst, n, H, D, dt = _prep(row_ptr, col, h, a_src, a_dst)
+        dout = np.ascontiguousarray(dout)
+        assert dout.shape == h.shape and dout.dtype == h.dtype
+        dh = np.empty((n, H, D), np.float64)
+        da_src = np.empty((H, D), np.float64)
+        da_dst = np.empty((H, D), np.float64)
+        dh_mag = np.empty((n, H, D), np.float64) if with_mag else None
+        da_mag = np.empty((2, H, D), np.float64) if with_mag else None
+        rc = self.lib.oracle_gat_backward(n, _p(row_ptr), _p(col), H, D, dt, _p(h), _p(a_src),
+                                         _p(a_dst), float(slope), _p(dout), _p(dh), _p(da_src),
+                                         _p(da_dst), _p(dh_mag), _p(da_mag))
+        _check(rc, "backward")
+        return dict(dh=dh, da_src=da_src, da_dst=da_dst, dh_mag=dh_mag,
+                    da_src_mag=None if da_mag is None else da_mag[0],
+                    da_dst_mag=None if da_mag is None else da_mag[1])
+
+    def backward_rows(self, row_ptr, col, h, a_src, a_dst, slope, dout, sel, with_mag=False):
+        """dh rows of the listed (distinct) nodes only, each from its neighbourhood."""
+        row_ptr, col, h, a_src, a_dst, n, H, D, dt = _prep(row_ptr, col, h, a_src, a_dst)
+        dout = np.ascontiguousarray(dout)
+        assert dout.shape == h.shape and dout.dtype == h.dtype
+        sel = _sel(sel)
+        dh = np.empty((len(sel), H, D), np.float64)
+        dh_mag = np.empty((len(sel), H, D), np.float64) if with_mag else None
+        rc = self.lib.oracle_gat_backward_rows(n, _p(row_ptr), _p(col), H, D, dt, _p(h), _p(a_src),
+                                              _p(a_dst), float(slope), _p(dout), len(sel), _p(sel),
+                                              _p(dh), _p(dh_mag))
+        _check(rc, "backward_rows")
+        return dict(dh=dh, dh_mag=dh_mag)
+
+
+def _p(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _prep(row_ptr, col, h, a_src, a_dst):
+    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    col = np.ascontiguousarray(col, dtype=np.int32)
+    if h.dtype == np.uint16:
+        dtype = 1
+    elif h.dtype == np.float32:
+        dtype = 0
+    elif h.dtype == np.float64:
+        dtype = 2
+    else:
+        raise TypeError("h must be float32, float64 or bfloat16 bit patterns (uint16)")
+    h = np.ascontiguousarray(h)
+    if h.ndim != 3:
+        raise ValueError("h must be [N, H, D]")
+    n, H, D = h.shape
+    if len(row_ptr) != n + 1:
+        raise ValueError("row_ptr must have N + 1 entries")
+    # float32 attention vectors widen exactly; float64 ones pass through
+    a_src = np.ascontiguousarray(a_src, dtype=np.float64).reshape(H, D)
+    a_dst = np.ascontiguousarray(a_dst, dtype=np.float64).reshape(H, D)
+    return row_ptr, col, h, a_src, a_dst, n, H, D, dtype
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its inputs (code {rc})")
+
+
+def _sel(sel):
+    return None if sel is None else np.ascontiguousarray(sel, dtype=np.int64)
+
+
+_default = Oracle()
+num_threads = _default.num_threads
+forward = _default.forward
+node_stats = _default.node_stats
+backward = _default.backward
+backward_rows = _default.backward_rows
