@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused GAT neighbour aggregation (forward + backward).
+
+One step = one forward and one backward pass over one synthetic graph whose
+inputs are resident in device memory (the graph is prepared once, outside the
+timed region, as in training).  Default workload: uniform random graph,
+N = 100,000, every in-degree 16 plus a self-loop, H = 4, D = 32, float32.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
+
+Prints one JSON line on rank 0.  `value` is forward+backward throughput in
+GEdge*head/s (E * H / step time, E counting self-loops); the forward-only
+figure, per-kernel times, the HBM roofline of the dominant kernel, an
+end-to-end figure through the public API with host buffers, the oracle's CPU
+throughput and the SM clocks seen during the timed region ride along.
+Under torchrun each rank runs an independent replica of the workload (the
+operation has no exchange step on one graph); the max time over ranks is
+used and `value` sums the replicas' units.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEdge·head/s fwd and fwd+bwd GAT aggregation; achieved HBM GB/s vs roofline"
+UNIT = "GEdge*head/s"
+DEFAULT_CONFIG = 2
+FWD_EVENTS, BWD_EVENTS = 3, 7
+FWD_KERNELS = ["fwd_main", "fwd_merge"]
+BWD_KERNELS = ["bwd_dst_main", "bwd_dst_merge", "bwd_src_main", "bwd_src_merge", "da_partial",
+               "da_final"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    p.add_argument("--impl", choices=["gnnagg", "reference"], default="gnnagg")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-budget-s", type=float, default=12.0,
+                   help="CPU seconds for the oracle baseline sample")
+    return p.parse_args(argv)
+
+
+# ---- bytes model (algorithmic, compulsory traffic) -----------------------------
+
+def algorithmic_bytes(n, e, H, D, s):
+    """Per-launch algorithmic bytes of the main kernels.
+
+    idx: CSR or CSC pointers + indices; gathered rows: one H*D row of s-byte
+    elements per edge; node rows: H*D per node.  Forward: indices, gathered
+    h_j, out written, lse written.  Backward, destination side: CSR indices,
+    gathered h_j, dout_i and h_i read.  Source side: CSC indices, gathered
+    dout_i, h_j read, dh_j written.  The per-edge gather of the 16-byte
+    destination statistics in the source-side pass is extra traffic, not
+    counted here (reported separately as stats_bytes)."""
+    idx = 4 * (n + 1) + 4 * e
+    gath = s * e * H * D
+    row = s * n * H * D
+    return {
+        "fwd_main": idx + gath + row + 4 * n * H,
+        "bwd_dst_main": idx + gath + 2 * row,
+        "bwd_src_main": idx + gath + 2 * row,
+        "stats_bytes": 16 * e * H,
+    }
+
+
+# ---- clocks during the timed region ------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- workload ---------------------------------------------------------------------
+
+def load_workload(idx):
+    import workload
+    w = workload.CONFIGS[idx]
+    rp, ci = workload.make_graph(w)
+    h, a_s, a_d, dout = workload.make_features(w, len(rp) - 1)
+    return w, rp, ci, h, a_s, a_d, dout
+
+
+def cpu_sample(rp, ci, frac_edges):
+    """The subgraph of the first m destination rows (all N nodes kept), with
+    about frac_edges of the edges: a prefix of the CSR."""
+    e_target = max(1, int(len(ci) * frac_edges))
+    m = int(np.searchsorted(rp, e_target, side="left"))
+    m = max(1, min(m, len(rp) - 1))
+    rp2 = rp.copy()
+    rp2[m + 1:] = rp[m]
+    return rp2, ci[:rp[m]].copy(), m
+
+
+def time_oracle(rp, ci, h, a_s, a_d, dout, slope):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.forward(rp, ci, h, a_s, a_d, slope)
+    oracle.backward(rp, ci, h, a_s, a_d, slope, dout)
+    return time.perf_counter() - t0
+
+
+def oracle_baseline(w, rp, ci, h, a_s, a_d, dout, budget_s):
+    """Oracle throughput on a bounded sample: a probe on 2% of the edges sizes
+    a prefix subgraph that takes about budget_s seconds."""
+    import oracle
+    probe_rp, probe_ci, _ = cpu_sample(rp, ci, 0.02)
+    t_probe = time_oracle(probe_rp, probe_ci, h, a_s, a_d, dout, w.slope)
+    frac = min(1.0, 0.02 * budget_s / max(t_probe, 1e-3))
+    srp, sci, m = cpu_sample(rp, ci, frac)
+    t = time_oracle(srp, sci, h, a_s, a_d, dout, w.slope)
+    units = len(sci) * w.H
+    return {"value": units / t / 1e9, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"destinations 0..{m - 1} of {len(rp) - 1} with their {len(sci)} in-edges "
+                      f"({100.0 * len(sci) / len(ci):.1f}% of E), all N nodes; fp64 forward + "
+                      f"backward, {t:.2f} s"}
+
+
+# ---- reference arm: the oracle on the host ------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    w, rp, ci, h, a_s, a_d, dout = load_workload(args.config)
+    # size each step so that warmup + steps fit in about three minutes
+    per_step = 180.0 / max(1, args.steps + args.warmup)
+    probe_rp, probe_ci, _ = cpu_sample(rp, ci, 0.02)
+    t_probe = time_oracle(probe_rp, probe_ci, h, a_s, a_d, dout, w.slope)
+    frac = min(1.0, 0.02 * per_step / max(t_probe, 1e-3))
+    srp, sci, m = cpu_sample(rp, ci, frac)
+    for _ in range(args.warmup):
+        time_oracle(srp, sci, h, a_s, a_d, dout, w.slope)
+    t = 0.0
+    for _ in range(args.steps):
+        t += time_oracle(srp, sci, h, a_s, a_d, dout, w.slope)
+    units = len(sci) * w.H
+    value = units * args.steps / t / 1e9
+    sample = (f"destinations 0..{m - 1} of {len(rp) - 1} with their {len(sci)} in-edges "
+              f"({100.0 * len(sci) / len(ci):.1f}% of E) per step, all N nodes")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "n_nodes": len(rp) - 1, "n_edges": len(ci),
+                       "H": w.H, "D": w.D},
+            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
+                             "cores": oracle.num_threads(), "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- the CUDA path ------------------------------------------------------------------
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload_name, kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if its
+    kernel source is unchanged since the capture; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        entry = rec.get(workload_name, {}).get(kernel)
+        if not entry:
+            return None
+        srcs = [os.path.join(ROOT, p) for p in entry["sources"]]
+        if source_hash(srcs) != entry["source_hash"]:
+            return None
+        return entry["bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
+def run_gnnagg(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    import graph_neural_network_gb300 as gnn
+    from graph_neural_network_gb300 import _native
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w, rp, ci, h_np, a_s_np, a_d_np, dout_np = load_workload(args.config)
+    n, e, H, D = len(rp) - 1, len(ci), w.H, w.D
+    s = 4 if w.dtype == "f32" else 2
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+
+    def dev_feat(x):
+        x = np.ascontiguousarray(x)
+        t = torch.from_numpy(x.view(np.int16) if w.dtype == "bf16" else x)
+        t = t.to(dev)
+        return t.view(torch.bfloat16) if w.dtype == "bf16" else t
+
+    rp_d = torch.from_numpy(rp).to(dev)
+    ci_d = torch.from_numpy(ci).to(dev)
+    h = dev_feat(h_np)
+    dout = dev_feat(dout_np)
+    a_s = torch.from_numpy(a_s_np).to(dev)
+    a_d = torch.from_numpy(a_d_np).to(dev)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem0 = torch.cuda.memory_allocated(dev)
+    t0 = time.perf_counter()
+    g = gnn.Graph(rp_d, ci_d)
+    prepare_ms = 1e3 * (time.perf_counter() - t0)
+    st = g.stats()
+    out = torch.empty_like(h)
+    lse = torch.empty((n, H), dtype=torch.float32, device=dev)
+    dh = torch.empty_like(h)
+    da_s = torch.empty((H, D), dtype=torch.float32, device=dev)
+    da_d = torch.empty((H, D), dtype=torch.float32, device=dev)
+    ws = g.workspace(H, D, tdt)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    lib = _native.load()
+    dt_code = _native.F32 if w.dtype == "f32" else _native.BF16
+    P = ctypes.c_void_p
+
+    def ptr(t):
+        return P(t.data_ptr())
+
+    stream = torch.cuda.current_stream(dev)
+    sp = P(stream.cuda_stream)
+
+    def make_events(k):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+        for ev in evs:
+            ev.record(stream)  # creates the underlying event
+        arr = (ctypes.c_void_p * k)(*[ev.cuda_event for ev in evs])
+        return evs, arr
+
+    def step(fe=None, be=None):
+        rc = lib.gat_agg_forward_timed(g.handle, H, D, dt_code, ptr(h), ptr(a_s), ptr(a_d),
+                                       w.slope, ptr(out), ptr(lse), ptr(ws), ws.numel(), sp,
+                                       fe, FWD_EVENTS if fe is not None else 0)
+        _native.check(rc, "forward")
+        rc = lib.gat_agg_backward_timed(g.handle, H, D, dt_code, ptr(h), ptr(a_s), ptr(a_d),
+                                        w.slope, ptr(lse), ptr(dout), ptr(dh), ptr(da_s),
+                                        ptr(da_d), ptr(ws), ws.numel(), sp,
+                                        be, BWD_EVENTS if be is not None else 0)
+        _native.check(rc, "backward")
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    gnn.check_device_error(g)
+    peak_mem = torch.cuda.max_memory_allocated(dev) - mem0
+
+    K = args.steps
+    fev = [make_events(FWD_EVENTS) for _ in range(K)]
+    bev = [make_events(BWD_EVENTS) for _ in range(K)]
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(visible.split(",")[dev.index].strip() if visible else dev.index)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    wall0 = time.perf_counter()
+    for k in range(K):
+        flush.zero_()  # L2 flush between steps, outside the timed events
+        step(fev[k][1], bev[k][1])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    gnn.check_device_error(g)
+
+    kern = {name: 0.0 for name in FWD_KERNELS + BWD_KERNELS}
+    t_fwd = t_bwd = 0.0
+    for k in range(K):
+        fe, be = fev[k][0], bev[k][0]
+        for i, name in enumerate(FWD_KERNELS):
+            kern[name] += fe[i].elapsed_time(fe[i + 1])
+        for i, name in enumerate(BWD_KERNELS):
+            kern[name] += be[i].elapsed_time(be[i + 1])
+        t_fwd += fe[0].elapsed_time(fe[-1])
+        t_bwd += be[0].elapsed_time(be[-1])
+    t_fwd /= K
+    t_bwd /= K
+    kern = {k: v / K for k, v in kern.items()}
+    ms_step = t_fwd + t_bwd
+    if world > 1:
+        tt = torch.tensor([ms_step, t_fwd], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step, t_fwd = float(tt[0]), float(tt[1])
+    units = e * H
+    value = world * units / (ms_step * 1e-3) / 1e9
+    fwd_value = world * units / (t_fwd * 1e-3) / 1e9
+
+    # roofline of the dominant kernel
+    ab = algorithmic_bytes(n, e, H, D, s)
+    main = {k: kern[k] for k in ("fwd_main", "bwd_dst_main", "bwd_src_main")}
+    dom = max(main, key=main.get)
+    peak, peak_kind = peaks()
+    achieved = ab[dom] / (kern[dom] * 1e-3) / 1e9
+    traffic = measured_traffic(w.name, dom)
+    step_bytes = ab["fwd_main"] + ab["bwd_dst_main"] + ab["bwd_src_main"]
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                "algorithmic_bytes": ab[dom], "peak_source": peak_kind}
+    kernel_frac = {k: ab[k] / (kern[k] * 1e-3) / 1e9 / peak for k in main if kern[k] > 0}
+
+    launches_per_step = (1 + (st["csr"]["hubs"] > 0)) + (1 + (st["csr"]["hubs"] > 0)) + \
+        (1 + (st["csc"]["hubs"] > 0)) + 2
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "n_nodes": n, "n_edges": e, "H": H, "D": D,
+                       "feature_dtype": w.dtype,
+                       "max_in_degree": st["csr"]["max_deg"],
+                       "max_out_degree": st["csc"]["max_deg"],
+                       "l2": f"flushed before every step ({flush.numel() >> 20} MiB write)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "fwd_value": fwd_value, "fwd_ms": t_fwd, "bwd_ms": t_bwd,
+            "kernels_ms": kern, "kernel_hbm_frac": kernel_frac,
+            "roofline": roofline,
+            "step_roofline": {"achieved": step_bytes / (ms_step * 1e-3) / 1e9, "peak": peak,
+                              "unit": "GB/s", "frac": step_bytes / (ms_step * 1e-3) / 1e9 / peak},
+            "gpu_launches": launches_per_step * K,
+            "prepare_ms": prepare_ms, "peak_mem_gb": peak_mem / 1e9,
+            "clocks": clocks, "wall_s": wall}
+
+    if not args.no_e2e:
+        line["e2e"] = e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world,
+                          dev, units)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(w, rp, ci, h_np, a_s_np, a_d_np, dout_np,
+                                               args.cpu_budget_s)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev, units):
+    """Same metric through the public API with host buffers: every step copies
+    the step's inputs from pinned host memory and reads every result back."""
+    import torch
+    import torch.distributed as dist
+    import graph_neural_network_gb300 as gnn
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h_host, d_host = pin(h), pin(dout)
+    h_host.copy_(h)
+    d_host.copy_(dout)
+    as_host, ad_host = pin(a_s), pin(a_d)
+    as_host.copy_(a_s)
+    ad_host.copy_(a_d)
+    o_host, l_host, dh_host = pin(out), pin(lse), pin(dh)
+    das_host, dad_host = pin(da_s), pin(da_d)
+    h2d = sum(t.numel() * t.element_size() for t in (h_host, d_host, as_host, ad_host))
+    d2h = sum(t.numel() * t.element_size() for t in (o_host, l_host, dh_host, das_host, dad_host))
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        h.copy_(h_host, non_blocking=True)
+        dout.copy_(d_host, non_blocking=True)
+        a_s.copy_(as_host, non_blocking=True)
+        a_d.copy_(ad_host, non_blocking=True)
+        gnn.gat_forward(g, h, a_s, a_d, w.slope, out=out, lse=lse, ws=ws)
+        gnn.gat_backward(g, h, a_s, a_d, w.slope, lse, dout, dh=dh, da_src=da_s, da_dst=da_d,
+                         ws=ws)
+        o_host.copy_(out, non_blocking=True)
+        l_host.copy_(lse, non_blocking=True)
+        dh_host.copy_(dh, non_blocking=True)
+        das_host.copy_(da_s, non_blocking=True)
+        dad_host.copy_(da_d, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    K = max(1, min(args.steps, 200))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt[0])
+    return {"value": world * units / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+            "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    try:
+        return run_gnnagg(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,288 @@
+// Device-side helpers shared by the aggregation kernels: 16-byte row
+// vectors, per-head warp reductions, the lane geometry of a feature row, and
+// the bulk-copy staging of an edge list into shared memory.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace gnn {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kWarps = 8;      // warps per thread block in every aggregation kernel
+constexpr int kThreads = kWarps * 32;
+constexpr int kUnroll = 4;     // edges in flight per lane and batch
+
+// Resident blocks per SM the main kernels are compiled for (register cap):
+// 3 blocks (24 warps, <= 80 registers) for rows up to 512 bytes.
+template <int NV>
+struct MinBlocks {
+  static constexpr int value = NV == 1 ? 3 : (NV == 2 ? 2 : 1);
+};
+
+template <typename T>
+struct VecOf;
+template <>
+struct VecOf<float> {
+  static constexpr int n = 4;
+};
+template <>
+struct VecOf<__nv_bfloat16> {
+  static constexpr int n = 8;
+};
+
+// Read-only 16-byte load (gathered feature rows, edge lists, statistics).
+__device__ __forceinline__ uint4 ld16(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ float4 ld16f(const void* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4& r, float (&x)[VecOf<T>::n]);
+
+template <>
+__device__ __forceinline__ void unpack<float>(const uint4& r, float (&x)[4]) {
+  x[0] = __uint_as_float(r.x);
+  x[1] = __uint_as_float(r.y);
+  x[2] = __uint_as_float(r.z);
+  x[3] = __uint_as_float(r.w);
+}
+
+// bfloat16 -> float32 is exact: the 16 bits become the high half of a float.
+template <>
+__device__ __forceinline__ void unpack<__nv_bfloat16>(const uint4& r, float (&x)[8]) {
+  x[0] = __uint_as_float(r.x << 16);
+  x[1] = __uint_as_float(r.x & 0xffff0000u);
+  x[2] = __uint_as_float(r.y << 16);
+  x[3] = __uint_as_float(r.y & 0xffff0000u);
+  x[4] = __uint_as_float(r.z << 16);
+  x[5] = __uint_as_float(r.z & 0xffff0000u);
+  x[6] = __uint_as_float(r.w << 16);
+  x[7] = __uint_as_float(r.w & 0xffff0000u);
+}
+
+// Same values as unpack(), computed with byte permutes instead of shifts.  The
+// kernels widen each gathered vector twice (once for the score, once for the
+// accumulation); the different instruction sequence keeps the compiler from
+// holding all widened values of a batch live in registers between the two.
+template <typename T>
+__device__ __forceinline__ void unpack_alt(const uint4& r, float (&x)[VecOf<T>::n]);
+
+template <>
+__device__ __forceinline__ void unpack_alt<float>(const uint4& r, float (&x)[4]) {
+  unpack<float>(r, x);
+}
+
+template <>
+__device__ __forceinline__ void unpack_alt<__nv_bfloat16>(const uint4& r, float (&x)[8]) {
+  x[0] = __uint_as_float(__byte_perm(r.x, 0u, 0x1054));
+  x[1] = __uint_as_float(__byte_perm(r.x, 0u, 0x3244));
+  x[2] = __uint_as_float(__byte_perm(r.y, 0u, 0x1054));
+  x[3] = __uint_as_float(__byte_perm(r.y, 0u, 0x3244));
+  x[4] = __uint_as_float(__byte_perm(r.z, 0u, 0x1054));
+  x[5] = __uint_as_float(__byte_perm(r.z, 0u, 0x3244));
+  x[6] = __uint_as_float(__byte_perm(r.w, 0u, 0x1054));
+  x[7] = __uint_as_float(__byte_perm(r.w, 0u, 0x3244));
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack(const float (&x)[VecOf<T>::n]);
+
+template <>
+__device__ __forceinline__ uint4 pack<float>(const float (&x)[4]) {
+  return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                    __float_as_uint(x[3]));
+}
+
+__device__ __forceinline__ uint32_t bf2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <>
+__device__ __forceinline__ uint4 pack<__nv_bfloat16>(const float (&x)[8]) {
+  return make_uint4(bf2(x[0], x[1]), bf2(x[2], x[3]), bf2(x[4], x[5]), bf2(x[6], x[7]));
+}
+
+__device__ __forceinline__ void st16(void* p, const uint4& v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+// Sum over the `hv` consecutive lanes that hold one head (hv a power of two).
+__device__ __forceinline__ float head_sum(float v, int hv) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1)
+    if (o < hv) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Where one lane sits in a feature row.  A row of rv 16-byte vectors is spread
+// over lpr lanes (a power of two); a warp therefore handles G = 32 / lpr rows
+// (edges) at once, sub-group g = lane / lpr.  With nv > 1 (rows wider than
+// 512 bytes) lpr = 32 and lane p holds vectors p, p + 32, ...
+template <int NV>
+struct Lane {
+  int lane, g, G, p;
+  int q[NV];     // vector index within the row
+  bool ok[NV];   // q < rv
+  int k[NV];     // head of the vector
+  __device__ __forceinline__ Lane(const Shape& s) {
+    lane = threadIdx.x & 31;
+    g = lane / s.lpr;
+    G = 32 / s.lpr;
+    p = lane - g * s.lpr;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      q[v] = p + s.lpr * v;
+      ok[v] = q[v] < s.rv;
+      k[v] = ok[v] ? q[v] / s.hv : 0;
+    }
+  }
+  // lane writes the per-head scalar of vector v (one lane per head)
+  __device__ __forceinline__ bool head_leader(const Shape& s, int v) const {
+    return ok[v] && (q[v] % s.hv) == 0;
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ const char* row_base(const void* base, int64_t node, int rv) {
+  return reinterpret_cast<const char*>(base) + node * int64_t(rv) * 16;
+}
+
+// This lane's slice of an attention vector [H][D] (float), times `scale`.
+template <typename T, int NV>
+__device__ __forceinline__ void load_att(const float* a, const Lane<NV>& L, float scale,
+                                         float (&w)[NV][VecOf<T>::n]) {
+  constexpr int V = VecOf<T>::n;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+#pragma unroll
+    for (int c4 = 0; c4 < V; c4 += 4) {
+      float4 t = L.ok[v] ? ld16f(a + L.q[v] * V + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[v][c4 + 0] = t.x * scale;
+      w[v][c4 + 1] = t.y * scale;
+      w[v][c4 + 2] = t.z * scale;
+      w[v][c4 + 3] = t.w * scale;
+    }
+  }
+}
+
+// This lane's vectors of row `node` of x, widened to float (zeros where q >= rv).
+template <typename T, int NV>
+__device__ __forceinline__ void load_row(const void* x, int64_t node, const Shape& s,
+                                         const Lane<NV>& L, float (&r)[NV][VecOf<T>::n]) {
+  const char* row = row_base<T>(x, node, s.rv);
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+    unpack<T>(L.ok[v] ? ld16(row + 16 * L.q[v]) : make_uint4(0, 0, 0, 0), r[v]);
+}
+
+// Per-head dot product w[k] . x[node][k] for the heads this lane touches.
+template <typename T, int NV>
+__device__ __forceinline__ void row_dot(const void* x, int64_t node, const Shape& s,
+                                        const Lane<NV>& L, const float (&w)[NV][VecOf<T>::n],
+                                        float (&out)[NV]) {
+  constexpr int V = VecOf<T>::n;
+  float r[NV][V];
+  load_row<T, NV>(x, node, s, L, r);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    float d = 0.f;
+#pragma unroll
+    for (int c = 0; c < V; ++c) d = fmaf(r[v][c], w[v][c], d);
+    out[v] = head_sum(d, s.hv);
+  }
+}
+
+// ---- mbarrier + bulk copy (shared::cta) --------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// One-dimensional bulk copy global -> shared, completing on `bar`.  Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bounded wait on phase `parity`; false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int limit) {
+  const uint32_t a = smem_u32(bar);
+  for (int it = 0; it < limit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+constexpr int kWaitLimit = 1 << 20;
+
+// Stage idx[beg, end) into shared memory `dst` (16-byte aligned) such that
+// element x lands at dst[x - (beg & ~3)].  The 16-byte-aligned interior moves
+// with one bulk copy; the ragged ends (< 4 elements each) with plain loads.
+// Must be called by all threads of the block; returns false (after recording
+// a timeout in *err) when the bulk copy did not complete within the limit.
+__device__ __forceinline__ bool stage_edges(int32_t* dst, const int32_t* idx, int beg, int end,
+                                            uint64_t* bar, int32_t* err) {
+  const int base = beg & ~3;
+  const int a0 = (beg + 3) & ~3;
+  const int a1 = end & ~3;
+  const bool bulk = a1 > a0;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    if (bulk) {
+      mbar_expect_tx(bar, uint32_t(a1 - a0) * 4u);
+      bulk_g2s(dst + (a0 - base), idx + a0, uint32_t(a1 - a0) * 4u, bar);
+    }
+  }
+  // ragged head and tail (or everything when the item is short)
+  const int h1 = bulk ? a0 : end;
+  for (int x = beg + int(threadIdx.x); x < h1; x += blockDim.x) dst[x - base] = __ldg(idx + x);
+  if (bulk)
+    for (int x = a1 + int(threadIdx.x); x < end; x += blockDim.x) dst[x - base] = __ldg(idx + x);
+  __syncthreads();  // barrier initialised before anyone waits on it
+  bool timed_out = false;
+  if (bulk) timed_out = !mbar_wait(bar, 0, kWaitLimit);
+  if (__syncthreads_or(timed_out)) {
+    if (threadIdx.x == 0) {
+      atomicOr(err, DEVERR_TIMEOUT);
+      mbar_wait(bar, 0, kWaitLimit);  // let the copy land before the block exits
+    }
+    return false;
+  }
+  return true;
+}
+
+}  // namespace gnn

@@ -1,0 +1,672 @@
+// Backward pass of the fused GAT neighbour aggregation.
+//
+// alpha is never stored: both passes recompute it from the per-node
+// log-sum-exp the forward pass kept ("On Efficient Scaling of GNNs via
+// IO-Aware Layers Implementations", Technical Summary > Methodology,
+// attention-based layers, backward: compact per-node statistics instead of
+// edge weights, attention recomputed on the fly).  With da_ij = dout_i . h_j,
+// Delta_i = sum_j alpha_ij da_ij, dz_ij = alpha_ij (da_ij - Delta_i) g_ij and
+// g_ij the LeakyReLU slope factor:
+//
+//   pass 1, destination side, over the CSR (one streaming pass per node):
+//     SA = sum alpha da g,  SB = sum alpha g,  SD = sum alpha da = Delta_i,
+//     ds_dst(i) = SA - Delta_i SB = sum_j dz_ij
+//     -> per-node record {s_dst (base 2), lse (base 2), Delta, ds_dst} per head
+//   pass 2, source side, over the cached CSC transpose (same page, SpMM
+//   bullet: transposed adjacency cached for the backward pass):
+//     dh_j = sum_i alpha_ij dout_i + ds_src(j) a_src + ds_dst(j) a_dst,
+//     ds_src(j) = sum_i dz_ij, gathering dout_i and i's record per edge
+//   da_src = sum_j ds_src(j) h_j, da_dst = sum_i ds_dst(i) h_i: per-block
+//     partial sums, then a fixed-order float64 sum over blocks.
+//
+// Both passes use the same degree-aware tiling as the forward pass (warp per
+// light node, block per mid node, chunked hubs with fixed-order merges), over
+// in-degrees for pass 1 and out-degrees for pass 2.
+#include "device.cuh"
+
+namespace gnn {
+namespace {
+
+struct DirArgs {
+  const int32_t* ptr;
+  const int32_t* idx;
+  const int32_t* light;
+  int64_t n_light;
+  const int4* items;
+  int64_t n_items;
+  const int4* hubs;
+  int64_t n_hubs;
+  int col_off;  // bytes of shared memory before the per-warp partials
+};
+
+struct BwdArgs {
+  Shape s;
+  DirArgs csr, csc;
+  int64_t n;
+  const void* h;
+  const float* a_src;
+  const float* a_dst;
+  float slope;
+  const float* lse;
+  const void* dout;
+  void* dh;
+  float* da_src;
+  float* da_dst;
+  float4* stats;     // [N][H] {s_dst2, lse2, Delta, ds_dst}
+  float* ds_src;     // [N][H]
+  float4* dst_part;  // [CSR hub chunks][H] {SA, SB, SD, s_dst2}
+  float* src_acc;    // [CSC hub chunks][H * D]
+  float* src_sum;    // [CSC hub chunks][H]
+  double* da_part;   // [da blocks][2][H * D]
+  int da_blocks;
+  int32_t* err;
+};
+
+__device__ __forceinline__ float leaky(float z, float slope) { return z > 0.f ? z : slope * z; }
+__device__ __forceinline__ float leaky_grad(float z, float slope) { return z > 0.f ? 1.f : slope; }
+
+// Butterfly sum over the warp's sub-groups (all lanes end with the total).
+__device__ __forceinline__ float subgroup_sum(float x, const Shape& s) {
+  for (int o = s.lpr; o < 32; o <<= 1) x += __shfl_xor_sync(kFull, x, o);
+  return x;
+}
+
+// ---------------------------------------------------------------------------
+// pass 1: destination side (CSR)
+// ---------------------------------------------------------------------------
+
+template <typename T, int NV>
+__device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
+                                          const int32_t* cols, int colbase, int beg, int end,
+                                          const float (&as2)[NV][VecOf<T>::n],
+                                          const float (&gi)[NV][VecOf<T>::n],
+                                          const float (&sd2)[NV], const float (&lse2)[NV],
+                                          float (&SA)[NV], float (&SB)[NV], float (&SD)[NV]) {
+  constexpr int V = VecOf<T>::n;
+  constexpr int U = kUnroll;
+  const int step = L.G * U;
+  int jn[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = beg + u * L.G + L.g;
+    jn[u] = e < end ? cols[e - colbase] : -1;
+  }
+  for (int base = beg; base < end; base += step) {
+    int j[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) j[u] = jn[u];
+    if (base + step < end) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = base + step + u * L.G + L.g;
+        jn[u] = e < end ? cols[e - colbase] : -1;
+      }
+    }
+    uint4 raw[U][NV];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+        raw[u][v] = (j[u] >= 0 && L.ok[v]) ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v])
+                                           : make_uint4(0, 0, 0, 0);
+    float ss[U][NV], dd[U][NV];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        float x[V];
+        unpack<T>(raw[u][v], x);
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          a = fmaf(x[c], as2[v][c], a);
+          b = fmaf(x[c], gi[v][c], b);
+        }
+        ss[u][v] = a;
+        dd[u][v] = b;
+      }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const float z = sd2[v] + head_sum(ss[u][v], A.s.hv);
+        const float da = head_sum(dd[u][v], A.s.hv);
+        const float al = j[u] >= 0 ? exp2f(leaky(z, A.slope) - lse2[v]) : 0.f;
+        const float g = leaky_grad(z, A.slope);
+        const float ad = al * da;
+        SA[v] = fmaf(ad, g, SA[v]);
+        SB[v] = fmaf(al, g, SB[v]);
+        SD[v] += ad;
+      }
+  }
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_dst_main(const BwdArgs A) {
+  constexpr int V = VecOf<T>::n;
+  const DirArgs& D = A.csr;
+  const Lane<NV> L(A.s);
+  const int wid = threadIdx.x >> 5;
+  extern __shared__ __align__(16) unsigned char smem[];
+  const bool item = blockIdx.x < D.n_items;
+  int i, beg, end, slot = -1;
+  const int32_t* cols = D.idx;
+  int colbase = 0;
+  if (item) {
+    const int4 it = D.items[blockIdx.x];
+    i = it.x;
+    slot = it.w;
+    int32_t* sc = reinterpret_cast<int32_t*>(smem + 16);
+    if (!stage_edges(sc, D.idx, it.y, it.z, reinterpret_cast<uint64_t*>(smem), A.err)) return;
+    cols = sc;
+    colbase = it.y & ~3;
+    const int per = (it.z - it.y + kWarps - 1) / kWarps;
+    beg = min(it.z, it.y + wid * per);
+    end = min(it.z, beg + per);
+  } else {
+    const int64_t t = (int64_t(blockIdx.x) - D.n_items) * kWarps + wid;
+    if (t >= D.n_light) return;
+    i = D.light[t];
+    beg = D.ptr[i];
+    end = D.ptr[i + 1];
+  }
+  float as2[NV][V], gi[NV][V], sd2[NV], lse2[NV];
+  {
+    float ad2[NV][V];
+    load_att<T, NV>(A.a_dst, L, kLog2e, ad2);
+    row_dot<T, NV>(A.h, i, A.s, L, ad2, sd2);
+  }
+  load_att<T, NV>(A.a_src, L, kLog2e, as2);
+  load_row<T, NV>(A.dout, i, A.s, L, gi);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) lse2[v] = L.ok[v] ? A.lse[int64_t(i) * A.s.H + L.k[v]] * kLog2e : 0.f;
+  float SA[NV], SB[NV], SD[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) SA[v] = SB[v] = SD[v] = 0.f;
+  dst_edges<T, NV>(A, L, cols, colbase, beg, end, as2, gi, sd2, lse2, SA, SB, SD);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    SA[v] = subgroup_sum(SA[v], A.s);
+    SB[v] = subgroup_sum(SB[v], A.s);
+    SD[v] = subgroup_sum(SD[v], A.s);
+  }
+  if (!item) {
+    if (L.g == 0)
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+        if (L.head_leader(A.s, v))
+          A.stats[int64_t(i) * A.s.H + L.k[v]] =
+              make_float4(sd2[v], lse2[v], SD[v], SA[v] - SD[v] * SB[v]);
+    return;
+  }
+  // block item: fold the warps' partial sums in warp order
+  float* wp = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H][3]
+  const int H = A.s.H;
+  if (L.g == 0)
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+      if (L.head_leader(A.s, v)) {
+        float* p = wp + (wid * H + L.k[v]) * 3;
+        p[0] = SA[v];
+        p[1] = SB[v];
+        p[2] = SD[v];
+      }
+  __syncthreads();
+  if (wid != 0 || L.g != 0) return;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    if (!L.head_leader(A.s, v)) continue;
+    float a = 0.f, b = 0.f, d = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float* p = wp + (w * H + L.k[v]) * 3;
+      a += p[0];
+      b += p[1];
+      d += p[2];
+    }
+    if (slot < 0)
+      A.stats[int64_t(i) * H + L.k[v]] = make_float4(sd2[v], lse2[v], d, a - d * b);
+    else
+      A.dst_part[int64_t(slot) * H + L.k[v]] = make_float4(a, b, d, sd2[v]);
+  }
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads) bwd_dst_merge(const BwdArgs A) {
+  const Lane<NV> L(A.s);
+  const int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (t >= A.csr.n_hubs || L.g != 0) return;
+  const int4 hb = A.csr.hubs[t];
+  const int H = A.s.H;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    if (!L.head_leader(A.s, v)) continue;
+    float a = 0.f, b = 0.f, d = 0.f;
+    for (int c = 0; c < hb.z; ++c) {
+      const float4 p = A.dst_part[(int64_t(hb.y) + c) * H + L.k[v]];
+      a += p.x;
+      b += p.y;
+      d += p.z;
+    }
+    const float sd2 = A.dst_part[int64_t(hb.y) * H + L.k[v]].w;
+    const float lse2 = A.lse[int64_t(hb.x) * H + L.k[v]] * kLog2e;
+    A.stats[int64_t(hb.x) * H + L.k[v]] = make_float4(sd2, lse2, d, a - d * b);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// pass 2: source side (CSC)
+// ---------------------------------------------------------------------------
+
+template <typename T, int NV>
+__device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
+                                          const int32_t* cols, int colbase, int beg, int end,
+                                          const float (&xj)[NV][VecOf<T>::n],
+                                          const float (&ss2)[NV], float (&acc)[NV][VecOf<T>::n],
+                                          float (&SZ)[NV]) {
+  constexpr int V = VecOf<T>::n;
+  constexpr int U = kUnroll;
+  const int step = L.G * U;
+  const int H = A.s.H;
+  int in[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = beg + u * L.G + L.g;
+    in[u] = e < end ? cols[e - colbase] : -1;
+  }
+  for (int base = beg; base < end; base += step) {
+    int i[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) i[u] = in[u];
+    if (base + step < end) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = base + step + u * L.G + L.g;
+        in[u] = e < end ? cols[e - colbase] : -1;
+      }
+    }
+    uint4 raw[U][NV];
+    float4 st[U][NV];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const bool ok = i[u] >= 0 && L.ok[v];
+        raw[u][v] = ok ? ld16(row_base<T>(A.dout, i[u], A.s.rv) + 16 * L.q[v])
+                       : make_uint4(0, 0, 0, 0);
+        st[u][v] = ok ? ld16f(A.stats + int64_t(i[u]) * H + L.k[v])
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    float dd[U][NV];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        float g[V];
+        unpack<T>(raw[u][v], g);
+        float b = 0.f;
+#pragma unroll
+        for (int c = 0; c < V; ++c) b = fmaf(g[c], xj[v][c], b);
+        dd[u][v] = b;
+      }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const float da = head_sum(dd[u][v], A.s.hv);
+        const float z = st[u][v].x + ss2[v];
+        const float al = i[u] >= 0 ? exp2f(leaky(z, A.slope) - st[u][v].y) : 0.f;
+        SZ[v] = fmaf(al * (da - st[u][v].z), leaky_grad(z, A.slope), SZ[v]);
+        float g[V];
+        unpack_alt<T>(raw[u][v], g);
+#pragma unroll
+        for (int c = 0; c < V; ++c) acc[v][c] = fmaf(al, g[c], acc[v][c]);
+      }
+  }
+}
+
+// dh_j = acc + ds_src a_src + ds_dst a_dst (natural units), ds_src(j) = SZ.
+template <typename T, int NV>
+__device__ __forceinline__ void write_src(const BwdArgs& A, const Lane<NV>& L, int64_t j,
+                                          const float (&acc)[NV][VecOf<T>::n],
+                                          const float (&SZ)[NV]) {
+  constexpr int V = VecOf<T>::n;
+  float as[NV][V], ad[NV][V];
+  load_att<T, NV>(A.a_src, L, 1.f, as);
+  load_att<T, NV>(A.a_dst, L, 1.f, ad);
+  char* orow = reinterpret_cast<char*>(A.dh) + j * int64_t(A.s.rv) * 16;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    if (!L.ok[v]) continue;
+    const float dsd = A.stats[j * A.s.H + L.k[v]].w;
+    float x[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c) x[c] = fmaf(dsd, ad[v][c], fmaf(SZ[v], as[v][c], acc[v][c]));
+    st16(orow + 16 * L.q[v], pack<T>(x));
+    if (L.head_leader(A.s, v)) A.ds_src[j * A.s.H + L.k[v]] = SZ[v];
+  }
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(const BwdArgs A) {
+  constexpr int V = VecOf<T>::n;
+  const DirArgs& D = A.csc;
+  const Lane<NV> L(A.s);
+  const int wid = threadIdx.x >> 5;
+  extern __shared__ __align__(16) unsigned char smem[];
+  const bool item = blockIdx.x < D.n_items;
+  int j, beg, end, slot = -1;
+  const int32_t* cols = D.idx;
+  int colbase = 0;
+  if (item) {
+    const int4 it = D.items[blockIdx.x];
+    j = it.x;
+    slot = it.w;
+    int32_t* sc = reinterpret_cast<int32_t*>(smem + 16);
+    if (!stage_edges(sc, D.idx, it.y, it.z, reinterpret_cast<uint64_t*>(smem), A.err)) return;
+    cols = sc;
+    colbase = it.y & ~3;
+    const int per = (it.z - it.y + kWarps - 1) / kWarps;
+    beg = min(it.z, it.y + wid * per);
+    end = min(it.z, beg + per);
+  } else {
+    const int64_t t = (int64_t(blockIdx.x) - D.n_items) * kWarps + wid;
+    if (t >= D.n_light) return;
+    j = D.light[t];
+    beg = D.ptr[j];
+    end = D.ptr[j + 1];
+  }
+  float xj[NV][V], ss2[NV], acc[NV][V], SZ[NV];
+  load_row<T, NV>(A.h, j, A.s, L, xj);
+  {
+    float as2[NV][V];
+    load_att<T, NV>(A.a_src, L, kLog2e, as2);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      float d = 0.f;
+#pragma unroll
+      for (int c = 0; c < V; ++c) d = fmaf(xj[v][c], as2[v][c], d);
+      ss2[v] = head_sum(d, A.s.hv);
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    SZ[v] = 0.f;
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
+  }
+  src_edges<T, NV>(A, L, cols, colbase, beg, end, xj, ss2, acc, SZ);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    SZ[v] = subgroup_sum(SZ[v], A.s);
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[v][c] = subgroup_sum(acc[v][c], A.s);
+  }
+  if (!item) {
+    if (L.g == 0) write_src<T, NV>(A, L, j, acc, SZ);
+    return;
+  }
+  const int H = A.s.H;
+  const int row_f = A.s.rv * V;
+  float* wsum = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H]
+  float* wacc = wsum + kWarps * H;                            // [kWarps][H * D]
+  if (L.g == 0)
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      if (!L.ok[v]) continue;
+#pragma unroll
+      for (int c = 0; c < V; ++c) wacc[wid * row_f + L.q[v] * V + c] = acc[v][c];
+      if (L.head_leader(A.s, v)) wsum[wid * H + L.k[v]] = SZ[v];
+    }
+  __syncthreads();
+  if (wid != 0 || L.g != 0) return;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    SZ[v] = 0.f;
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
+    if (!L.ok[v]) continue;
+    for (int w = 0; w < kWarps; ++w) {
+      SZ[v] += wsum[w * H + L.k[v]];
+#pragma unroll
+      for (int c = 0; c < V; ++c) acc[v][c] += wacc[w * row_f + L.q[v] * V + c];
+    }
+  }
+  if (slot < 0) {
+    write_src<T, NV>(A, L, j, acc, SZ);
+    return;
+  }
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    if (!L.ok[v]) continue;
+    float* pa = A.src_acc + int64_t(slot) * row_f + L.q[v] * V;
+#pragma unroll
+    for (int c4 = 0; c4 < V; c4 += 4)
+      *reinterpret_cast<float4*>(pa + c4) =
+          make_float4(acc[v][c4], acc[v][c4 + 1], acc[v][c4 + 2], acc[v][c4 + 3]);
+    if (L.head_leader(A.s, v)) A.src_sum[int64_t(slot) * H + L.k[v]] = SZ[v];
+  }
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads) bwd_src_merge(const BwdArgs A) {
+  constexpr int V = VecOf<T>::n;
+  const Lane<NV> L(A.s);
+  const int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (t >= A.csc.n_hubs || L.g != 0) return;
+  const int4 hb = A.csc.hubs[t];
+  const int H = A.s.H;
+  const int row_f = A.s.rv * V;
+  float acc[NV][V], SZ[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    SZ[v] = 0.f;
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
+    if (!L.ok[v]) continue;
+    for (int c = 0; c < hb.z; ++c) {
+      const int64_t slot = int64_t(hb.y) + c;
+      SZ[v] += A.src_sum[slot * H + L.k[v]];
+      const float* pa = A.src_acc + slot * row_f + L.q[v] * V;
+#pragma unroll
+      for (int c4 = 0; c4 < V; c4 += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(pa + c4);
+        acc[v][c4] += q.x;
+        acc[v][c4 + 1] += q.y;
+        acc[v][c4 + 2] += q.z;
+        acc[v][c4 + 3] += q.w;
+      }
+    }
+  }
+  write_src<T, NV>(A, L, hb.x, acc, SZ);
+}
+
+// ---------------------------------------------------------------------------
+// attention-vector gradients
+// ---------------------------------------------------------------------------
+
+// Block b sums ds_src(n) h_n and ds_dst(n) h_n over its nodes n = b, b + B,
+// ... (per sub-group: every G-th of them) in float32, then folds its warps'
+// and sub-groups' sums in float64 in a fixed order into da_part[b].
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads) da_partial(const BwdArgs A) {
+  constexpr int V = VecOf<T>::n;
+  const Lane<NV> L(A.s);
+  const int wid = threadIdx.x >> 5;
+  const int H = A.s.H;
+  const int row_f = A.s.rv * V;
+  float s_acc[NV][V], d_acc[NV][V];
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int c = 0; c < V; ++c) s_acc[v][c] = d_acc[v][c] = 0.f;
+  const int64_t lanes_per_step = int64_t(A.da_blocks) * kWarps * L.G;
+  for (int64_t n = (int64_t(blockIdx.x) * kWarps + wid) * L.G + L.g; n < A.n; n += lanes_per_step) {
+    float x[NV][V];
+    load_row<T, NV>(A.h, n, A.s, L, x);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      if (!L.ok[v]) continue;
+      const float ds = A.ds_src[n * H + L.k[v]];
+      const float dd = A.stats[n * H + L.k[v]].w;
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        s_acc[v][c] = fmaf(ds, x[v][c], s_acc[v][c]);
+        d_acc[v][c] = fmaf(dd, x[v][c], d_acc[v][c]);
+      }
+    }
+  }
+  extern __shared__ __align__(16) unsigned char smem[];
+  float* buf = reinterpret_cast<float*>(smem);  // [kWarps * G][2][row_f]
+  const int sub = wid * L.G + L.g;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    if (!L.ok[v]) continue;
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+      buf[(sub * 2 + 0) * row_f + L.q[v] * V + c] = s_acc[v][c];
+      buf[(sub * 2 + 1) * row_f + L.q[v] * V + c] = d_acc[v][c];
+    }
+  }
+  __syncthreads();
+  const int nsub = kWarps * L.G;
+  for (int t = threadIdx.x; t < 2 * row_f; t += blockDim.x) {
+    const int which = t / row_f, e = t - which * row_f;
+    double s = 0.0;
+    for (int q = 0; q < nsub; ++q) s += double(buf[(q * 2 + which) * row_f + e]);
+    A.da_part[int64_t(blockIdx.x) * 2 * row_f + t] = s;
+  }
+}
+
+__global__ void da_final(const double* part, int blocks, int row_f, float* da_src, float* da_dst) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= 2 * row_f) return;
+  double s = 0.0;
+  for (int b = 0; b < blocks; ++b) s += part[int64_t(b) * 2 * row_f + t];
+  if (t < row_f)
+    da_src[t] = float(s);
+  else
+    da_dst[t - row_f] = float(s);
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+}
+
+template <typename T, int NV>
+cudaError_t launch_t(const BwdArgs& A, cudaStream_t st, const cudaEvent_t* ev) {
+  constexpr int V = VecOf<T>::n;
+  const int H = A.s.H, row_f = A.s.rv * V;
+  cudaError_t e;
+  auto mark = [&](int k) {
+    if (ev) cudaEventRecord(ev[k], st);
+  };
+  mark(0);
+  // pass 1
+  {
+    const int64_t blocks = A.csr.n_items + (A.csr.n_light + kWarps - 1) / kWarps;
+    const size_t smem = size_t(A.csr.col_off) + size_t(kWarps) * H * 3 * 4;
+    if (blocks > 0) {
+      if ((e = set_smem(bwd_dst_main<T, NV>, smem)) != cudaSuccess) return e;
+      bwd_dst_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    mark(1);
+    if (A.csr.n_hubs > 0) {
+      bwd_dst_merge<T, NV><<<unsigned((A.csr.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    mark(2);
+  }
+  // pass 2
+  {
+    const int64_t blocks = A.csc.n_items + (A.csc.n_light + kWarps - 1) / kWarps;
+    const size_t smem = size_t(A.csc.col_off) + size_t(kWarps) * (H + row_f) * 4;
+    if (blocks > 0) {
+      if ((e = set_smem(bwd_src_main<T, NV>, smem)) != cudaSuccess) return e;
+      bwd_src_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    mark(3);
+    if (A.csc.n_hubs > 0) {
+      bwd_src_merge<T, NV><<<unsigned((A.csc.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    mark(4);
+  }
+  // attention-vector gradients
+  {
+    const size_t smem = size_t(kWarps) * (32 / A.s.lpr) * 2 * row_f * 4;
+    if ((e = set_smem(da_partial<T, NV>, smem)) != cudaSuccess) return e;
+    da_partial<T, NV><<<unsigned(A.da_blocks), kThreads, smem, st>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark(5);
+    da_final<<<unsigned((2 * row_f + 127) / 128), 128, 0, st>>>(A.da_part, A.da_blocks, row_f,
+                                                                A.da_src, A.da_dst);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark(6);
+  }
+  return cudaGetLastError();
+}
+
+DirArgs dir_args(const Dir& d) {
+  DirArgs a{};
+  a.ptr = d.ptr;
+  a.idx = d.idx;
+  a.light = d.light;
+  a.n_light = d.n_light;
+  a.items = d.items;
+  a.n_items = d.n_items;
+  a.hubs = d.hubs;
+  a.n_hubs = d.n_hubs;
+  a.col_off = int(16 + align_up(size_t(d.max_item + 4) * 4, 16));
+  return a;
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt, const void* h,
+                            const float* a_src, const float* a_dst, float slope,
+                            const float* lse, const void* dout, void* dh, float* da_src,
+                            float* da_dst, char* ws, const WsLayout& L, cudaStream_t st,
+                            const cudaEvent_t* ev) {
+  BwdArgs A{};
+  A.s = s;
+  A.csr = dir_args(g->csr);
+  A.csc = dir_args(g->csc);
+  A.n = g->n;
+  A.h = h;
+  A.a_src = a_src;
+  A.a_dst = a_dst;
+  A.slope = slope;
+  A.lse = lse;
+  A.dout = dout;
+  A.dh = dh;
+  A.da_src = da_src;
+  A.da_dst = da_dst;
+  A.stats = reinterpret_cast<float4*>(ws + L.stats);
+  A.ds_src = reinterpret_cast<float*>(ws + L.ds_src);
+  A.dst_part = reinterpret_cast<float4*>(ws + L.dst_part);
+  A.src_acc = reinterpret_cast<float*>(ws + L.src_acc);
+  A.src_sum = reinterpret_cast<float*>(ws + L.src_sum);
+  A.da_part = reinterpret_cast<double*>(ws + L.da_part);
+  A.da_blocks = L.da_blocks;
+  A.err = g->err;
+  if (dt == GNN_F32) {
+    switch (s.nv) {
+      case 1: return launch_t<float, 1>(A, st, ev);
+      case 2: return launch_t<float, 2>(A, st, ev);
+      case 4: return launch_t<float, 4>(A, st, ev);
+    }
+  } else {
+    switch (s.nv) {
+      case 1: return launch_t<__nv_bfloat16, 1>(A, st, ev);
+      case 2: return launch_t<__nv_bfloat16, 2>(A, st, ev);
+      case 4: return launch_t<__nv_bfloat16, 4>(A, st, ev);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gnn

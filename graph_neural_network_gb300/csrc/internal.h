@@ -1,0 +1,88 @@
+// Internal structures shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gnnagg.h"
+
+namespace gnn {
+
+// Device status word bits.
+enum : int32_t {
+  DEVERR_BAD_ROW_PTR = 1 << 0,  // row_ptr[0] != 0, decreasing, or row_ptr[N] != E
+  DEVERR_BAD_COL = 1 << 1,      // col_idx outside [0, N)
+  DEVERR_TIMEOUT = 1 << 4,      // a bounded mbarrier wait ran out
+  DEVERR_INTERNAL = 1 << 5,     // an internal consistency check failed
+};
+
+// One direction of the adjacency with its degree buckets.
+//   CSR: ptr/idx = caller's row_ptr/col_idx, grouped by destination (in-edges)
+//   CSC: ptr/idx = transpose built by prepare, grouped by source (out-edges)
+// items: {node, begin, end, slot}; slot >= 0 marks one chunk of a hub (its
+// partial state goes to workspace slot `slot`), slot < 0 a whole mid node.
+// Hub chunks come first (ascending node, then chunk), then mid nodes.
+// hubs: {node, first_slot, n_chunks, 0}.
+struct Dir {
+  const int32_t* ptr = nullptr;
+  const int32_t* idx = nullptr;
+  int32_t* light = nullptr;
+  int4* items = nullptr;
+  int4* hubs = nullptr;
+  int64_t n_light = 0, n_items = 0, n_hubs = 0, n_hub_chunks = 0;
+  int32_t max_deg = 0, max_item = 0;
+};
+
+}  // namespace gnn
+
+struct gnn_graph {
+  int64_t n = 0, e = 0;
+  gnn_tiling tiling{};
+  gnn::Dir csr, csc;
+  int32_t* err = nullptr;  // device status word (in the caller's buffer)
+  int device = 0;
+};
+
+namespace gnn {
+
+// Per-call shape of the feature rows.
+struct Shape {
+  int H = 0, D = 0;
+  int esize = 0;  // bytes per element
+  int rv = 0;     // 16-byte vectors per row (H * D * esize / 16)
+  int hv = 0;     // 16-byte vectors per head (power of two, <= 32)
+  int lpr = 0;    // lanes per row (power of two, <= 32)
+  int nv = 0;     // vectors per lane (1, 2 or 4)
+};
+
+// Workspace layout of one call (byte offsets into ws, 256-aligned).
+struct WsLayout {
+  size_t fwd_acc = 0, fwd_ml = 0, fwd_total = 0;
+  size_t stats = 0, ds_src = 0, dst_part = 0, src_acc = 0, src_sum = 0, da_part = 0, bwd_total = 0;
+  int da_blocks = 0;
+};
+
+bool make_shape(int H, int D, gnn_dtype dt, Shape* s);
+WsLayout ws_layout(const gnn_graph* g, const Shape& s);
+
+// Kernel launchers (gat_fwd.cu, gat_bwd.cu); return the launch error.
+cudaError_t launch_forward(const gnn_graph* g, const Shape& s, gnn_dtype dt, const void* h,
+                           const float* a_src, const float* a_dst, float slope, void* out,
+                           float* lse, char* ws, const WsLayout& L, cudaStream_t st,
+                           const cudaEvent_t* ev);
+cudaError_t launch_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt, const void* h,
+                            const float* a_src, const float* a_dst, float slope,
+                            const float* lse, const void* dout, void* dh, float* da_src,
+                            float* da_dst, char* ws, const WsLayout& L, cudaStream_t st,
+                            const cudaEvent_t* ev);
+
+// Graph preparation (prepare.cu).
+gnn_status prepare_graph(gnn_graph* g, const int32_t* row_ptr, const int32_t* col,
+                         char* buffer, size_t buffer_bytes, char* scratch, size_t scratch_bytes,
+                         cudaStream_t st);
+size_t graph_buffer_bytes(int64_t n, int64_t e, const gnn_tiling& t);
+size_t graph_scratch_bytes(int64_t n, int64_t e);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace gnn

@@ -1,0 +1,197 @@
+/*
+ * gnnagg.h -- IO-aware fused GAT neighbour aggregation for one GPU (sm_103a).
+ *
+ * The operation.  For a directed graph in CSR form (row i lists the sources j
+ * of the edges j -> i) and node features h[N][H][D] (H heads of width D), each
+ * destination i and head k gets
+ *
+ *     e_ij   = LeakyReLU(a_dst[k] . h_i[k] + a_src[k] . h_j[k])
+ *     alpha  = softmax over the in-neighbours j of i of e_ij
+ *     out_i[k] = sum_j alpha_ij h_j[k],   lse_i[k] = log sum_j exp(e_ij)
+ *
+ * The score is the additive attention of Graph Attention Networks (Velickovic
+ * et al., ICLR 2018, eqs. 1-3) with the projection W applied by the caller.
+ * Following "On Efficient Scaling of GNNs via IO-Aware Layers Implementations"
+ * (Technical Summary > Methodology, attention-based layers), the forward pass
+ * computes scores, softmax and aggregation in one streaming pass over each
+ * node's neighbours with an online softmax, so no per-edge score, weight or
+ * message is ever written to device memory; it keeps the per-node
+ * log-sum-exp, from which the backward pass recomputes alpha on the fly.
+ * The backward pass walks the CSR for the destination-side gradient terms
+ * and a cached transposed adjacency (CSC, built once per graph; same page,
+ * SpMM bullet: transposed adjacency cached for the backward pass) for the
+ * source-side terms.  Degree-aware tiling (same page, reduction bullet:
+ * light and heavy nodes split by a degree threshold, heavy nodes tiled over
+ * edge chunks) assigns a warp to each light node, a thread block to each
+ * mid-degree node and several thread blocks to each hub, whose partial
+ * (max, sum, accumulator) states are merged in a fixed order.  Results are
+ * bitwise reproducible run to run.
+ *
+ * Conventions.
+ *   - Every pointer argument named *_d or listed as "device" is a device
+ *     pointer on the current device; all device memory is owned by the
+ *     caller.  The library keeps only a small host-side struct per graph.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Compute calls are asynchronous on that stream and never synchronise,
+ *     except gnn_graph_prepare (two synchronisations) and
+ *     gnn_check_device_error (one).
+ *   - Feature layout: h, out, dout, dh are [N][H][D] row-major, contiguous,
+ *     of the given dtype; lse is float [N][H] (natural log, -inf for a node
+ *     with no in-neighbours); a_src, a_dst, da_src, da_dst are float [H][D].
+ *   - Supported shapes: D * sizeof(dtype) a multiple of 16 bytes with
+ *     D * sizeof(dtype) / 16 a power of two no larger than 32, and
+ *     H * D * sizeof(dtype) <= 2048 bytes.  Others return GNN_ERR_UNSUPPORTED.
+ *   - h, out, dout, dh, a_src, a_dst must be 16-byte aligned, the workspace
+ *     256-byte aligned, col_idx 16-byte aligned.
+ *   - Multi-edges count with their multiplicity.  The library adds no
+ *     self-loops.  n_edges must be below 2^31.
+ *   - Errors never abort, trap or print; every call returns a gnn_status.
+ */
+#ifndef GNNAGG_H_
+#define GNNAGG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GNNAGG_ABI_VERSION 1
+
+typedef enum {
+  GNN_OK = 0,
+  GNN_ERR_INVALID_ARG = 1,        /* null/misaligned pointer, bad size, bad enum */
+  GNN_ERR_UNSUPPORTED = 2,        /* (H, D, dtype) outside the supported set */
+  GNN_ERR_INVALID_GRAPH = 3,      /* CSR failed validation in gnn_graph_prepare */
+  GNN_ERR_WORKSPACE_TOO_SMALL = 4,
+  GNN_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
+  GNN_ERR_DEVICE_ASSERT = 6,      /* a kernel recorded an internal consistency error */
+  GNN_ERR_TIMEOUT = 7             /* a kernel gave up a bounded wait (see gnn_check_device_error) */
+} gnn_status;
+
+typedef enum { GNN_F32 = 0, GNN_BF16 = 1 } gnn_dtype;
+
+/* Degree-aware tiling thresholds (in edges).  A node of in-degree (CSR) or
+ * out-degree (CSC) d is "light" when d <= light_max_deg and gets one warp;
+ * "mid" when light_max_deg < d <= cta_max_deg and gets one thread block;
+ * a "hub" otherwise, split into chunks of hub_chunk edges, one thread block
+ * each.  Constraints: 0 <= light_max_deg <= cta_max_deg <= 16384,
+ * 1 <= hub_chunk <= 16384. */
+typedef struct {
+  int32_t light_max_deg;
+  int32_t cta_max_deg;
+  int32_t hub_chunk;
+} gnn_tiling;
+
+/* Fills *t with the default thresholds. */
+void gnn_default_tiling(gnn_tiling* t);
+
+typedef struct gnn_graph gnn_graph; /* opaque; immutable after prepare */
+
+/* Bytes of caller-owned device memory the prepared graph keeps (CSC
+ * transpose, degree buckets, hub chunk tables, status word).  An upper bound
+ * computed from sizes only; tiling NULL = defaults.  Returns 0 for invalid
+ * sizes. */
+size_t gnn_graph_buffer_bytes(int64_t n_nodes, int64_t n_edges, const gnn_tiling* tiling);
+
+/* Bytes of temporary device memory gnn_graph_prepare needs during the call
+ * (radix-sort ping-pong buffers, degree arrays, scan partials). */
+size_t gnn_graph_scratch_bytes(int64_t n_nodes, int64_t n_edges);
+
+/* Validate a CSR graph and build everything the aggregation kernels read.
+ *   row_ptr_d [n_nodes + 1], col_idx_d [n_edges]: device, int32; must stay
+ *     alive and unchanged for the lifetime of *out (they are read, not copied).
+ *   buffer_d / buffer_bytes: device memory that holds the prepared structures
+ *     for the lifetime of *out (>= gnn_graph_buffer_bytes, 256-byte aligned).
+ *   scratch_d / scratch_bytes: device memory used only during this call
+ *     (>= gnn_graph_scratch_bytes, 256-byte aligned).
+ *   tiling: NULL = defaults.
+ * Validation: row_ptr[0] = 0, non-decreasing, row_ptr[n] = n_edges, every
+ * col_idx in [0, n_nodes); a failure returns GNN_ERR_INVALID_GRAPH.  The CSC
+ * lists each column's rows in ascending order (deterministic).  The call
+ * synchronises `stream` twice (after validation, and to read bucket counts).
+ * On success *out receives a handle owned by the caller (gnn_graph_destroy). */
+gnn_status gnn_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t* row_ptr_d,
+                             const int32_t* col_idx_d, void* buffer_d, size_t buffer_bytes,
+                             void* scratch_d, size_t scratch_bytes, const gnn_tiling* tiling,
+                             void* stream, gnn_graph** out);
+
+/* Frees the host-side handle only (the device buffer belongs to the caller). */
+gnn_status gnn_graph_destroy(gnn_graph* g);
+
+/* Host-side counts recorded by prepare, 16 int64 values:
+ *   [0] n_nodes [1] n_edges
+ *   [2..7]  CSR (by in-degree):  light nodes, block items, hubs, hub chunks,
+ *           max in-degree, longest block item
+ *   [8..13] CSC (by out-degree): the same six
+ *   [14] light_max_deg [15] cta_max_deg
+ * n must be >= 16. */
+gnn_status gnn_graph_stats(const gnn_graph* g, int64_t* stats, int n);
+
+/* Device pointers of the prepared structures, for inspection and tests.
+ * ptrs[8] receives: CSC col_ptr [N+1], CSC row_idx [E] (int32); CSR light
+ * list [light], CSR block items [items] (int4 {node, begin, end, slot}), CSR
+ * hubs [hubs] (int4 {node, first slot, chunks, 0}); CSC light, items, hubs.
+ * Counts are those of gnn_graph_stats.  All lie inside the caller's buffer. */
+gnn_status gnn_graph_arrays(const gnn_graph* g, const void** ptrs, int n);
+
+/* Device memory the compute calls need as workspace, for either pass (the
+ * larger of the two), 256-byte aligned sizes.  Grows with the number of hub
+ * chunks and with N * H, never with E * H.  Returns 0 for unsupported shapes. */
+size_t gat_agg_workspace_bytes(const gnn_graph* g, int H, int D, gnn_dtype dtype);
+
+/* Forward pass.  Writes every element of out [N][H][D] (dtype) and lse
+ * [N][H] (float).  h [N][H][D] dtype, a_src/a_dst [H][D] float, all device.
+ * slope: LeakyReLU negative slope.  ws: device workspace of ws_bytes bytes
+ * (>= gat_agg_workspace_bytes; may be NULL when that is 0).
+ * Asynchronous; returns GNN_ERR_CUDA on a launch failure. */
+gnn_status gat_agg_forward(const gnn_graph* g, int H, int D, gnn_dtype dtype, const void* h,
+                           const float* a_src, const float* a_dst, float slope, void* out,
+                           float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward pass of L(out) given dout = dL/dout [N][H][D] (dtype) and the lse
+ * [N][H] written by gat_agg_forward on the same inputs.  Writes every element
+ * of dh [N][H][D] (dtype), da_src and da_dst [H][D] (float): nothing is
+ * accumulated into, so no output needs zeroing.  alpha is recomputed from
+ * lse; the only intermediates are O(N * H) per-node statistics and the hub
+ * partials in ws.  Asynchronous. */
+gnn_status gat_agg_backward(const gnn_graph* g, int H, int D, gnn_dtype dtype, const void* h,
+                            const float* a_src, const float* a_dst, float slope,
+                            const float* lse, const void* dout, void* dh, float* da_src,
+                            float* da_dst, void* ws, size_t ws_bytes, void* stream);
+
+/* gat_agg_forward / gat_agg_backward that also record the caller's CUDA
+ * events (cudaEvent_t passed as void*) on `stream` between their kernels, for
+ * per-kernel timing.  Forward: n_events = 3 -- before the main kernel, after
+ * it, after the hub merge.  Backward: n_events = 7 -- before the
+ * destination-side pass, after its main kernel, after its hub merge, after
+ * the source-side main kernel, after its hub merge, after the
+ * attention-vector partial sums, at the end.  A kernel with no work records
+ * its events back to back.  Other behaviour as the untimed calls. */
+gnn_status gat_agg_forward_timed(const gnn_graph* g, int H, int D, gnn_dtype dtype, const void* h,
+                                 const float* a_src, const float* a_dst, float slope, void* out,
+                                 float* lse, void* ws, size_t ws_bytes, void* stream,
+                                 void* const* events, int n_events);
+gnn_status gat_agg_backward_timed(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                                  const void* h, const float* a_src, const float* a_dst,
+                                  float slope, const float* lse, const void* dout, void* dh,
+                                  float* da_src, float* da_dst, void* ws, size_t ws_bytes,
+                                  void* stream, void* const* events, int n_events);
+
+/* Synchronises `stream`, reads and clears the graph's device status word.
+ * Returns GNN_OK, GNN_ERR_TIMEOUT (a bounded wait on an asynchronous copy ran
+ * out) or GNN_ERR_DEVICE_ASSERT; *info (may be NULL) receives the raw word. */
+gnn_status gnn_check_device_error(const gnn_graph* g, void* stream, int32_t* info);
+
+/* Static description of a status code. */
+const char* gnn_status_string(gnn_status s);
+
+/* GNNAGG_ABI_VERSION of the loaded library. */
+int gnn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GNNAGG_H_ */

@@ -1,0 +1,65 @@
+"""Error paths of the compute entry points (no fault is provoked: every case
+is rejected by the host-side checks before a kernel launches)."""
+import pytest
+import torch
+
+from workload import testgraphs
+from gpu_util import device_graph, make_case, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def setup():
+    rp, ci = testgraphs.with_in_degrees([3, 90, 2], n_nodes=200, seed=1)
+    case = make_case(rp, ci, 2, 16, "f32", 1)
+    return case, device_graph(case, (8, 64, 16))
+
+
+def test_unsupported_shapes(setup):
+    import graph_neural_network_gb300 as gnn
+    case, g = setup
+    for H, D, dt in [(2, 6, torch.float32), (2, 24, torch.bfloat16), (1, 256, torch.float32),
+                     (64, 16, torch.float32)]:
+        h = torch.zeros(g.n, H, D, dtype=dt, device="cuda")
+        with pytest.raises(gnn.GnnError) as ex:
+            gnn.gat_forward(g, h, torch.zeros(H, D, device="cuda"), torch.zeros(H, D, device="cuda"))
+        assert ex.value.status == 2
+
+
+def test_misaligned_features(setup):
+    import graph_neural_network_gb300 as gnn
+    case, g = setup
+    flat = torch.zeros(g.n * 2 * 16 + 1, device="cuda")
+    h = flat[1:].view(g.n, 2, 16)
+    with pytest.raises(gnn.GnnError) as ex:
+        gnn.gat_forward(g, h, torch.zeros(2, 16, device="cuda"), torch.zeros(2, 16, device="cuda"))
+    assert ex.value.status == 1
+
+
+def test_workspace_too_small(setup):
+    import graph_neural_network_gb300 as gnn
+    case, g = setup
+    h = to_device(case["h"], "f32")
+    a = torch.zeros(2, 16, device="cuda")
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    out, lse = gnn.gat_forward(g, h, a, a)
+    with pytest.raises(gnn.GnnError) as ex:
+        gnn.gat_backward(g, h, a, a, 0.2, lse, h, ws=small)
+    assert ex.value.status == 4
+
+
+def test_workspace_has_no_edge_by_head_term():
+    """Workspace grows with N * H and the hub chunks, never with E * H."""
+    import workload
+    rp, ci = workload.chung_lu(30_000, 2.1, 40.0, 5_000.0, 3)
+    case = make_case(rp, ci, 8, 16, "bf16", 3)
+    g = device_graph(case)
+    st = g.stats()
+    n, e, H, D = st["n"], st["e"], 8, 16
+    ws = g.workspace_bytes(H, D, torch.bfloat16)
+    blocks = min(1024, max(1, -(-n // 2048)))
+    bound = (20 * n * H + 16 * st["csr"]["hub_chunks"] * H
+             + 4 * st["csc"]["hub_chunks"] * H * (D + 1) + 16 * blocks * H * D + 8 * 256)
+    assert ws <= bound
+    assert ws < 4 * e * H / 2

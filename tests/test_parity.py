@@ -1,0 +1,130 @@
+"""CUDA path vs the fp64 oracle on the same seeded inputs, element by element:
+out, lse, dh, da_src, da_dst over every bucket path, shape and dtype."""
+import numpy as np
+import pytest
+import torch
+
+import workload
+from workload import testgraphs
+from gpu_util import compare, make_case, run_gpu, run_oracle, to_device, assert_close
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [  # (H, D, dtype): row vectors rv = H * D * size / 16
+    (1, 4, "f32"), (1, 16, "f32"), (3, 4, "f32"), (4, 32, "f32"), (2, 128, "f32"),
+    (8, 64, "f32"), (2, 8, "bf16"), (6, 8, "bf16"), (8, 16, "bf16"), (1, 128, "bf16"),
+    (4, 64, "bf16"), (12, 32, "bf16"), (1, 256, "bf16"),
+]
+TILINGS = [(64, 4096, 2048), (8, 64, 16), (0, 0, 1)]
+THRESHOLD_DEGREES = [0, 1, 2, 3, 7, 8, 9, 15, 16, 17, 63, 64, 65, 127, 128, 129, 257, 1000, 2049,
+                     4096, 4097]
+
+
+def test_config1_tiny_erdos_renyi():
+    w = workload.CONFIGS[1]
+    rp, ci = workload.make_graph(w)
+    case = make_case(rp, ci, w.H, w.D, w.dtype, w.seed, w.slope)
+    compare(run_gpu(case), run_oracle(case), w.dtype, what="cfg1")
+
+
+@pytest.mark.parametrize("tiling", TILINGS, ids=lambda t: "t%d_%d_%d" % t)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bucket_thresholds(tiling, dtype):
+    """In-degrees at every threshold +-1 (zero in-degree, multi-edges, hubs of
+    one, two and many chunks, ragged last chunks), Zipf sources so that the
+    CSC side has hubs too."""
+    rp, ci = testgraphs.with_in_degrees(THRESHOLD_DEGREES, n_nodes=2500, seed=7)
+    case = make_case(rp, ci, 4, 16 if dtype == "bf16" else 8, dtype, 11)
+    compare(run_gpu(case, tiling), run_oracle(case), dtype, what=f"thresholds {tiling}")
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "H%d_D%d_%s" % s)
+def test_shapes(shape):
+    H, D, dtype = shape
+    rp, ci = testgraphs.with_in_degrees([0, 5, 70, 300], n_nodes=700, seed=H * 100 + D)
+    case = make_case(rp, ci, H, D, dtype, 17)
+    compare(run_gpu(case, (8, 64, 16)), run_oracle(case), dtype, what=f"shape {shape}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_uniform_graph_default_tiling(dtype):
+    rp, ci = workload.uniform(20_000, 16, 5)
+    case = make_case(rp, ci, 4, 32 if dtype == "f32" else 64, dtype, 5)
+    compare(run_gpu(case), run_oracle(case), dtype, what="uniform")
+
+
+def test_power_law_default_tiling():
+    rp, ci = workload.chung_lu(50_000, 2.1, 20.0, 10_000.0, 13)
+    case = make_case(rp, ci, 8, 16, "bf16", 13)
+    compare(run_gpu(case), run_oracle(case), "bf16", what="chung-lu")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_single_neighbour_is_a_copy(dtype):
+    """One in-neighbour: alpha = 1 and out_i = h_j exactly (bitwise)."""
+    rp, ci = testgraphs.ring(1000)
+    case = make_case(rp, ci, 2, 32, dtype, 23)
+    gpu = run_gpu(case)
+    h = case["h"] if dtype == "f32" else workload.bf16_bits_to_f32(case["h"])
+    assert np.array_equal(gpu["out"], h[ci].astype(np.float64))
+    compare(gpu, run_oracle(case), dtype, what="ring")
+
+
+def test_equal_scores_give_the_mean():
+    rp, ci = testgraphs.with_in_degrees([1, 2, 3, 50, 5000], n_nodes=600, seed=29)
+    case = make_case(rp, ci, 2, 16, "f32", 29)
+    case["a_src"][:] = 0
+    case["a_dst"][:] = 0
+    gpu = run_gpu(case, (8, 64, 16))
+    deg = np.diff(rp)
+    ok = deg > 0
+    mean = np.add.reduceat(case["h"][ci].astype(np.float64), rp[:-1][ok], axis=0) / deg[ok][:, None, None]
+    assert_close(gpu["out"][ok], mean, "f32", None, "mean")
+    assert np.allclose(gpu["lse"][ok], np.log(deg[ok])[:, None], rtol=1e-6)
+
+
+def test_isolated_nodes_and_empty_edge_set():
+    rp, ci = testgraphs.isolated(50)
+    case = make_case(rp, ci, 2, 16, "f32", 31)
+    gpu = run_gpu(case)
+    assert np.all(gpu["out"] == 0.0) and np.all(np.isneginf(gpu["lse"]))
+    assert np.all(gpu["dh"] == 0.0)
+    assert np.all(gpu["da_src"] == 0.0) and np.all(gpu["da_dst"] == 0.0)
+
+
+@pytest.mark.parametrize("tiling", [(64, 4096, 2048), (8, 64, 16)], ids=str)
+def test_bitwise_deterministic(tiling):
+    rp, ci = testgraphs.with_in_degrees(THRESHOLD_DEGREES, n_nodes=3000, seed=37)
+    case = make_case(rp, ci, 4, 32, "bf16", 37)
+    a = run_gpu(case, tiling)
+    b = run_gpu(case, tiling)
+    for k in ("out", "lse", "dh", "da_src", "da_dst"):
+        assert np.array_equal(a[k], b[k], equal_nan=True), k
+
+
+def test_side_stream_matches_default_stream():
+    rp, ci = testgraphs.with_in_degrees(THRESHOLD_DEGREES, n_nodes=2000, seed=41)
+    case = make_case(rp, ci, 2, 32, "f32", 41)
+    a = run_gpu(case, (8, 64, 16))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = run_gpu(case, (8, 64, 16), stream=s)
+    for k in ("out", "lse", "dh", "da_src", "da_dst"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_autograd_function():
+    import graph_neural_network_gb300 as gnn
+    rp, ci = testgraphs.with_in_degrees([4, 90, 3], n_nodes=300, seed=43)
+    case = make_case(rp, ci, 2, 16, "f32", 43)
+    g = run_gpu(case, backward=False)["graph"]
+    h = to_device(case["h"], "f32").requires_grad_(True)
+    a_s = torch.from_numpy(case["a_src"]).cuda().requires_grad_(True)
+    a_d = torch.from_numpy(case["a_dst"]).cuda().requires_grad_(True)
+    out = gnn.GATAggregate.apply(g, h, a_s, a_d, 0.2)
+    out.backward(to_device(case["dout"], "f32"))
+    ref = run_oracle(case)
+    assert_close(out.detach().cpu().numpy(), ref["out"], "f32", ref["out_mag"], "autograd out")
+    assert_close(h.grad.cpu().numpy(), ref["dh"], "f32", ref["dh_mag"], "autograd dh")
+    assert_close(a_s.grad.cpu().numpy(), ref["da_src"], "f32", ref["da_src_mag"], "da_src")
+    assert_close(a_d.grad.cpu().numpy(), ref["da_dst"], "f32", ref["da_dst_mag"], "da_dst")
