@@ -50,6 +50,8 @@ def _bind(path: str):
     lib.oracle_gat_backward.restype = i32
     lib.oracle_gat_backward_rows.argtypes = common + [P, i64, P, P, P]
     lib.oracle_gat_backward_rows.restype = i32
+    lib.oracle_gat_att_grads.argtypes = common + [P, P, P, P]
+    lib.oracle_gat_att_grads.restype = i32
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     return lib
@@ -143,6 +145,22 @@ class Oracle:
                     da_src_mag=None if da_mag is None else da_mag[0],
                     da_dst_mag=None if da_mag is None else da_mag[1])
 
+    def att_grads(self, row_ptr, col, h, a_src, a_dst, slope, dout, with_mag=False):
+        """da_src, da_dst summed per destination row (parallel over rows)."""
+        row_ptr, col, h, a_src, a_dst, n, H, D, dt = _prep(row_ptr, col, h, a_src, a_dst)
+        dout = np.ascontiguousarray(dout)
+        assert dout.shape == h.shape and dout.dtype == h.dtype
+        da_src = np.empty((H, D), np.float64)
+        da_dst = np.empty((H, D), np.float64)
+        mag = np.empty((2, H, D), np.float64) if with_mag else None
+        rc = self.lib.oracle_gat_att_grads(n, _p(row_ptr), _p(col), H, D, dt, _p(h), _p(a_src),
+                                           _p(a_dst), float(slope), _p(dout), _p(da_src),
+                                           _p(da_dst), _p(mag))
+        _check(rc, "att_grads")
+        return dict(da_src=da_src, da_dst=da_dst,
+                    da_src_mag=None if mag is None else mag[0],
+                    da_dst_mag=None if mag is None else mag[1])
+
     def backward_rows(self, row_ptr, col, h, a_src, a_dst, slope, dout, sel, with_mag=False):
         """dh rows of the listed (distinct) nodes only, each from its neighbourhood."""
         row_ptr, col, h, a_src, a_dst, n, H, D, dt = _prep(row_ptr, col, h, a_src, a_dst)
@@ -195,6 +213,7 @@ def _sel(sel):
 
 
 _default = Oracle()
+att_grads = _default.att_grads
 num_threads = _default.num_threads
 forward = _default.forward
 node_stats = _default.node_stats

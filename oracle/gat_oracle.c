@@ -436,3 +436,82 @@ int oracle_gat_backward_rows(int64_t n, const int32_t* row_ptr, const int32_t* c
   free(target); free(cnt); free(fill); free(edge_dst); free(edge_pos);
   return 0;
 }
+
+/*
+ * Attention-vector gradients only, summed per destination row so the work
+ * parallelises over rows: da_src = sum_i sum_{j in N(i)} dz_ij h_j and
+ * da_dst = sum_i ds_dst(i) h_i.  (The same sums as oracle_gat_backward's,
+ * grouped by destination instead of by source.)  Rows are split statically
+ * over threads and the per-thread float64 sums are added in thread order.
+ * da_src, da_dst [H][D]; da_mag [2][H][D] may be NULL.
+ */
+int oracle_gat_att_grads(int64_t n, const int32_t* row_ptr, const int32_t* col, int H, int D,
+                         int dtype, const void* h, const double* a_src, const double* a_dst,
+                         double slope, const void* dout, double* da_src, double* da_dst,
+                         double* da_mag) {
+  gat_inputs g = {n, row_ptr, col, H, D, dtype, h, a_src, a_dst, slope};
+  int rc = check_inputs(&g);
+  if (rc) return rc;
+  if (!dout && n > 0) return 1;
+  const int64_t HD = (int64_t)H * D;
+  const int64_t maxdeg = max_in_degree(&g);
+  int nt = oracle_num_threads();
+  double* part = (double*)calloc((size_t)(nt * 4 * HD), sizeof(double));
+  if (!part) return 3;
+#pragma omp parallel num_threads(nt)
+  {
+    int t = 0;
+#ifdef _OPENMP
+    t = omp_get_thread_num();
+#endif
+    double* ps = part + (int64_t)t * 4 * HD; /* src, dst, src mag, dst mag */
+    double* z = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
+    double* alpha = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
+    double* da = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
+#pragma omp for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t b = row_ptr[i], deg = (int64_t)row_ptr[i + 1] - b;
+      if (deg == 0) continue;
+      for (int k = 0; k < H; ++k) {
+        double ds, mag;
+        row_softmax(&g, i, k, z, alpha);
+        const double dl = row_backward_stats(&g, dout, i, k, z, alpha, da, &ds, &mag);
+        for (int64_t q = 0; q < deg; ++q) {
+          const int64_t j = col[b + q];
+          const double dz = alpha[q] * (da[q] - dl) * leaky_grad(z[q], slope);
+          const double dm = alpha[q] * (fabs(da[q]) + fabs(dl));
+          for (int d = 0; d < D; ++d) {
+            const double x = feat(&g, h, j, k, d);
+            ps[k * D + d] += dz * x;
+            ps[2 * HD + k * D + d] += dm * fabs(x);
+          }
+        }
+        for (int d = 0; d < D; ++d) {
+          const double x = feat(&g, h, i, k, d);
+          ps[HD + k * D + d] += ds * x;
+          ps[3 * HD + k * D + d] += mag * fabs(x);
+        }
+      }
+    }
+    free(z);
+    free(alpha);
+    free(da);
+  }
+  for (int64_t x = 0; x < HD; ++x) {
+    double s = 0.0, d = 0.0, ms = 0.0, md = 0.0;
+    for (int t = 0; t < nt; ++t) {
+      s += part[(int64_t)t * 4 * HD + x];
+      d += part[(int64_t)t * 4 * HD + HD + x];
+      ms += part[(int64_t)t * 4 * HD + 2 * HD + x];
+      md += part[(int64_t)t * 4 * HD + 3 * HD + x];
+    }
+    da_src[x] = s;
+    da_dst[x] = d;
+    if (da_mag) {
+      da_mag[x] = ms;
+      da_mag[HD + x] = md;
+    }
+  }
+  free(part);
+  return 0;
+}

@@ -311,9 +311,13 @@ def pin_sampled_modes(o):
     f = o.forward(rp, ci, h, a_s, a_d, 0.2)
     fs = o.forward(rp, ci, h, a_s, a_d, 0.2, sel=sel)
     close(fs["out"], f["out"][sel], 1e-14, 0, "sampled out")
-    b = o.backward(rp, ci, h, a_s, a_d, 0.2, dout)
-    bs = o.backward_rows(rp, ci, h, a_s, a_d, 0.2, dout, sel)
+    b = o.backward(rp, ci, h, a_s, a_d, 0.2, dout, with_mag=True)
+    bs = o.backward_rows(rp, ci, h, a_s, a_d, 0.2, dout, sel, with_mag=True)
     close(bs["dh"], b["dh"][sel], 1e-12, 1e-13, "sampled dh")
+    close(bs["dh_mag"], b["dh_mag"][sel], 1e-12, 1e-13, "sampled dh_mag")
+    ag = o.att_grads(rp, ci, h, a_s, a_d, 0.2, dout, with_mag=True)
+    for k in ("da_src", "da_dst", "da_src_mag", "da_dst_mag"):
+        close(ag[k], b[k], 1e-12, 1e-13, "row-grouped " + k)
 
 
 def pin_bf16_inputs(o):
