@@ -38,6 +38,8 @@ SIGNATURES = [
                                      _P, _I32]),
     ("gat_agg_backward_timed", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _F, _P, _P, _P, _P, _P,
                                       _P, _SZ, _P, _P, _I32]),
+    ("gat_agg_forward_noalloc", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _F, _P, _P, _P]),
+    ("gat_agg_forward_noalloc_capacity", _SZ, []),
     ("gnn_check_device_error", _I32, [_P, _P, _P]),
     ("gnn_status_string", ctypes.c_char_p, [_I32]),
     ("gnn_abi_version", _I32, []),

@@ -179,6 +179,35 @@ gnn_status gat_agg_backward_timed(const gnn_graph* g, int H, int D, gnn_dtype dt
                                   float* da_src, float* da_dst, void* ws, size_t ws_bytes,
                                   void* stream, void* const* events, int n_events);
 
+/* Forward pass that allocates nothing and takes no workspace.  The page has
+ * no counterpart to this call; it exists for callers that must not allocate
+ * device memory -- for example code that runs under another framework's
+ * memory pool, an inference runtime with a static memory plan, or a
+ * latency-critical path where an allocation (and the synchronisation it can
+ * imply) is not allowed.  Such callers still pass h, a_src, a_dst, out and
+ * lse, exactly as for gat_agg_forward, and get the same results.
+ * The hub partial states that gat_agg_forward keeps in `ws` go instead to a
+ * fixed array inside this library of gat_agg_forward_noalloc_capacity()
+ * bytes (16 MiB) on each GPU that loads the library, held until the process
+ * exits.  A graph whose forward workspace (gat_agg_workspace_bytes' forward
+ * part: hub chunks * H * (D + 2) * 4 bytes) exceeds that size is rejected
+ * with GNN_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ * The first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture.  The device must be the one the
+ * graph was prepared on (else GNN_ERR_INVALID_ARG).
+ * Every call shares the one array: calls that overlap on the GPU (on
+ * different streams, or from several threads) race and must be serialised
+ * by the caller.  The array keeps the last call's contents; nothing in it
+ * needs to start at zero, as each call writes every partial before reading
+ * it. */
+gnn_status gat_agg_forward_noalloc(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                                   const void* h, const float* a_src, const float* a_dst,
+                                   float slope, void* out, float* lse, void* stream);
+
+/* Size in bytes of the array gat_agg_forward_noalloc uses. */
+size_t gat_agg_forward_noalloc_capacity(void);
+
 /* Synchronises `stream`, reads and clears the graph's device status word.
  * Returns GNN_OK, GNN_ERR_TIMEOUT (a bounded wait on an asynchronous copy ran
  * out) or GNN_ERR_DEVICE_ASSERT; *info (may be NULL) receives the raw word. */
