@@ -50,9 +50,11 @@ WsLayout ws_layout(const gnn_graph* g, const Shape& s) {
   L.dst_part = take(size_t(g->csr.n_hub_chunks) * s.H * 16);
   L.src_acc = take(size_t(g->csc.n_hub_chunks) * HD * 4);
   L.src_sum = take(size_t(g->csc.n_hub_chunks) * s.H * 4);
-  int64_t blocks = (g->n + 2047) / 2048;
+  // enough blocks to fill the GPU (8 per SM on 152 SMs), each summing at
+  // least 64 nodes per warp before its float64 fold
+  int64_t blocks = (g->n + 511) / 512;
   if (blocks < 1) blocks = 1;
-  if (blocks > 1024) blocks = 1024;
+  if (blocks > 1216) blocks = 1216;
   L.da_blocks = int(blocks);
   L.da_part = take(size_t(blocks) * 2 * HD * 8);
   L.bwd_total = off;

@@ -60,7 +60,7 @@ def device_graph(case, tiling=None, stream=None):
     return gnn.Graph(rp, ci, t, stream=stream)
 
 
-def run_gpu(case, tiling=None, backward=True, stream=None, graph=None):
+def run_gpu(case, tiling=None, backward=True, stream=None, graph=None, fetch=True):
     import graph_neural_network_gb300 as gnn
     g = graph if graph is not None else device_graph(case, tiling, stream)
     h = to_device(case["h"], case["dtype"])
@@ -74,6 +74,8 @@ def run_gpu(case, tiling=None, backward=True, stream=None, graph=None):
         res.update(dh_t=dh, da_src_t=da_s, da_dst_t=da_d)
     torch.cuda.synchronize()
     gnn.check_device_error(g)
+    if not fetch:
+        return res
     res["out"] = to_f64(out)
     res["lse"] = to_f64(lse)
     if backward:

@@ -58,7 +58,7 @@ def test_workspace_has_no_edge_by_head_term():
     st = g.stats()
     n, e, H, D = st["n"], st["e"], 8, 16
     ws = g.workspace_bytes(H, D, torch.bfloat16)
-    blocks = min(1024, max(1, -(-n // 2048)))
+    blocks = min(1216, max(1, -(-n // 512)))
     bound = (20 * n * H + 16 * st["csr"]["hub_chunks"] * H
              + 4 * st["csc"]["hub_chunks"] * H * (D + 1) + 16 * blocks * H * D + 8 * 256)
     assert ws <= bound

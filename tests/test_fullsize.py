@@ -1,0 +1,56 @@
+"""Full-size workloads, in the launch configuration bench.py times (default
+tiling): sampled outputs against the oracle computed node by node, and the
+attention-vector gradients against the oracle's row-parallel sum."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workload
+from gpu_util import assert_close, run_gpu, to_f64
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _rows(t, sel):
+    return to_f64(t[torch.from_numpy(np.asarray(sel, np.int64)).to(t.device)])
+
+
+def _backward_cost(rp, ci):
+    """Edge visits the per-node oracle makes for dh_j: sum of the in-degrees
+    of j's out-neighbours."""
+    indeg = np.diff(rp).astype(np.float64)
+    dst = np.repeat(np.arange(len(rp) - 1), np.diff(rp))
+    return np.bincount(ci, weights=indeg[dst], minlength=len(rp) - 1)
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4, 5, 6])
+def test_full_size_sampled_parity(idx):
+    w = workload.CONFIGS[idx]
+    rp, ci = workload.make_graph(w)
+    n = len(rp) - 1
+    h, a_s, a_d, dout = workload.make_features(w, n)
+    case = dict(row_ptr=rp, col=ci, h=h, dout=dout, a_src=a_s, a_dst=a_d, H=w.H, D=w.D,
+                dtype=w.dtype, slope=w.slope)
+    gpu = run_gpu(case, fetch=False)
+    rng = np.random.default_rng(1000 + idx)
+    indeg = np.diff(rp)
+    outdeg = np.bincount(ci, minlength=n)
+    # forward: random nodes, the largest in-degrees (hub split + merge), ragged tail
+    sel_f = np.unique(np.concatenate([rng.choice(n, 3000, replace=False),
+                                      np.argsort(indeg)[-64:], np.arange(n - 17, n)]))
+    f = oracle.forward(rp, ci, h, a_s, a_d, w.slope, sel=sel_f, with_mag=True)
+    assert_close(_rows(gpu["out_t"], sel_f), f["out"], w.dtype, f["out_mag"], f"cfg{idx} out")
+    assert_close(_rows(gpu["lse_t"], sel_f), f["lse"], w.dtype, None, f"cfg{idx} lse")
+    # backward rows: random nodes plus the largest out-degrees the oracle can afford
+    cost = _backward_cost(rp, ci)
+    cheap = np.nonzero(cost < 2e5)[0]
+    top = [j for j in np.argsort(outdeg)[::-1][:400] if cost[j] < 3e7][:24]
+    sel_b = np.unique(np.concatenate([rng.choice(cheap, min(400, len(cheap)), replace=False),
+                                      np.asarray(top, np.int64)]))
+    b = oracle.backward_rows(rp, ci, h, a_s, a_d, w.slope, dout, sel_b, with_mag=True)
+    assert_close(_rows(gpu["dh_t"], sel_b), b["dh"], w.dtype, b["dh_mag"], f"cfg{idx} dh")
+    ag = oracle.att_grads(rp, ci, h, a_s, a_d, w.slope, dout, with_mag=True)
+    assert_close(to_f64(gpu["da_src_t"]), ag["da_src"], w.dtype, ag["da_src_mag"], "da_src")
+    assert_close(to_f64(gpu["da_dst_t"]), ag["da_dst"], w.dtype, ag["da_dst_mag"], "da_dst")
+    assert outdeg[top].max() > 4096 or idx == 2      # the CSC hub path was sampled
