@@ -27,6 +27,10 @@ bool make_shape(int H, int D, gnn_dtype dt, Shape* s) {
     s->nv = (s->rv + 31) / 32;
     if (s->nv == 3) s->nv = 4;
   }
+  s->hv_log2 = 0;
+  while ((1 << s->hv_log2) < s->hv) ++s->hv_log2;
+  s->lpr_log2 = 0;
+  while ((1 << s->lpr_log2) < s->lpr) ++s->lpr_log2;
   return true;
 }
 
@@ -39,12 +43,14 @@ WsLayout ws_layout(const gnn_graph* g, const Shape& s) {
     off += align_up(bytes > 0 ? bytes : 1, 256);
     return r;
   };
-  // forward: hub chunk partials of the CSR direction
+  // forward: work counters, hub chunk partials of the CSR direction
+  L.fwd_ctr = take(kCounters * 4);
   L.fwd_acc = take(size_t(g->csr.n_hub_chunks) * HD * 4);
   L.fwd_ml = take(size_t(g->csr.n_hub_chunks) * s.H * 8);
   L.fwd_total = off;
   // backward
   off = 0;
+  L.bwd_ctr = take(kCounters * 4);
   L.stats = take(size_t(g->n) * s.H * 16);
   L.ds_src = take(size_t(g->n) * s.H * 4);
   L.dst_part = take(size_t(g->csr.n_hub_chunks) * s.H * 16);
@@ -155,7 +161,9 @@ gnn_status gnn_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t* ro
   g->n = n_nodes;
   g->e = n_edges;
   g->tiling = t;
-  if (cudaGetDevice(&g->device) != cudaSuccess) {
+  if (cudaGetDevice(&g->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&g->sm_count, cudaDevAttrMultiProcessorCount, g->device) !=
+          cudaSuccess) {
     delete g;
     return GNN_ERR_CUDA;
   }

@@ -116,6 +116,14 @@ __device__ __forceinline__ void st16(void* p, const uint4& v) {
   *reinterpret_cast<uint4*>(p) = v;
 }
 
+// 2^x with the SFU instruction (relative error about 2^-22; results below
+// 2^-126 flush to zero, which a softmax weight can ignore).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Sum over the `hv` consecutive lanes that hold one head (hv a power of two).
 __device__ __forceinline__ float head_sum(float v, int hv) {
 #pragma unroll
@@ -136,19 +144,19 @@ struct Lane {
   int k[NV];     // head of the vector
   __device__ __forceinline__ Lane(const Shape& s) {
     lane = threadIdx.x & 31;
-    g = lane / s.lpr;
-    G = 32 / s.lpr;
-    p = lane - g * s.lpr;
+    g = lane >> s.lpr_log2;
+    G = 32 >> s.lpr_log2;
+    p = lane & (s.lpr - 1);
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-      q[v] = p + s.lpr * v;
+      q[v] = p + (v << s.lpr_log2);
       ok[v] = q[v] < s.rv;
-      k[v] = ok[v] ? q[v] / s.hv : 0;
+      k[v] = ok[v] ? q[v] >> s.hv_log2 : 0;
     }
   }
   // lane writes the per-head scalar of vector v (one lane per head)
   __device__ __forceinline__ bool head_leader(const Shape& s, int v) const {
-    return ok[v] && (q[v] % s.hv) == 0;
+    return ok[v] && (q[v] & (s.hv - 1)) == 0;
   }
 };
 
@@ -249,40 +257,57 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int li
 
 constexpr int kWaitLimit = 1 << 20;
 
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Stage idx[beg, end) into shared memory `dst` (16-byte aligned) such that
 // element x lands at dst[x - (beg & ~3)].  The 16-byte-aligned interior moves
-// with one bulk copy; the ragged ends (< 4 elements each) with plain loads.
-// Must be called by all threads of the block; returns false (after recording
-// a timeout in *err) when the bulk copy did not complete within the limit.
+// with one bulk copy completing on `bar` (initialised once per kernel with
+// mbar_init(bar, 1); `parity` tracks its phase across calls); the ragged
+// ends (< 4 elements each) move with plain loads.  Must be called by all
+// threads of the block, after a __syncthreads that ends every read of the
+// previous contents.  Returns false (after recording a timeout in *err and
+// letting the copy land) when the bulk copy did not complete within the
+// limit.
 __device__ __forceinline__ bool stage_edges(int32_t* dst, const int32_t* idx, int beg, int end,
-                                            uint64_t* bar, int32_t* err) {
+                                            uint64_t* bar, uint32_t& parity, int32_t* err) {
   const int base = beg & ~3;
   const int a0 = (beg + 3) & ~3;
   const int a1 = end & ~3;
   const bool bulk = a1 > a0;
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
-    if (bulk) {
-      mbar_expect_tx(bar, uint32_t(a1 - a0) * 4u);
-      bulk_g2s(dst + (a0 - base), idx + a0, uint32_t(a1 - a0) * 4u, bar);
-    }
+  if (threadIdx.x == 0 && bulk) {
+    fence_proxy_async();  // earlier generic-proxy reads of dst come first
+    mbar_expect_tx(bar, uint32_t(a1 - a0) * 4u);
+    bulk_g2s(dst + (a0 - base), idx + a0, uint32_t(a1 - a0) * 4u, bar);
   }
   // ragged head and tail (or everything when the item is short)
   const int h1 = bulk ? a0 : end;
   for (int x = beg + int(threadIdx.x); x < h1; x += blockDim.x) dst[x - base] = __ldg(idx + x);
   if (bulk)
     for (int x = a1 + int(threadIdx.x); x < end; x += blockDim.x) dst[x - base] = __ldg(idx + x);
-  __syncthreads();  // barrier initialised before anyone waits on it
   bool timed_out = false;
-  if (bulk) timed_out = !mbar_wait(bar, 0, kWaitLimit);
+  if (bulk) timed_out = !mbar_wait(bar, parity, kWaitLimit);
   if (__syncthreads_or(timed_out)) {
     if (threadIdx.x == 0) {
       atomicOr(err, DEVERR_TIMEOUT);
-      mbar_wait(bar, 0, kWaitLimit);  // let the copy land before the block exits
+      mbar_wait(bar, parity, kWaitLimit);  // let the copy land before the block exits
     }
     return false;
   }
+  if (bulk) parity ^= 1u;
   return true;
+}
+
+// Number of persistent blocks for a kernel: what fits on every SM at once.
+template <typename K>
+__host__ int persistent_blocks(K kernel, size_t smem, int sm_count) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  return per_sm * (sm_count > 0 ? sm_count : 1);
 }
 
 }  // namespace gnn

@@ -59,8 +59,24 @@ struct BwdArgs {
   float* src_sum;    // [CSC hub chunks][H]
   double* da_part;   // [da blocks][2][H * D]
   int da_blocks;
+  int* ctr;          // work counters: [0], [1] pass 1 items / light; [2], [3] pass 2
   int32_t* err;
 };
+
+constexpr int kGrab = 4;  // light nodes a warp takes per counter access
+
+// Sources (or destinations) of the batch of edges starting at beg that this
+// lane's sub-group takes (edges beg + g, beg + g + G, ... below end; -1 past
+// the end).
+template <int U>
+__device__ __forceinline__ void batch_ids(const int32_t* cols, int colbase, int beg, int end,
+                                          int g, int G, int (&j)[U]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = beg + u * G + g;
+    j[u] = e < end ? cols[e - colbase] : -1;
+  }
+}
 
 __device__ __forceinline__ float leaky(float z, float slope) { return z > 0.f ? z : slope * z; }
 __device__ __forceinline__ float leaky_grad(float z, float slope) { return z > 0.f ? 1.f : slope; }
@@ -78,6 +94,7 @@ __device__ __forceinline__ float subgroup_sum(float x, const Shape& s) {
 template <typename T, int NV>
 __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
+                                          int (&jn)[kUnroll],
                                           const float (&as2)[NV][VecOf<T>::n],
                                           const float (&gi)[NV][VecOf<T>::n],
                                           const float (&sd2)[NV], const float (&lse2)[NV],
@@ -85,23 +102,10 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
   const int step = L.G * U;
-  int jn[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int e = beg + u * L.G + L.g;
-    jn[u] = e < end ? cols[e - colbase] : -1;
-  }
   for (int base = beg; base < end; base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
-    if (base + step < end) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = base + step + u * L.G + L.g;
-        jn[u] = e < end ? cols[e - colbase] : -1;
-      }
-    }
     uint4 raw[U][NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -109,6 +113,7 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
       for (int v = 0; v < NV; ++v)
         raw[u][v] = (j[u] >= 0 && L.ok[v]) ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v])
                                            : make_uint4(0, 0, 0, 0);
+    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
     float ss[U][NV], dd[U][NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -131,7 +136,7 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
       for (int v = 0; v < NV; ++v) {
         const float z = sd2[v] + head_sum(ss[u][v], A.s.hv);
         const float da = head_sum(dd[u][v], A.s.hv);
-        const float al = j[u] >= 0 ? exp2f(leaky(z, A.slope) - lse2[v]) : 0.f;
+        const float al = j[u] >= 0 ? ex2(leaky(z, A.slope) - lse2[v]) : 0.f;
         const float g = leaky_grad(z, A.slope);
         const float ad = al * da;
         SA[v] = fmaf(ad, g, SA[v]);
@@ -141,92 +146,135 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
   }
 }
 
+// Destination-side sums of node i over its edges [beg, end) taken by this
+// warp (jn: sources of the first batch), summed over the warp's sub-groups.
 template <typename T, int NV>
-__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_dst_main(const BwdArgs A) {
+__device__ __forceinline__ void dst_node(const BwdArgs& A, const Lane<NV>& L, int i,
+                                         const int32_t* cols, int colbase, int beg, int end,
+                                         int (&jn)[kUnroll],
+                                         const float (&as2)[NV][VecOf<T>::n],
+                                         const float (&ad2)[NV][VecOf<T>::n], float (&sd2)[NV],
+                                         float (&lse2)[NV], float (&SA)[NV], float (&SB)[NV],
+                                         float (&SD)[NV]) {
   constexpr int V = VecOf<T>::n;
-  const DirArgs& D = A.csr;
-  const Lane<NV> L(A.s);
-  const int wid = threadIdx.x >> 5;
-  extern __shared__ __align__(16) unsigned char smem[];
-  const bool item = blockIdx.x < D.n_items;
-  int i, beg, end, slot = -1;
-  const int32_t* cols = D.idx;
-  int colbase = 0;
-  if (item) {
-    const int4 it = D.items[blockIdx.x];
-    i = it.x;
-    slot = it.w;
-    int32_t* sc = reinterpret_cast<int32_t*>(smem + 16);
-    if (!stage_edges(sc, D.idx, it.y, it.z, reinterpret_cast<uint64_t*>(smem), A.err)) return;
-    cols = sc;
-    colbase = it.y & ~3;
-    const int per = (it.z - it.y + kWarps - 1) / kWarps;
-    beg = min(it.z, it.y + wid * per);
-    end = min(it.z, beg + per);
-  } else {
-    const int64_t t = (int64_t(blockIdx.x) - D.n_items) * kWarps + wid;
-    if (t >= D.n_light) return;
-    i = D.light[t];
-    beg = D.ptr[i];
-    end = D.ptr[i + 1];
-  }
-  float as2[NV][V], gi[NV][V], sd2[NV], lse2[NV];
-  {
-    float ad2[NV][V];
-    load_att<T, NV>(A.a_dst, L, kLog2e, ad2);
-    row_dot<T, NV>(A.h, i, A.s, L, ad2, sd2);
-  }
-  load_att<T, NV>(A.a_src, L, kLog2e, as2);
+  float gi[NV][V];
+  row_dot<T, NV>(A.h, i, A.s, L, ad2, sd2);
   load_row<T, NV>(A.dout, i, A.s, L, gi);
 #pragma unroll
-  for (int v = 0; v < NV; ++v) lse2[v] = L.ok[v] ? A.lse[int64_t(i) * A.s.H + L.k[v]] * kLog2e : 0.f;
-  float SA[NV], SB[NV], SD[NV];
-#pragma unroll
-  for (int v = 0; v < NV; ++v) SA[v] = SB[v] = SD[v] = 0.f;
-  dst_edges<T, NV>(A, L, cols, colbase, beg, end, as2, gi, sd2, lse2, SA, SB, SD);
+  for (int v = 0; v < NV; ++v) {
+    lse2[v] = L.ok[v] ? A.lse[int64_t(i) * A.s.H + L.k[v]] * kLog2e : 0.f;
+    SA[v] = SB[v] = SD[v] = 0.f;
+  }
+  dst_edges<T, NV>(A, L, cols, colbase, beg, end, jn, as2, gi, sd2, lse2, SA, SB, SD);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     SA[v] = subgroup_sum(SA[v], A.s);
     SB[v] = subgroup_sum(SB[v], A.s);
     SD[v] = subgroup_sum(SD[v], A.s);
   }
-  if (!item) {
-    if (L.g == 0)
-#pragma unroll
-      for (int v = 0; v < NV; ++v)
-        if (L.head_leader(A.s, v))
-          A.stats[int64_t(i) * A.s.H + L.k[v]] =
-              make_float4(sd2[v], lse2[v], SD[v], SA[v] - SD[v] * SB[v]);
-    return;
-  }
-  // block item: fold the warps' partial sums in warp order
-  float* wp = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H][3]
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_dst_main(const BwdArgs A) {
+  constexpr int V = VecOf<T>::n;
+  const DirArgs& D = A.csr;
+  const Lane<NV> L(A.s);
+  const int wid = threadIdx.x >> 5;
   const int H = A.s.H;
-  if (L.g == 0)
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_item;
+  float as2[NV][V], ad2[NV][V];
+  load_att<T, NV>(A.a_src, L, kLog2e, as2);
+  load_att<T, NV>(A.a_dst, L, kLog2e, ad2);
+  float sd2[NV], lse2[NV], SA[NV], SB[NV], SD[NV];
+
+  // ---- block items -------------------------------------------------------
+  if (D.n_items > 0) {
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int32_t* cols = reinterpret_cast<int32_t*>(smem + 16);
+    float* wp = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H][3]
+    uint32_t parity = 0;
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    for (;;) {
+      if (threadIdx.x == 0) s_item = atomicAdd(A.ctr + 0, 1);
+      __syncthreads();
+      const int idx = s_item;
+      if (idx >= D.n_items) break;
+      const int4 it = D.items[idx];
+      if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
+      const int per = (it.z - it.y + kWarps - 1) / kWarps;
+      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      int jn[kUnroll];
+      batch_ids<kUnroll>(cols, it.y & ~3, wb, we, L.g, L.G, jn);
+      dst_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, jn, as2, ad2, sd2, lse2, SA, SB, SD);
+      if (L.g == 0)
 #pragma unroll
-    for (int v = 0; v < NV; ++v)
-      if (L.head_leader(A.s, v)) {
-        float* p = wp + (wid * H + L.k[v]) * 3;
-        p[0] = SA[v];
-        p[1] = SB[v];
-        p[2] = SD[v];
+        for (int v = 0; v < NV; ++v)
+          if (L.head_leader(A.s, v)) {
+            float* p = wp + (wid * H + L.k[v]) * 3;
+            p[0] = SA[v];
+            p[1] = SB[v];
+            p[2] = SD[v];
+          }
+      __syncthreads();
+      if (wid == 0 && L.g == 0) {
+        // warp 0 folds the warps' partial sums in warp order
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          if (!L.head_leader(A.s, v)) continue;
+          float a = 0.f, b = 0.f, d = 0.f;
+          for (int w = 0; w < kWarps; ++w) {
+            const float* p = wp + (w * H + L.k[v]) * 3;
+            a += p[0];
+            b += p[1];
+            d += p[2];
+          }
+          if (it.w < 0)
+            A.stats[int64_t(it.x) * H + L.k[v]] = make_float4(sd2[v], lse2[v], d, a - d * b);
+          else
+            A.dst_part[int64_t(it.w) * H + L.k[v]] = make_float4(a, b, d, sd2[v]);
+        }
       }
-  __syncthreads();
-  if (wid != 0 || L.g != 0) return;
-#pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    if (!L.head_leader(A.s, v)) continue;
-    float a = 0.f, b = 0.f, d = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      const float* p = wp + (w * H + L.k[v]) * 3;
-      a += p[0];
-      b += p[1];
-      d += p[2];
+      __syncthreads();  // shared memory is reused by the next item
     }
-    if (slot < 0)
-      A.stats[int64_t(i) * H + L.k[v]] = make_float4(sd2[v], lse2[v], d, a - d * b);
-    else
-      A.dst_part[int64_t(slot) * H + L.k[v]] = make_float4(a, b, d, sd2[v]);
+  }
+
+  // ---- light nodes: one warp each ------------------------------------------
+  for (;;) {
+    int t0 = 0;
+    if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
+    t0 = __shfl_sync(kFull, t0, 0);
+    if (t0 >= D.n_light) break;
+    int my_i = -1, my_b = 0, my_e = 0;
+    if (L.lane < kGrab && t0 + L.lane < D.n_light) {
+      my_i = D.light[t0 + L.lane];
+      my_b = D.ptr[my_i];
+      my_e = D.ptr[my_i + 1];
+    }
+    int i = __shfl_sync(kFull, my_i, 0);
+    int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
+    int jn[kUnroll];
+    batch_ids<kUnroll>(D.idx, 0, beg, end, L.g, L.G, jn);
+    for (int q = 0; q < kGrab && i >= 0; ++q) {
+      const int nq = (q + 1) & (kGrab - 1);
+      const int i2 = q + 1 < kGrab ? __shfl_sync(kFull, my_i, nq) : -1;
+      const int b2 = __shfl_sync(kFull, my_b, nq);
+      const int e2 = __shfl_sync(kFull, my_e, nq);
+      int jn2[kUnroll];
+      batch_ids<kUnroll>(D.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
+      dst_node<T, NV>(A, L, i, D.idx, 0, beg, end, jn, as2, ad2, sd2, lse2, SA, SB, SD);
+      if (L.g == 0)
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+          if (L.head_leader(A.s, v))
+            A.stats[int64_t(i) * H + L.k[v]] =
+                make_float4(sd2[v], lse2[v], SD[v], SA[v] - SD[v] * SB[v]);
+      i = i2;
+      beg = b2;
+      end = e2;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) jn[u] = jn2[u];
+    }
   }
 }
 
@@ -260,6 +308,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dst_merge(const BwdArgs A) {
 template <typename T, int NV>
 __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
+                                          int (&in)[kUnroll],
                                           const float (&xj)[NV][VecOf<T>::n],
                                           const float (&ss2)[NV], float (&acc)[NV][VecOf<T>::n],
                                           float (&SZ)[NV]) {
@@ -267,23 +316,10 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
   constexpr int U = kUnroll;
   const int step = L.G * U;
   const int H = A.s.H;
-  int in[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int e = beg + u * L.G + L.g;
-    in[u] = e < end ? cols[e - colbase] : -1;
-  }
   for (int base = beg; base < end; base += step) {
     int i[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) i[u] = in[u];
-    if (base + step < end) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = base + step + u * L.G + L.g;
-        in[u] = e < end ? cols[e - colbase] : -1;
-      }
-    }
     uint4 raw[U][NV];
     float4 st[U][NV];
 #pragma unroll
@@ -296,6 +332,7 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
         st[u][v] = ok ? ld16f(A.stats + int64_t(i[u]) * H + L.k[v])
                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, in);
     float dd[U][NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -314,13 +351,43 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
       for (int v = 0; v < NV; ++v) {
         const float da = head_sum(dd[u][v], A.s.hv);
         const float z = st[u][v].x + ss2[v];
-        const float al = i[u] >= 0 ? exp2f(leaky(z, A.slope) - st[u][v].y) : 0.f;
+        const float al = i[u] >= 0 ? ex2(leaky(z, A.slope) - st[u][v].y) : 0.f;
         SZ[v] = fmaf(al * (da - st[u][v].z), leaky_grad(z, A.slope), SZ[v]);
         float g[V];
         unpack_alt<T>(raw[u][v], g);
 #pragma unroll
         for (int c = 0; c < V; ++c) acc[v][c] = fmaf(al, g[c], acc[v][c]);
       }
+  }
+}
+
+// Source-side sums of node j over its out-edges [beg, end) taken by this warp
+// (in: destinations of the first batch), summed over the warp's sub-groups.
+template <typename T, int NV>
+__device__ __forceinline__ void src_node(const BwdArgs& A, const Lane<NV>& L, int j,
+                                         const int32_t* cols, int colbase, int beg, int end,
+                                         int (&in)[kUnroll],
+                                         const float (&as2)[NV][VecOf<T>::n],
+                                         float (&acc)[NV][VecOf<T>::n], float (&SZ)[NV]) {
+  constexpr int V = VecOf<T>::n;
+  float xj[NV][V], ss2[NV];
+  load_row<T, NV>(A.h, j, A.s, L, xj);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    float d = 0.f;
+#pragma unroll
+    for (int c = 0; c < V; ++c) d = fmaf(xj[v][c], as2[v][c], d);
+    ss2[v] = head_sum(d, A.s.hv);
+    SZ[v] = 0.f;
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
+  }
+  src_edges<T, NV>(A, L, cols, colbase, beg, end, in, xj, ss2, acc, SZ);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    SZ[v] = subgroup_sum(SZ[v], A.s);
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[v][c] = subgroup_sum(acc[v][c], A.s);
   }
 }
 
@@ -352,98 +419,107 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
   const DirArgs& D = A.csc;
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
-  extern __shared__ __align__(16) unsigned char smem[];
-  const bool item = blockIdx.x < D.n_items;
-  int j, beg, end, slot = -1;
-  const int32_t* cols = D.idx;
-  int colbase = 0;
-  if (item) {
-    const int4 it = D.items[blockIdx.x];
-    j = it.x;
-    slot = it.w;
-    int32_t* sc = reinterpret_cast<int32_t*>(smem + 16);
-    if (!stage_edges(sc, D.idx, it.y, it.z, reinterpret_cast<uint64_t*>(smem), A.err)) return;
-    cols = sc;
-    colbase = it.y & ~3;
-    const int per = (it.z - it.y + kWarps - 1) / kWarps;
-    beg = min(it.z, it.y + wid * per);
-    end = min(it.z, beg + per);
-  } else {
-    const int64_t t = (int64_t(blockIdx.x) - D.n_items) * kWarps + wid;
-    if (t >= D.n_light) return;
-    j = D.light[t];
-    beg = D.ptr[j];
-    end = D.ptr[j + 1];
-  }
-  float xj[NV][V], ss2[NV], acc[NV][V], SZ[NV];
-  load_row<T, NV>(A.h, j, A.s, L, xj);
-  {
-    float as2[NV][V];
-    load_att<T, NV>(A.a_src, L, kLog2e, as2);
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      float d = 0.f;
-#pragma unroll
-      for (int c = 0; c < V; ++c) d = fmaf(xj[v][c], as2[v][c], d);
-      ss2[v] = head_sum(d, A.s.hv);
-    }
-  }
-#pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    SZ[v] = 0.f;
-#pragma unroll
-    for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
-  }
-  src_edges<T, NV>(A, L, cols, colbase, beg, end, xj, ss2, acc, SZ);
-#pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    SZ[v] = subgroup_sum(SZ[v], A.s);
-#pragma unroll
-    for (int c = 0; c < V; ++c) acc[v][c] = subgroup_sum(acc[v][c], A.s);
-  }
-  if (!item) {
-    if (L.g == 0) write_src<T, NV>(A, L, j, acc, SZ);
-    return;
-  }
   const int H = A.s.H;
-  const int row_f = A.s.rv * V;
-  float* wsum = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H]
-  float* wacc = wsum + kWarps * H;                            // [kWarps][H * D]
-  if (L.g == 0)
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_item;
+  float as2[NV][V];
+  load_att<T, NV>(A.a_src, L, kLog2e, as2);
+  float acc[NV][V], SZ[NV];
+
+  // ---- block items -------------------------------------------------------
+  if (D.n_items > 0) {
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int32_t* cols = reinterpret_cast<int32_t*>(smem + 16);
+    const int row_f = A.s.rv * V;
+    float* wsum = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H]
+    float* wacc = wsum + kWarps * H;                            // [kWarps][H * D]
+    uint32_t parity = 0;
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    for (;;) {
+      if (threadIdx.x == 0) s_item = atomicAdd(A.ctr + 2, 1);
+      __syncthreads();
+      const int idx = s_item;
+      if (idx >= D.n_items) break;
+      const int4 it = D.items[idx];
+      if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
+      const int per = (it.z - it.y + kWarps - 1) / kWarps;
+      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      int in[kUnroll];
+      batch_ids<kUnroll>(cols, it.y & ~3, wb, we, L.g, L.G, in);
+      src_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, in, as2, acc, SZ);
+      if (L.g == 0)
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      if (!L.ok[v]) continue;
+        for (int v = 0; v < NV; ++v) {
+          if (!L.ok[v]) continue;
 #pragma unroll
-      for (int c = 0; c < V; ++c) wacc[wid * row_f + L.q[v] * V + c] = acc[v][c];
-      if (L.head_leader(A.s, v)) wsum[wid * H + L.k[v]] = SZ[v];
-    }
-  __syncthreads();
-  if (wid != 0 || L.g != 0) return;
+          for (int c = 0; c < V; ++c) wacc[wid * row_f + L.q[v] * V + c] = acc[v][c];
+          if (L.head_leader(A.s, v)) wsum[wid * H + L.k[v]] = SZ[v];
+        }
+      __syncthreads();
+      if (wid == 0 && L.g == 0) {
+        // warp 0 folds the warps' partial sums in warp order
 #pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    SZ[v] = 0.f;
+        for (int v = 0; v < NV; ++v) {
+          SZ[v] = 0.f;
 #pragma unroll
-    for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
-    if (!L.ok[v]) continue;
-    for (int w = 0; w < kWarps; ++w) {
-      SZ[v] += wsum[w * H + L.k[v]];
+          for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
+          if (!L.ok[v]) continue;
+          for (int w = 0; w < kWarps; ++w) {
+            SZ[v] += wsum[w * H + L.k[v]];
 #pragma unroll
-      for (int c = 0; c < V; ++c) acc[v][c] += wacc[w * row_f + L.q[v] * V + c];
+            for (int c = 0; c < V; ++c) acc[v][c] += wacc[w * row_f + L.q[v] * V + c];
+          }
+        }
+        if (it.w < 0) {
+          write_src<T, NV>(A, L, it.x, acc, SZ);
+        } else {
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            if (!L.ok[v]) continue;
+            float* pa = A.src_acc + int64_t(it.w) * row_f + L.q[v] * V;
+#pragma unroll
+            for (int c4 = 0; c4 < V; c4 += 4)
+              *reinterpret_cast<float4*>(pa + c4) =
+                  make_float4(acc[v][c4], acc[v][c4 + 1], acc[v][c4 + 2], acc[v][c4 + 3]);
+            if (L.head_leader(A.s, v)) A.src_sum[int64_t(it.w) * H + L.k[v]] = SZ[v];
+          }
+        }
+      }
+      __syncthreads();  // shared memory is reused by the next item
     }
   }
-  if (slot < 0) {
-    write_src<T, NV>(A, L, j, acc, SZ);
-    return;
-  }
+
+  // ---- light nodes: one warp each ------------------------------------------
+  for (;;) {
+    int t0 = 0;
+    if (L.lane == 0) t0 = atomicAdd(A.ctr + 3, kGrab);
+    t0 = __shfl_sync(kFull, t0, 0);
+    if (t0 >= D.n_light) break;
+    int my_j = -1, my_b = 0, my_e = 0;
+    if (L.lane < kGrab && t0 + L.lane < D.n_light) {
+      my_j = D.light[t0 + L.lane];
+      my_b = D.ptr[my_j];
+      my_e = D.ptr[my_j + 1];
+    }
+    int j = __shfl_sync(kFull, my_j, 0);
+    int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
+    int in[kUnroll];
+    batch_ids<kUnroll>(D.idx, 0, beg, end, L.g, L.G, in);
+    for (int q = 0; q < kGrab && j >= 0; ++q) {
+      const int nq = (q + 1) & (kGrab - 1);
+      const int j2 = q + 1 < kGrab ? __shfl_sync(kFull, my_j, nq) : -1;
+      const int b2 = __shfl_sync(kFull, my_b, nq);
+      const int e2 = __shfl_sync(kFull, my_e, nq);
+      int in2[kUnroll];
+      batch_ids<kUnroll>(D.idx, 0, b2, j2 >= 0 ? e2 : b2, L.g, L.G, in2);
+      src_node<T, NV>(A, L, j, D.idx, 0, beg, end, in, as2, acc, SZ);
+      if (L.g == 0) write_src<T, NV>(A, L, j, acc, SZ);
+      j = j2;
+      beg = b2;
+      end = e2;
 #pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    if (!L.ok[v]) continue;
-    float* pa = A.src_acc + int64_t(slot) * row_f + L.q[v] * V;
-#pragma unroll
-    for (int c4 = 0; c4 < V; c4 += 4)
-      *reinterpret_cast<float4*>(pa + c4) =
-          make_float4(acc[v][c4], acc[v][c4 + 1], acc[v][c4 + 2], acc[v][c4 + 3]);
-    if (L.head_leader(A.s, v)) A.src_sum[int64_t(slot) * H + L.k[v]] = SZ[v];
+      for (int u = 0; u < kUnroll; ++u) in[u] = in2[u];
+    }
   }
 }
 
@@ -555,20 +631,23 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 }
 
 template <typename T, int NV>
-cudaError_t launch_t(const BwdArgs& A, cudaStream_t st, const cudaEvent_t* ev) {
+cudaError_t launch_t(const BwdArgs& A, int sm_count, cudaStream_t st, const cudaEvent_t* ev) {
   constexpr int V = VecOf<T>::n;
   const int H = A.s.H, row_f = A.s.rv * V;
   cudaError_t e;
   auto mark = [&](int k) {
     if (ev) cudaEventRecord(ev[k], st);
   };
+  if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), st)) != cudaSuccess) return e;
   mark(0);
   // pass 1
   {
-    const int64_t blocks = A.csr.n_items + (A.csr.n_light + kWarps - 1) / kWarps;
+    const int64_t work = A.csr.n_items + (A.csr.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
     const size_t smem = size_t(A.csr.col_off) + size_t(kWarps) * H * 3 * 4;
-    if (blocks > 0) {
+    if (work > 0) {
       if ((e = set_smem(bwd_dst_main<T, NV>, smem)) != cudaSuccess) return e;
+      const int64_t cap = persistent_blocks(bwd_dst_main<T, NV>, smem, sm_count);
+      const int64_t blocks = work < cap ? work : cap;
       bwd_dst_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -581,10 +660,12 @@ cudaError_t launch_t(const BwdArgs& A, cudaStream_t st, const cudaEvent_t* ev) {
   }
   // pass 2
   {
-    const int64_t blocks = A.csc.n_items + (A.csc.n_light + kWarps - 1) / kWarps;
+    const int64_t work = A.csc.n_items + (A.csc.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
     const size_t smem = size_t(A.csc.col_off) + size_t(kWarps) * (H + row_f) * 4;
-    if (blocks > 0) {
+    if (work > 0) {
       if ((e = set_smem(bwd_src_main<T, NV>, smem)) != cudaSuccess) return e;
+      const int64_t cap = persistent_blocks(bwd_src_main<T, NV>, smem, sm_count);
+      const int64_t blocks = work < cap ? work : cap;
       bwd_src_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -652,18 +733,19 @@ cudaError_t launch_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt, co
   A.src_sum = reinterpret_cast<float*>(ws + L.src_sum);
   A.da_part = reinterpret_cast<double*>(ws + L.da_part);
   A.da_blocks = L.da_blocks;
+  A.ctr = reinterpret_cast<int*>(ws + L.bwd_ctr);
   A.err = g->err;
   if (dt == GNN_F32) {
     switch (s.nv) {
-      case 1: return launch_t<float, 1>(A, st, ev);
-      case 2: return launch_t<float, 2>(A, st, ev);
-      case 4: return launch_t<float, 4>(A, st, ev);
+      case 1: return launch_t<float, 1>(A, g->sm_count, st, ev);
+      case 2: return launch_t<float, 2>(A, g->sm_count, st, ev);
+      case 4: return launch_t<float, 4>(A, g->sm_count, st, ev);
     }
   } else {
     switch (s.nv) {
-      case 1: return launch_t<__nv_bfloat16, 1>(A, st, ev);
-      case 2: return launch_t<__nv_bfloat16, 2>(A, st, ev);
-      case 4: return launch_t<__nv_bfloat16, 4>(A, st, ev);
+      case 1: return launch_t<__nv_bfloat16, 1>(A, g->sm_count, st, ev);
+      case 2: return launch_t<__nv_bfloat16, 2>(A, g->sm_count, st, ev);
+      case 4: return launch_t<__nv_bfloat16, 4>(A, g->sm_count, st, ev);
     }
   }
   return cudaErrorInvalidValue;

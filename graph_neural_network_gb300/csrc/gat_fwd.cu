@@ -10,18 +10,24 @@
 // per-edge score, weight or message is stored.
 //
 // Scores are kept in base 2 (a_src and a_dst are pre-scaled by log2 e, which
-// commutes with LeakyReLU), so every exponential is one exp2f; lse is stored
+// commutes with LeakyReLU), so every exponential is one ex2; lse is stored
 // in natural log.
 //
-// Degree-aware tiling: light nodes get one warp each; mid-degree nodes one
-// thread block whose warps split the edge list (staged in shared memory by a
-// bulk copy) and merge their states in warp order; hubs are split into edge
-// chunks, one block each, whose partial states a second kernel folds in chunk
-// order.  Every merge has a fixed order, so results are reproducible.
+// Degree-aware tiling: mid-degree nodes get one thread block whose warps split
+// the edge list (staged in shared memory by a bulk copy) and merge their
+// states in warp order; hubs are split into edge chunks, one block each, whose
+// partial states a second kernel folds in chunk order; light nodes get one
+// warp each.  Blocks are persistent: each first pulls block items (hub chunks
+// first, then mid nodes) from a work counter, then its warps pull light
+// nodes in groups.  Which block or warp handles a node never changes the
+// arithmetic applied to it, and every merge has a fixed order, so results
+// are reproducible bit for bit.
 #include "device.cuh"
 
 namespace gnn {
 namespace {
+
+constexpr int kGrab = 4;  // light nodes a warp takes per counter access
 
 struct FwdArgs {
   Shape s;
@@ -41,6 +47,7 @@ struct FwdArgs {
   float* lse;
   float* part_acc;   // [hub chunks][H * D]
   float2* part_ml;   // [hub chunks][H]  (max in base 2, sum)
+  int* ctr;          // [0] block items taken, [1] light nodes taken
   int32_t* err;
   int col_off;       // bytes of shared memory before the per-warp states
 };
@@ -65,7 +72,7 @@ struct Online {
   __device__ __forceinline__ void merge(int v, float mb, float lb, const float (&ab)[V]) {
     const float M = fmaxf(m[v], mb);
     const float Mr = (M == -INFINITY) ? 0.f : M;
-    const float sa = exp2f(m[v] - Mr), sb = exp2f(mb - Mr);
+    const float sa = ex2(m[v] - Mr), sb = ex2(mb - Mr);
     l[v] = l[v] * sa + lb * sb;
 #pragma unroll
     for (int c = 0; c < V; ++c) acc[v][c] = acc[v][c] * sa + ab[c] * sb;
@@ -89,33 +96,34 @@ struct Online {
   }
 };
 
-// Stream the edges beg, beg + G, ... < end of this lane's sub-group through
-// the online softmax.  cols[x - colbase] is the source of edge x.
+// Sources of the batch of edges starting at beg that this lane's sub-group
+// takes (edges beg + g, beg + g + G, ... below end; -1 past the end).
+template <int U>
+__device__ __forceinline__ void batch_sources(const int32_t* cols, int colbase, int beg, int end,
+                                              int g, int G, int (&j)[U]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = beg + u * G + g;
+    j[u] = e < end ? cols[e - colbase] : -1;
+  }
+}
+
+// Stream the edges beg + g, beg + g + G, ... < end through the online
+// softmax.  cols[x - colbase] is the source of edge x; jn holds the sources
+// of the first batch (already loaded).
 template <typename T, int NV>
 __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
+                                          int (&jn)[kUnroll],
                                           const float (&as2)[NV][VecOf<T>::n],
                                           const float (&sd2)[NV], Online<T, NV>& st) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
   const int step = L.G * U;
-  int jn[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int e = beg + u * L.G + L.g;
-    jn[u] = e < end ? cols[e - colbase] : -1;
-  }
   for (int base = beg; base < end; base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
-    if (base + step < end) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = base + step + u * L.G + L.g;
-        jn[u] = e < end ? cols[e - colbase] : -1;
-      }
-    }
     uint4 raw[U][NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -123,6 +131,7 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
       for (int v = 0; v < NV; ++v)
         raw[u][v] = (j[u] >= 0 && L.ok[v]) ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v])
                                            : make_uint4(0, 0, 0, 0);
+    if (base + step < end) batch_sources<U>(cols, colbase, base + step, end, L.g, L.G, jn);
     float sc[U][NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -150,13 +159,13 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
       for (int u = 1; u < U; ++u) bm = fmaxf(bm, sc[u][v]);
       const float mn = fmaxf(st.m[v], bm);
       const float mr = (mn == -INFINITY) ? 0.f : mn;
-      const float s0 = exp2f(st.m[v] - mr);
+      const float s0 = ex2(st.m[v] - mr);
       st.l[v] *= s0;
 #pragma unroll
       for (int c = 0; c < V; ++c) st.acc[v][c] *= s0;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const float pu = exp2f(sc[u][v] - mr);
+        const float pu = ex2(sc[u][v] - mr);
         st.l[v] += pu;
         float x[V];
         unpack_alt<T>(raw[u][v], x);
@@ -177,7 +186,7 @@ __device__ __forceinline__ void write_node(const FwdArgs& A, const Lane<NV>& L, 
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     if (!L.ok[v]) continue;
-    const float inv = st.l[v] > 0.f ? 1.f / st.l[v] : 0.f;
+    const float inv = st.l[v] > 0.f ? __frcp_rn(st.l[v]) : 0.f;
     float x[V];
 #pragma unroll
     for (int c = 0; c < V; ++c) x[c] = st.acc[v][c] * inv;
@@ -188,49 +197,32 @@ __device__ __forceinline__ void write_node(const FwdArgs& A, const Lane<NV>& L, 
   }
 }
 
+// One block item: a whole mid node (slot < 0) or one chunk of a hub.
 template <typename T, int NV>
-__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) fwd_main(const FwdArgs A) {
+__device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, int wid,
+                                         const int4 it, unsigned char* smem, uint32_t& parity,
+                                         const float (&as2)[NV][VecOf<T>::n],
+                                         const float (&ad2)[NV][VecOf<T>::n]) {
   constexpr int V = VecOf<T>::n;
-  const Lane<NV> L(A.s);
-  const int wid = threadIdx.x >> 5;
-  float as2[NV][V], ad2[NV][V];
-  load_att<T, NV>(A.a_src, L, kLog2e, as2);
-  load_att<T, NV>(A.a_dst, L, kLog2e, ad2);
-  Online<T, NV> st;
-  st.init();
-
-  if (blockIdx.x >= A.n_items) {
-    // ---- light node: one warp ------------------------------------------
-    const int64_t t = (int64_t(blockIdx.x) - A.n_items) * kWarps + wid;
-    if (t >= A.n_light) return;
-    const int i = A.light[t];
-    const int beg = A.ptr[i], end = A.ptr[i + 1];
-    float sd2[NV];
-    row_dot<T, NV>(A.h, i, A.s, L, ad2, sd2);
-    fwd_edges<T, NV>(A, L, A.idx, 0, beg, end, as2, sd2, st);
-    st.merge_subgroups(A.s);
-    if (L.g == 0) write_node<T, NV>(A, L, i, st);
-    return;
-  }
-
-  // ---- block item: a mid node, or one chunk of a hub ---------------------
-  extern __shared__ __align__(16) unsigned char smem[];
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
   int32_t* cols = reinterpret_cast<int32_t*>(smem + 16);
   float* wm = reinterpret_cast<float*>(smem + A.col_off);
   float* wl = wm + kWarps * A.s.H;
   float* wacc = wl + kWarps * A.s.H;
-  const int row_f = A.s.rv * V;  // floats per accumulator row
-
-  const int4 it = A.items[blockIdx.x];
+  const int row_f = A.s.rv * V;
   const int i = it.x, beg = it.y, end = it.z, slot = it.w;
-  if (!stage_edges(cols, A.idx, beg, end, bar, A.err)) return;
-  float sd2[NV];
-  row_dot<T, NV>(A.h, i, A.s, L, ad2, sd2);
+  if (!stage_edges(cols, A.idx, beg, end, bar, parity, A.err)) return false;
   const int len = end - beg;
   const int per = (len + kWarps - 1) / kWarps;
   const int wb = min(end, beg + wid * per), we = min(end, wb + per);
-  fwd_edges<T, NV>(A, L, cols, beg & ~3, wb, we, as2, sd2, st);
+  const int colbase = beg & ~3;
+  int jn[kUnroll];
+  batch_sources<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
+  float sd2[NV];
+  row_dot<T, NV>(A.h, i, A.s, L, ad2, sd2);
+  Online<T, NV> st;
+  st.init();
+  fwd_edges<T, NV>(A, L, cols, colbase, wb, we, jn, as2, sd2, st);
   st.merge_subgroups(A.s);
   if (L.g == 0) {
 #pragma unroll
@@ -245,39 +237,107 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) fwd_main(const
     }
   }
   __syncthreads();
-  if (wid != 0 || L.g != 0) return;
-  // warp 0 folds the warps' states in warp order
-  Online<T, NV> tot;
-#pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    tot.m[v] = L.ok[v] ? wm[L.k[v]] : -INFINITY;
-    tot.l[v] = L.ok[v] ? wl[L.k[v]] : 0.f;
-#pragma unroll
-    for (int c = 0; c < V; ++c) tot.acc[v][c] = L.ok[v] ? wacc[L.q[v] * V + c] : 0.f;
-  }
-  for (int w = 1; w < kWarps; ++w) {
+  if (wid == 0 && L.g == 0) {
+    // warp 0 folds the warps' states in warp order
+    Online<T, NV> tot;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-      if (!L.ok[v]) continue;
-      float ab[V];
+      tot.m[v] = L.ok[v] ? wm[L.k[v]] : -INFINITY;
+      tot.l[v] = L.ok[v] ? wl[L.k[v]] : 0.f;
 #pragma unroll
-      for (int c = 0; c < V; ++c) ab[c] = wacc[w * row_f + L.q[v] * V + c];
-      tot.merge(v, wm[w * A.s.H + L.k[v]], wl[w * A.s.H + L.k[v]], ab);
+      for (int c = 0; c < V; ++c) tot.acc[v][c] = L.ok[v] ? wacc[L.q[v] * V + c] : 0.f;
+    }
+    for (int w = 1; w < kWarps; ++w) {
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        if (!L.ok[v]) continue;
+        float ab[V];
+#pragma unroll
+        for (int c = 0; c < V; ++c) ab[c] = wacc[w * row_f + L.q[v] * V + c];
+        tot.merge(v, wm[w * A.s.H + L.k[v]], wl[w * A.s.H + L.k[v]], ab);
+      }
+    }
+    if (slot < 0) {
+      write_node<T, NV>(A, L, i, tot);
+    } else {
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        if (!L.ok[v]) continue;
+        float* pa = A.part_acc + int64_t(slot) * row_f + L.q[v] * V;
+#pragma unroll
+        for (int c4 = 0; c4 < V; c4 += 4)
+          *reinterpret_cast<float4*>(pa + c4) = make_float4(tot.acc[v][c4], tot.acc[v][c4 + 1],
+                                                            tot.acc[v][c4 + 2], tot.acc[v][c4 + 3]);
+        if (L.head_leader(A.s, v))
+          A.part_ml[int64_t(slot) * A.s.H + L.k[v]] = make_float2(tot.m[v], tot.l[v]);
+      }
     }
   }
-  if (slot < 0) {
-    write_node<T, NV>(A, L, i, tot);
-    return;
+  __syncthreads();  // shared memory is reused by the next item
+  return true;
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) fwd_main(const FwdArgs A) {
+  constexpr int V = VecOf<T>::n;
+  const Lane<NV> L(A.s);
+  const int wid = threadIdx.x >> 5;
+  float as2[NV][V], ad2[NV][V];
+  load_att<T, NV>(A.a_src, L, kLog2e, as2);
+  load_att<T, NV>(A.a_dst, L, kLog2e, ad2);
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_item;
+
+  // ---- block items: mid nodes and hub chunks -----------------------------
+  if (A.n_items > 0) {
+    uint32_t parity = 0;
+    if (threadIdx.x == 0) mbar_init(reinterpret_cast<uint64_t*>(smem), 1);
+    for (;;) {
+      if (threadIdx.x == 0) s_item = atomicAdd(A.ctr + 0, 1);
+      __syncthreads();
+      const int it = s_item;
+      if (it >= A.n_items) break;
+      if (!fwd_item<T, NV>(A, L, wid, A.items[it], smem, parity, as2, ad2)) return;
+    }
   }
+
+  // ---- light nodes: one warp each, pulled kGrab at a time ----------------
+  for (;;) {
+    int t0 = 0;
+    if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
+    t0 = __shfl_sync(kFull, t0, 0);
+    if (t0 >= A.n_light) break;
+    int my_i = -1, my_b = 0, my_e = 0;
+    if (L.lane < kGrab && t0 + L.lane < A.n_light) {
+      my_i = A.light[t0 + L.lane];
+      my_b = A.ptr[my_i];
+      my_e = A.ptr[my_i + 1];
+    }
+    int i = __shfl_sync(kFull, my_i, 0);
+    int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
+    int jn[kUnroll];
+    batch_sources<kUnroll>(A.idx, 0, beg, end, L.g, L.G, jn);
+    for (int q = 0; q < kGrab && i >= 0; ++q) {
+      // the next node's range and first sources, loaded while this one runs
+      const int nq = (q + 1) & (kGrab - 1);
+      const int i2 = q + 1 < kGrab ? __shfl_sync(kFull, my_i, nq) : -1;
+      const int b2 = __shfl_sync(kFull, my_b, nq);
+      const int e2 = __shfl_sync(kFull, my_e, nq);
+      int jn2[kUnroll];
+      batch_sources<kUnroll>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
+      float sd2[NV];
+      row_dot<T, NV>(A.h, i, A.s, L, ad2, sd2);
+      Online<T, NV> st;
+      st.init();
+      fwd_edges<T, NV>(A, L, A.idx, 0, beg, end, jn, as2, sd2, st);
+      st.merge_subgroups(A.s);
+      if (L.g == 0) write_node<T, NV>(A, L, i, st);
+      i = i2;
+      beg = b2;
+      end = e2;
 #pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    if (!L.ok[v]) continue;
-    float* pa = A.part_acc + int64_t(slot) * row_f + L.q[v] * V;
-#pragma unroll
-    for (int c4 = 0; c4 < V; c4 += 4)
-      *reinterpret_cast<float4*>(pa + c4) =
-          make_float4(tot.acc[v][c4], tot.acc[v][c4 + 1], tot.acc[v][c4 + 2], tot.acc[v][c4 + 3]);
-    if (L.head_leader(A.s, v)) A.part_ml[int64_t(slot) * A.s.H + L.k[v]] = make_float2(tot.m[v], tot.l[v]);
+      for (int u = 0; u < kUnroll; ++u) jn[u] = jn2[u];
+    }
   }
 }
 
@@ -315,27 +375,28 @@ __global__ void __launch_bounds__(kThreads) fwd_merge(const FwdArgs A) {
 }
 
 template <typename T, int NV>
-cudaError_t launch_t(const FwdArgs& A0, cudaStream_t stream, const cudaEvent_t* ev) {
-  FwdArgs A = A0;
+cudaError_t launch_t(const FwdArgs& A, int sm_count, cudaStream_t stream,
+                     const cudaEvent_t* ev) {
   constexpr int V = VecOf<T>::n;
-  const int64_t blocks = A.n_items + (A.n_light + kWarps - 1) / kWarps;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), stream)) != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[0], stream);
-  if (blocks > 0) {
+  if (A.n_items + A.n_light > 0) {
     const size_t smem = size_t(A.col_off) + size_t(kWarps) * (2 * A.s.H + A.s.rv * V) * 4;
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(fwd_main<T, NV>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-      if (e != cudaSuccess) return e;
-    }
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(fwd_main<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(smem))) != cudaSuccess)
+      return e;
+    const int64_t work = A.n_items + (A.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
+    const int64_t cap = persistent_blocks(fwd_main<T, NV>, smem, sm_count);
+    const int64_t blocks = work < cap ? work : cap;
     fwd_main<T, NV><<<unsigned(blocks), kThreads, smem, stream>>>(A);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (ev) cudaEventRecord(ev[1], stream);
   if (A.n_hubs > 0) {
     fwd_merge<T, NV><<<unsigned((A.n_hubs + kWarps - 1) / kWarps), kThreads, 0, stream>>>(A);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (ev) cudaEventRecord(ev[2], stream);
   return cudaGetLastError();
@@ -365,19 +426,20 @@ cudaError_t launch_forward(const gnn_graph* g, const Shape& s, gnn_dtype dt, con
   A.lse = lse;
   A.part_acc = reinterpret_cast<float*>(ws + L.fwd_acc);
   A.part_ml = reinterpret_cast<float2*>(ws + L.fwd_ml);
+  A.ctr = reinterpret_cast<int*>(ws + L.fwd_ctr);
   A.err = g->err;
   A.col_off = int(16 + align_up(size_t(g->csr.max_item + 4) * 4, 16));
   if (dt == GNN_F32) {
     switch (s.nv) {
-      case 1: return launch_t<float, 1>(A, st, ev);
-      case 2: return launch_t<float, 2>(A, st, ev);
-      case 4: return launch_t<float, 4>(A, st, ev);
+      case 1: return launch_t<float, 1>(A, g->sm_count, st, ev);
+      case 2: return launch_t<float, 2>(A, g->sm_count, st, ev);
+      case 4: return launch_t<float, 4>(A, g->sm_count, st, ev);
     }
   } else {
     switch (s.nv) {
-      case 1: return launch_t<__nv_bfloat16, 1>(A, st, ev);
-      case 2: return launch_t<__nv_bfloat16, 2>(A, st, ev);
-      case 4: return launch_t<__nv_bfloat16, 4>(A, st, ev);
+      case 1: return launch_t<__nv_bfloat16, 1>(A, g->sm_count, st, ev);
+      case 2: return launch_t<__nv_bfloat16, 2>(A, g->sm_count, st, ev);
+      case 4: return launch_t<__nv_bfloat16, 4>(A, g->sm_count, st, ev);
     }
   }
   return cudaErrorInvalidValue;

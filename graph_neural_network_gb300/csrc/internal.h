@@ -41,6 +41,7 @@ struct gnn_graph {
   gnn::Dir csr, csc;
   int32_t* err = nullptr;  // device status word (in the caller's buffer)
   int device = 0;
+  int sm_count = 0;
 };
 
 namespace gnn {
@@ -53,14 +54,20 @@ struct Shape {
   int hv = 0;     // 16-byte vectors per head (power of two, <= 32)
   int lpr = 0;    // lanes per row (power of two, <= 32)
   int nv = 0;     // vectors per lane (1, 2 or 4)
+  int hv_log2 = 0, lpr_log2 = 0;
 };
 
 // Workspace layout of one call (byte offsets into ws, 256-aligned).
 struct WsLayout {
-  size_t fwd_acc = 0, fwd_ml = 0, fwd_total = 0;
-  size_t stats = 0, ds_src = 0, dst_part = 0, src_acc = 0, src_sum = 0, da_part = 0, bwd_total = 0;
+  size_t fwd_ctr = 0, fwd_acc = 0, fwd_ml = 0, fwd_total = 0;
+  size_t bwd_ctr = 0, stats = 0, ds_src = 0, dst_part = 0, src_acc = 0, src_sum = 0, da_part = 0,
+         bwd_total = 0;
   int da_blocks = 0;
 };
+
+// Work counters at the head of each call's workspace, zeroed by the launcher
+// before the persistent kernels pull work from them.
+constexpr int kCounters = 8;
 
 bool make_shape(int H, int D, gnn_dtype dt, Shape* s);
 WsLayout ws_layout(const gnn_graph* g, const Shape& s);
