@@ -124,12 +124,75 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Sum over the `hv` consecutive lanes that hold one head (hv a power of two).
-__device__ __forceinline__ float head_sum(float v, int hv) {
+// Packed two-wide float32 arithmetic (one instruction for two lanes of
+// data on sm_100 and later).
+__device__ __forceinline__ unsigned long long pk(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+// (d0, d1) = (a0, a1) * (b0, b1) + (d0, d1)
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0,
+                                     float b1) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pk(a0, a1)), "l"(pk(b0, b1)),
+      "l"(pk(d0, d1)));
+  upk(d, d0, d1);
+}
+// (d0, d1) *= (s, s)
+__device__ __forceinline__ void mul2(float& d0, float& d1, float s) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(d0, d1)), "l"(pk(s, s)));
+  upk(d, d0, d1);
+}
+
+// x . w over V elements (two interleaved partial sums, added at the end).
+template <int V>
+__device__ __forceinline__ float dot(const float (&x)[V], const float (&w)[V]) {
+  float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1)
-    if (o < hv) v += __shfl_xor_sync(kFull, v, o);
-  return v;
+  for (int c = 0; c < V; c += 2) fma2(d0, d1, x[c], x[c + 1], w[c], w[c + 1]);
+  return d0 + d1;
+}
+
+// acc += p * x over V elements.
+template <int V>
+__device__ __forceinline__ void axpy(float (&acc)[V], float p, const float (&x)[V]) {
+#pragma unroll
+  for (int c = 0; c < V; c += 2) fma2(acc[c], acc[c + 1], x[c], x[c + 1], p, p);
+}
+
+// acc *= s over V elements.
+template <int V>
+__device__ __forceinline__ void scale(float (&acc)[V], float s) {
+#pragma unroll
+  for (int c = 0; c < V; c += 2) mul2(acc[c], acc[c + 1], s);
+}
+
+// Butterfly sums over aligned groups of 2^L lanes, for every element of x.
+template <int L, int N>
+__device__ __forceinline__ void group_sum(float (&x)[N]) {
+#pragma unroll
+  for (int o = 1; o < (1 << L); o <<= 1)
+#pragma unroll
+    for (int n = 0; n < N; ++n) x[n] += __shfl_xor_sync(kFull, x[n], o);
+}
+
+// Sum each element of x over the 2^hv_log2 lanes of its head.  One uniform
+// branch per call; the shuffles themselves are unrolled for the head width.
+template <int N>
+__device__ __forceinline__ void head_sums(float (&x)[N], int hv_log2) {
+  switch (hv_log2) {
+    case 0: break;
+    case 1: group_sum<1, N>(x); break;
+    case 2: group_sum<2, N>(x); break;
+    case 3: group_sum<3, N>(x); break;
+    case 4: group_sum<4, N>(x); break;
+    default: group_sum<5, N>(x); break;
+  }
 }
 
 // Where one lane sits in a feature row.  A row of rv 16-byte vectors is spread
@@ -202,12 +265,8 @@ __device__ __forceinline__ void row_dot(const void* x, int64_t node, const Shape
   float r[NV][V];
   load_row<T, NV>(x, node, s, L, r);
 #pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    float d = 0.f;
-#pragma unroll
-    for (int c = 0; c < V; ++c) d = fmaf(r[v][c], w[v][c], d);
-    out[v] = head_sum(d, s.hv);
-  }
+  for (int v = 0; v < NV; ++v) out[v] = dot<V>(r[v], w[v]);
+  head_sums<NV>(out, s.hv_log2);
 }
 
 // ---- mbarrier + bulk copy (shared::cta) --------------------------------------

@@ -114,28 +114,24 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
         raw[u][v] = (j[u] >= 0 && L.ok[v]) ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v])
                                            : make_uint4(0, 0, 0, 0);
     if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
-    float ss[U][NV], dd[U][NV];
+    // [0, U*NV): a_src . h_j; [U*NV, 2*U*NV): dout_i . h_j
+    float hs[2 * U * NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         float x[V];
         unpack<T>(raw[u][v], x);
-        float a = 0.f, b = 0.f;
-#pragma unroll
-        for (int c = 0; c < V; ++c) {
-          a = fmaf(x[c], as2[v][c], a);
-          b = fmaf(x[c], gi[v][c], b);
-        }
-        ss[u][v] = a;
-        dd[u][v] = b;
+        hs[u * NV + v] = dot<V>(x, as2[v]);
+        hs[U * NV + u * NV + v] = dot<V>(x, gi[v]);
       }
+    head_sums<2 * U * NV>(hs, A.s.hv_log2);
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
-        const float z = sd2[v] + head_sum(ss[u][v], A.s.hv);
-        const float da = head_sum(dd[u][v], A.s.hv);
+        const float z = sd2[v] + hs[u * NV + v];
+        const float da = hs[U * NV + u * NV + v];
         const float al = j[u] >= 0 ? ex2(leaky(z, A.slope) - lse2[v]) : 0.f;
         const float g = leaky_grad(z, A.slope);
         const float ad = al * da;
@@ -333,30 +329,27 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, in);
-    float dd[U][NV];
+    float dd[U * NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         float g[V];
         unpack<T>(raw[u][v], g);
-        float b = 0.f;
-#pragma unroll
-        for (int c = 0; c < V; ++c) b = fmaf(g[c], xj[v][c], b);
-        dd[u][v] = b;
+        dd[u * NV + v] = dot<V>(g, xj[v]);
       }
+    head_sums<U * NV>(dd, A.s.hv_log2);
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
-        const float da = head_sum(dd[u][v], A.s.hv);
+        const float da = dd[u * NV + v];
         const float z = st[u][v].x + ss2[v];
         const float al = i[u] >= 0 ? ex2(leaky(z, A.slope) - st[u][v].y) : 0.f;
         SZ[v] = fmaf(al * (da - st[u][v].z), leaky_grad(z, A.slope), SZ[v]);
         float g[V];
         unpack_alt<T>(raw[u][v], g);
-#pragma unroll
-        for (int c = 0; c < V; ++c) acc[v][c] = fmaf(al, g[c], acc[v][c]);
+        axpy<V>(acc[v], al, g);
       }
   }
 }
@@ -374,14 +367,12 @@ __device__ __forceinline__ void src_node(const BwdArgs& A, const Lane<NV>& L, in
   load_row<T, NV>(A.h, j, A.s, L, xj);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
-    float d = 0.f;
-#pragma unroll
-    for (int c = 0; c < V; ++c) d = fmaf(xj[v][c], as2[v][c], d);
-    ss2[v] = head_sum(d, A.s.hv);
+    ss2[v] = dot<V>(xj[v], as2[v]);
     SZ[v] = 0.f;
 #pragma unroll
     for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
   }
+  head_sums<NV>(ss2, A.s.hv_log2);
   src_edges<T, NV>(A, L, cols, colbase, beg, end, in, xj, ss2, acc, SZ);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {

@@ -74,8 +74,8 @@ struct Online {
     const float Mr = (M == -INFINITY) ? 0.f : M;
     const float sa = ex2(m[v] - Mr), sb = ex2(mb - Mr);
     l[v] = l[v] * sa + lb * sb;
-#pragma unroll
-    for (int c = 0; c < V; ++c) acc[v][c] = acc[v][c] * sa + ab[c] * sb;
+    scale<V>(acc[v], sa);
+    axpy<V>(acc[v], sb, ab);
     m[v] = M;
   }
 
@@ -132,45 +132,41 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
         raw[u][v] = (j[u] >= 0 && L.ok[v]) ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v])
                                            : make_uint4(0, 0, 0, 0);
     if (base + step < end) batch_sources<U>(cols, colbase, base + step, end, L.g, L.G, jn);
-    float sc[U][NV];
+    float sc[U * NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         float x[V];
         unpack<T>(raw[u][v], x);
-        float d = 0.f;
-#pragma unroll
-        for (int c = 0; c < V; ++c) d = fmaf(x[c], as2[v][c], d);
-        sc[u][v] = d;
+        sc[u * NV + v] = dot<V>(x, as2[v]);
       }
+    head_sums<U * NV>(sc, A.s.hv_log2);
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
-        const float z = sd2[v] + head_sum(sc[u][v], A.s.hv);
+        const float z = sd2[v] + sc[u * NV + v];
         const float e = z > 0.f ? z : A.slope * z;
-        sc[u][v] = j[u] >= 0 ? e : -INFINITY;
+        sc[u * NV + v] = j[u] >= 0 ? e : -INFINITY;
       }
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-      float bm = sc[0][v];
+      float bm = sc[v];
 #pragma unroll
-      for (int u = 1; u < U; ++u) bm = fmaxf(bm, sc[u][v]);
+      for (int u = 1; u < U; ++u) bm = fmaxf(bm, sc[u * NV + v]);
       const float mn = fmaxf(st.m[v], bm);
       const float mr = (mn == -INFINITY) ? 0.f : mn;
       const float s0 = ex2(st.m[v] - mr);
       st.l[v] *= s0;
-#pragma unroll
-      for (int c = 0; c < V; ++c) st.acc[v][c] *= s0;
+      scale<V>(st.acc[v], s0);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const float pu = ex2(sc[u][v] - mr);
+        const float pu = ex2(sc[u * NV + v] - mr);
         st.l[v] += pu;
         float x[V];
         unpack_alt<T>(raw[u][v], x);
-#pragma unroll
-        for (int c = 0; c < V; ++c) st.acc[v][c] = fmaf(pu, x[c], st.acc[v][c]);
+        axpy<V>(st.acc[v], pu, x);
       }
       st.m[v] = mn;
     }
@@ -189,11 +185,12 @@ __device__ __forceinline__ void write_node(const FwdArgs& A, const Lane<NV>& L, 
     const float inv = st.l[v] > 0.f ? __frcp_rn(st.l[v]) : 0.f;
     float x[V];
 #pragma unroll
-    for (int c = 0; c < V; ++c) x[c] = st.acc[v][c] * inv;
+    for (int c = 0; c < V; ++c) x[c] = st.acc[v][c];
+    scale<V>(x, inv);
     st16(orow + 16 * L.q[v], pack<T>(x));
     if (L.head_leader(A.s, v))
       A.lse[node * A.s.H + L.k[v]] =
-          st.l[v] > 0.f ? (st.m[v] + log2f(st.l[v])) * kLn2 : -INFINITY;
+          st.l[v] > 0.f ? (st.m[v] + __log2f(st.l[v])) * kLn2 : -INFINITY;
   }
 }
 
