@@ -39,10 +39,10 @@ sys.path.insert(0, ROOT)
 METRIC = "GEdge·head/s fwd and fwd+bwd GAT aggregation; achieved HBM GB/s vs roofline"
 UNIT = "GEdge*head/s"
 DEFAULT_CONFIG = 2
-FWD_EVENTS, BWD_EVENTS = 3, 7
-FWD_KERNELS = ["fwd_main", "fwd_merge"]
-BWD_KERNELS = ["bwd_dst_main", "bwd_dst_merge", "bwd_src_main", "bwd_src_merge", "da_partial",
-               "da_final"]
+FWD_EVENTS, BWD_EVENTS = 4, 8
+FWD_KERNELS = ["fwd_scores", "fwd_main", "fwd_merge"]
+BWD_KERNELS = ["bwd_scores", "bwd_dst_main", "bwd_dst_merge", "bwd_src_main", "bwd_src_merge",
+               "da_partial", "da_final"]
 
 
 def parse_args(argv=None):
@@ -70,11 +70,13 @@ def algorithmic_bytes(n, e, H, D, s):
     gathered h_j, dout_i and h_i read.  Source side: CSC indices, gathered
     dout_i, h_j read, dh_j written.  The per-edge gather of the 16-byte
     destination statistics in the source-side pass is extra traffic, not
-    counted here (reported separately as stats_bytes)."""
+    counted here (reported separately as stats_bytes).  The per-node score
+    pre-pass of each call reads h once and writes two float [N][H] arrays."""
     idx = 4 * (n + 1) + 4 * e
     gath = s * e * H * D
     row = s * n * H * D
     return {
+        "scores": row + 8 * n * H,
         "fwd_main": idx + gath + row + 4 * n * H,
         "bwd_dst_main": idx + gath + 2 * row,
         "bwd_src_main": idx + gath + 2 * row,
@@ -385,13 +387,18 @@ def run_gnnagg(args, rank, world):
     peak, peak_kind = peaks()
     achieved = ab[dom] / (kern[dom] * 1e-3) / 1e9
     traffic = measured_traffic(w.name, dom)
-    step_bytes = ab["fwd_main"] + ab["bwd_dst_main"] + ab["bwd_src_main"]
+    step_bytes = ab["fwd_main"] + ab["bwd_dst_main"] + ab["bwd_src_main"] + 2 * ab["scores"]
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_bytes": ab[dom], "peak_source": peak_kind}
     kernel_frac = {k: ab[k] / (kern[k] * 1e-3) / 1e9 / peak for k in main if kern[k] > 0}
+    for k in ("fwd_scores", "bwd_scores"):
+        if kern[k] > 0:
+            kernel_frac[k] = ab["scores"] / (kern[k] * 1e-3) / 1e9 / peak
 
-    launches_per_step = (1 + (st["csr"]["hubs"] > 0)) + (1 + (st["csr"]["hubs"] > 0)) + \
+    # forward: scores, main, hub merge; backward: scores, two main kernels and
+    # their hub merges, two attention-gradient kernels
+    launches_per_step = (2 + (st["csr"]["hubs"] > 0)) + (2 + (st["csr"]["hubs"] > 0)) + \
         (1 + (st["csc"]["hubs"] > 0)) + 2
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,

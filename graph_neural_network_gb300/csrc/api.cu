@@ -45,12 +45,14 @@ WsLayout ws_layout(const gnn_graph* g, const Shape& s) {
   };
   // forward: work counters, hub chunk partials of the CSR direction
   L.fwd_ctr = take(kCounters * 4);
+  L.fwd_scores = take(size_t(g->n) * s.H * 8);  // s_src [N][H] then s_dst [N][H]
   L.fwd_acc = take(size_t(g->csr.n_hub_chunks) * HD * 4);
   L.fwd_ml = take(size_t(g->csr.n_hub_chunks) * s.H * 8);
   L.fwd_total = off;
   // backward
   off = 0;
   L.bwd_ctr = take(kCounters * 4);
+  L.bwd_scores = take(size_t(g->n) * s.H * 8);
   L.stats = take(size_t(g->n) * s.H * 16);
   L.ds_src = take(size_t(g->n) * s.H * 4);
   L.dst_part = take(size_t(g->csr.n_hub_chunks) * s.H * 16);
@@ -229,7 +231,7 @@ gnn_status gat_agg_forward_timed(const gnn_graph* g, int H, int D, gnn_dtype dty
                                  const float* a_src, const float* a_dst, float slope, void* out,
                                  float* lse, void* ws, size_t ws_bytes, void* stream,
                                  void* const* events, int n_events) {
-  if (events && n_events < 3) return GNN_ERR_INVALID_ARG;
+  if (events && n_events < 4) return GNN_ERR_INVALID_ARG;
   Shape s;
   gnn_status r = check_call(g, H, D, dtype, &s);
   if (r != GNN_OK) return r;
@@ -259,7 +261,7 @@ gnn_status gat_agg_backward_timed(const gnn_graph* g, int H, int D, gnn_dtype dt
                                   float slope, const float* lse, const void* dout, void* dh,
                                   float* da_src, float* da_dst, void* ws, size_t ws_bytes,
                                   void* stream, void* const* events, int n_events) {
-  if (events && n_events < 7) return GNN_ERR_INVALID_ARG;
+  if (events && n_events < 8) return GNN_ERR_INVALID_ARG;
   Shape s;
   gnn_status r = check_call(g, H, D, dtype, &s);
   if (r != GNN_OK) return r;

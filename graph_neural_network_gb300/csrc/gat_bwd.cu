@@ -46,6 +46,8 @@ struct BwdArgs {
   const void* h;
   const float* a_src;
   const float* a_dst;
+  const float* ssrc;  // [N][H] base-2 a_src . h_n (pre-pass)
+  const float* sdst;  // [N][H] base-2 a_dst . h_n (pre-pass)
   float slope;
   const float* lse;
   const void* dout;
@@ -95,43 +97,44 @@ template <typename T, int NV>
 __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
                                           int (&jn)[kUnroll],
-                                          const float (&as2)[NV][VecOf<T>::n],
                                           const float (&gi)[NV][VecOf<T>::n],
                                           const float (&sd2)[NV], const float (&lse2)[NV],
                                           float (&SA)[NV], float (&SB)[NV], float (&SD)[NV]) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
   const int step = L.G * U;
+  const int H = A.s.H;
   for (int base = beg; base < end; base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
     uint4 raw[U][NV];
+    float ss[U * NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
-      for (int v = 0; v < NV; ++v)
-        raw[u][v] = (j[u] >= 0 && L.ok[v]) ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v])
-                                           : make_uint4(0, 0, 0, 0);
+      for (int v = 0; v < NV; ++v) {
+        const bool ok = j[u] >= 0 && L.ok[v];
+        raw[u][v] = ok ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v]) : make_uint4(0, 0, 0, 0);
+        ss[u * NV + v] = ok ? __ldg(A.ssrc + int64_t(j[u]) * H + L.k[v]) : 0.f;
+      }
     if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
-    // [0, U*NV): a_src . h_j; [U*NV, 2*U*NV): dout_i . h_j
-    float hs[2 * U * NV];
+    float dd[U * NV];  // dout_i . h_j per head
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         float x[V];
         unpack<T>(raw[u][v], x);
-        hs[u * NV + v] = dot<V>(x, as2[v]);
-        hs[U * NV + u * NV + v] = dot<V>(x, gi[v]);
+        dd[u * NV + v] = dot<V>(x, gi[v]);
       }
-    head_sums<2 * U * NV>(hs, A.s.hv_log2);
+    head_sums<U * NV>(dd, A.s.hv_log2);
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
-        const float z = sd2[v] + hs[u * NV + v];
-        const float da = hs[U * NV + u * NV + v];
+        const float z = sd2[v] + ss[u * NV + v];
+        const float da = dd[u * NV + v];
         const float al = j[u] >= 0 ? ex2(leaky(z, A.slope) - lse2[v]) : 0.f;
         const float g = leaky_grad(z, A.slope);
         const float ad = al * da;
@@ -147,21 +150,19 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
 template <typename T, int NV>
 __device__ __forceinline__ void dst_node(const BwdArgs& A, const Lane<NV>& L, int i,
                                          const int32_t* cols, int colbase, int beg, int end,
-                                         int (&jn)[kUnroll],
-                                         const float (&as2)[NV][VecOf<T>::n],
-                                         const float (&ad2)[NV][VecOf<T>::n], float (&sd2)[NV],
+                                         int (&jn)[kUnroll], float (&sd2)[NV],
                                          float (&lse2)[NV], float (&SA)[NV], float (&SB)[NV],
                                          float (&SD)[NV]) {
   constexpr int V = VecOf<T>::n;
   float gi[NV][V];
-  row_dot<T, NV>(A.h, i, A.s, L, ad2, sd2);
   load_row<T, NV>(A.dout, i, A.s, L, gi);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
+    sd2[v] = L.ok[v] ? __ldg(A.sdst + int64_t(i) * A.s.H + L.k[v]) : 0.f;
     lse2[v] = L.ok[v] ? A.lse[int64_t(i) * A.s.H + L.k[v]] * kLog2e : 0.f;
     SA[v] = SB[v] = SD[v] = 0.f;
   }
-  dst_edges<T, NV>(A, L, cols, colbase, beg, end, jn, as2, gi, sd2, lse2, SA, SB, SD);
+  dst_edges<T, NV>(A, L, cols, colbase, beg, end, jn, gi, sd2, lse2, SA, SB, SD);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     SA[v] = subgroup_sum(SA[v], A.s);
@@ -179,9 +180,6 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_dst_main(c
   const int H = A.s.H;
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int s_item;
-  float as2[NV][V], ad2[NV][V];
-  load_att<T, NV>(A.a_src, L, kLog2e, as2);
-  load_att<T, NV>(A.a_dst, L, kLog2e, ad2);
   float sd2[NV], lse2[NV], SA[NV], SB[NV], SD[NV];
 
   // ---- block items -------------------------------------------------------
@@ -202,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_dst_main(c
       const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
       int jn[kUnroll];
       batch_ids<kUnroll>(cols, it.y & ~3, wb, we, L.g, L.G, jn);
-      dst_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, jn, as2, ad2, sd2, lse2, SA, SB, SD);
+      dst_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, jn, sd2, lse2, SA, SB, SD);
       if (L.g == 0)
 #pragma unroll
         for (int v = 0; v < NV; ++v)
@@ -258,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_dst_main(c
       const int e2 = __shfl_sync(kFull, my_e, nq);
       int jn2[kUnroll];
       batch_ids<kUnroll>(D.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
-      dst_node<T, NV>(A, L, i, D.idx, 0, beg, end, jn, as2, ad2, sd2, lse2, SA, SB, SD);
+      dst_node<T, NV>(A, L, i, D.idx, 0, beg, end, jn, sd2, lse2, SA, SB, SD);
       if (L.g == 0)
 #pragma unroll
         for (int v = 0; v < NV; ++v)
@@ -359,20 +357,18 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
 template <typename T, int NV>
 __device__ __forceinline__ void src_node(const BwdArgs& A, const Lane<NV>& L, int j,
                                          const int32_t* cols, int colbase, int beg, int end,
-                                         int (&in)[kUnroll],
-                                         const float (&as2)[NV][VecOf<T>::n],
-                                         float (&acc)[NV][VecOf<T>::n], float (&SZ)[NV]) {
+                                         int (&in)[kUnroll], float (&acc)[NV][VecOf<T>::n],
+                                         float (&SZ)[NV]) {
   constexpr int V = VecOf<T>::n;
   float xj[NV][V], ss2[NV];
   load_row<T, NV>(A.h, j, A.s, L, xj);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
-    ss2[v] = dot<V>(xj[v], as2[v]);
+    ss2[v] = L.ok[v] ? __ldg(A.ssrc + int64_t(j) * A.s.H + L.k[v]) : 0.f;
     SZ[v] = 0.f;
 #pragma unroll
     for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
   }
-  head_sums<NV>(ss2, A.s.hv_log2);
   src_edges<T, NV>(A, L, cols, colbase, beg, end, in, xj, ss2, acc, SZ);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
@@ -413,8 +409,6 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
   const int H = A.s.H;
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int s_item;
-  float as2[NV][V];
-  load_att<T, NV>(A.a_src, L, kLog2e, as2);
   float acc[NV][V], SZ[NV];
 
   // ---- block items -------------------------------------------------------
@@ -437,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
       const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
       int in[kUnroll];
       batch_ids<kUnroll>(cols, it.y & ~3, wb, we, L.g, L.G, in);
-      src_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, in, as2, acc, SZ);
+      src_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, in, acc, SZ);
       if (L.g == 0)
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
@@ -503,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
       const int e2 = __shfl_sync(kFull, my_e, nq);
       int in2[kUnroll];
       batch_ids<kUnroll>(D.idx, 0, b2, j2 >= 0 ? e2 : b2, L.g, L.G, in2);
-      src_node<T, NV>(A, L, j, D.idx, 0, beg, end, in, as2, acc, SZ);
+      src_node<T, NV>(A, L, j, D.idx, 0, beg, end, in, acc, SZ);
       if (L.g == 0) write_src<T, NV>(A, L, j, acc, SZ);
       j = j2;
       beg = b2;
@@ -622,7 +616,8 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 }
 
 template <typename T, int NV>
-cudaError_t launch_t(const BwdArgs& A, int sm_count, cudaStream_t st, const cudaEvent_t* ev) {
+cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t st,
+                     const cudaEvent_t* ev) {
   constexpr int V = VecOf<T>::n;
   const int H = A.s.H, row_f = A.s.rv * V;
   cudaError_t e;
@@ -631,6 +626,10 @@ cudaError_t launch_t(const BwdArgs& A, int sm_count, cudaStream_t st, const cuda
   };
   if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), st)) != cudaSuccess) return e;
   mark(0);
+  if ((e = launch_node_scores(A.s, dt, A.h, A.a_src, A.a_dst, A.n, const_cast<float*>(A.ssrc),
+                              const_cast<float*>(A.sdst), sm_count, st)) != cudaSuccess)
+    return e;
+  mark(1);
   // pass 1
   {
     const int64_t work = A.csr.n_items + (A.csr.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
@@ -642,12 +641,12 @@ cudaError_t launch_t(const BwdArgs& A, int sm_count, cudaStream_t st, const cuda
       bwd_dst_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    mark(1);
+    mark(2);
     if (A.csr.n_hubs > 0) {
       bwd_dst_merge<T, NV><<<unsigned((A.csr.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    mark(2);
+    mark(3);
   }
   // pass 2
   {
@@ -660,12 +659,12 @@ cudaError_t launch_t(const BwdArgs& A, int sm_count, cudaStream_t st, const cuda
       bwd_src_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    mark(3);
+    mark(4);
     if (A.csc.n_hubs > 0) {
       bwd_src_merge<T, NV><<<unsigned((A.csc.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    mark(4);
+    mark(5);
   }
   // attention-vector gradients
   {
@@ -673,11 +672,11 @@ cudaError_t launch_t(const BwdArgs& A, int sm_count, cudaStream_t st, const cuda
     if ((e = set_smem(da_partial<T, NV>, smem)) != cudaSuccess) return e;
     da_partial<T, NV><<<unsigned(A.da_blocks), kThreads, smem, st>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    mark(5);
+    mark(6);
     da_final<<<unsigned((2 * row_f + 127) / 128), 128, 0, st>>>(A.da_part, A.da_blocks, row_f,
                                                                 A.da_src, A.da_dst);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    mark(6);
+    mark(7);
   }
   return cudaGetLastError();
 }
@@ -711,6 +710,8 @@ cudaError_t launch_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt, co
   A.h = h;
   A.a_src = a_src;
   A.a_dst = a_dst;
+  A.ssrc = reinterpret_cast<const float*>(ws + L.bwd_scores);
+  A.sdst = A.ssrc + g->n * s.H;
   A.slope = slope;
   A.lse = lse;
   A.dout = dout;
@@ -728,15 +729,15 @@ cudaError_t launch_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt, co
   A.err = g->err;
   if (dt == GNN_F32) {
     switch (s.nv) {
-      case 1: return launch_t<float, 1>(A, g->sm_count, st, ev);
-      case 2: return launch_t<float, 2>(A, g->sm_count, st, ev);
-      case 4: return launch_t<float, 4>(A, g->sm_count, st, ev);
+      case 1: return launch_t<float, 1>(A, dt, g->sm_count, st, ev);
+      case 2: return launch_t<float, 2>(A, dt, g->sm_count, st, ev);
+      case 4: return launch_t<float, 4>(A, dt, g->sm_count, st, ev);
     }
   } else {
     switch (s.nv) {
-      case 1: return launch_t<__nv_bfloat16, 1>(A, g->sm_count, st, ev);
-      case 2: return launch_t<__nv_bfloat16, 2>(A, g->sm_count, st, ev);
-      case 4: return launch_t<__nv_bfloat16, 4>(A, g->sm_count, st, ev);
+      case 1: return launch_t<__nv_bfloat16, 1>(A, dt, g->sm_count, st, ev);
+      case 2: return launch_t<__nv_bfloat16, 2>(A, dt, g->sm_count, st, ev);
+      case 4: return launch_t<__nv_bfloat16, 4>(A, dt, g->sm_count, st, ev);
     }
   }
   return cudaErrorInvalidValue;

@@ -11,7 +11,9 @@
 //
 // Scores are kept in base 2 (a_src and a_dst are pre-scaled by log2 e, which
 // commutes with LeakyReLU), so every exponential is one ex2; lse is stored
-// in natural log.
+// in natural log.  Both score halves of every node come from a streaming
+// pre-pass (scores.cu), so the edge loop gathers one float per edge and head
+// next to the row it aggregates.
 //
 // Degree-aware tiling: mid-degree nodes get one thread block whose warps split
 // the edge list (staged in shared memory by a bulk copy) and merge their
@@ -40,8 +42,8 @@ struct FwdArgs {
   const int4* hubs;
   int64_t n_hubs;
   const void* h;
-  const float* a_src;
-  const float* a_dst;
+  const float* ssrc;  // [N][H] base-2 a_src . h_n
+  const float* sdst;  // [N][H] base-2 a_dst . h_n
   float slope;
   void* out;
   float* lse;
@@ -114,34 +116,27 @@ __device__ __forceinline__ void batch_sources(const int32_t* cols, int colbase, 
 template <typename T, int NV>
 __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
-                                          int (&jn)[kUnroll],
-                                          const float (&as2)[NV][VecOf<T>::n],
-                                          const float (&sd2)[NV], Online<T, NV>& st) {
+                                          int (&jn)[kUnroll], const float (&sd2)[NV],
+                                          Online<T, NV>& st) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
   const int step = L.G * U;
+  const int H = A.s.H;
   for (int base = beg; base < end; base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
     uint4 raw[U][NV];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-#pragma unroll
-      for (int v = 0; v < NV; ++v)
-        raw[u][v] = (j[u] >= 0 && L.ok[v]) ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v])
-                                           : make_uint4(0, 0, 0, 0);
-    if (base + step < end) batch_sources<U>(cols, colbase, base + step, end, L.g, L.G, jn);
     float sc[U * NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
-        float x[V];
-        unpack<T>(raw[u][v], x);
-        sc[u * NV + v] = dot<V>(x, as2[v]);
+        const bool ok = j[u] >= 0 && L.ok[v];
+        raw[u][v] = ok ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v]) : make_uint4(0, 0, 0, 0);
+        sc[u * NV + v] = ok ? __ldg(A.ssrc + int64_t(j[u]) * H + L.k[v]) : 0.f;
       }
-    head_sums<U * NV>(sc, A.s.hv_log2);
+    if (base + step < end) batch_sources<U>(cols, colbase, base + step, end, L.g, L.G, jn);
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
@@ -165,12 +160,20 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
         const float pu = ex2(sc[u * NV + v] - mr);
         st.l[v] += pu;
         float x[V];
-        unpack_alt<T>(raw[u][v], x);
+        unpack<T>(raw[u][v], x);
         axpy<V>(st.acc[v], pu, x);
       }
       st.m[v] = mn;
     }
   }
+}
+
+// This lane's base-2 destination score halves of node i.
+template <int NV>
+__device__ __forceinline__ void node_sdst(const FwdArgs& A, const Lane<NV>& L, int64_t i,
+                                          float (&sd2)[NV]) {
+#pragma unroll
+  for (int v = 0; v < NV; ++v) sd2[v] = L.ok[v] ? __ldg(A.sdst + i * A.s.H + L.k[v]) : 0.f;
 }
 
 // out = acc / l, lse = (m + log2 l) ln 2; a node without edges gets 0 and -inf.
@@ -197,9 +200,7 @@ __device__ __forceinline__ void write_node(const FwdArgs& A, const Lane<NV>& L, 
 // One block item: a whole mid node (slot < 0) or one chunk of a hub.
 template <typename T, int NV>
 __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, int wid,
-                                         const int4 it, unsigned char* smem, uint32_t& parity,
-                                         const float (&as2)[NV][VecOf<T>::n],
-                                         const float (&ad2)[NV][VecOf<T>::n]) {
+                                         const int4 it, unsigned char* smem, uint32_t& parity) {
   constexpr int V = VecOf<T>::n;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
   int32_t* cols = reinterpret_cast<int32_t*>(smem + 16);
@@ -216,10 +217,10 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, in
   int jn[kUnroll];
   batch_sources<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
   float sd2[NV];
-  row_dot<T, NV>(A.h, i, A.s, L, ad2, sd2);
+  node_sdst<NV>(A, L, i, sd2);
   Online<T, NV> st;
   st.init();
-  fwd_edges<T, NV>(A, L, cols, colbase, wb, we, jn, as2, sd2, st);
+  fwd_edges<T, NV>(A, L, cols, colbase, wb, we, jn, sd2, st);
   st.merge_subgroups(A.s);
   if (L.g == 0) {
 #pragma unroll
@@ -276,12 +277,8 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, in
 
 template <typename T, int NV>
 __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) fwd_main(const FwdArgs A) {
-  constexpr int V = VecOf<T>::n;
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
-  float as2[NV][V], ad2[NV][V];
-  load_att<T, NV>(A.a_src, L, kLog2e, as2);
-  load_att<T, NV>(A.a_dst, L, kLog2e, ad2);
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int s_item;
 
@@ -294,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) fwd_main(const
       __syncthreads();
       const int it = s_item;
       if (it >= A.n_items) break;
-      if (!fwd_item<T, NV>(A, L, wid, A.items[it], smem, parity, as2, ad2)) return;
+      if (!fwd_item<T, NV>(A, L, wid, A.items[it], smem, parity)) return;
     }
   }
 
@@ -323,10 +320,10 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) fwd_main(const
       int jn2[kUnroll];
       batch_sources<kUnroll>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
       float sd2[NV];
-      row_dot<T, NV>(A.h, i, A.s, L, ad2, sd2);
+      node_sdst<NV>(A, L, i, sd2);
       Online<T, NV> st;
       st.init();
-      fwd_edges<T, NV>(A, L, A.idx, 0, beg, end, jn, as2, sd2, st);
+      fwd_edges<T, NV>(A, L, A.idx, 0, beg, end, jn, sd2, st);
       st.merge_subgroups(A.s);
       if (L.g == 0) write_node<T, NV>(A, L, i, st);
       i = i2;
@@ -372,12 +369,16 @@ __global__ void __launch_bounds__(kThreads) fwd_merge(const FwdArgs A) {
 }
 
 template <typename T, int NV>
-cudaError_t launch_t(const FwdArgs& A, int sm_count, cudaStream_t stream,
-                     const cudaEvent_t* ev) {
+cudaError_t launch_t(const FwdArgs& A, gnn_dtype dt, const float* a_src, const float* a_dst,
+                     int64_t n, int sm_count, cudaStream_t stream, const cudaEvent_t* ev) {
   constexpr int V = VecOf<T>::n;
   cudaError_t e;
   if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), stream)) != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[0], stream);
+  if ((e = launch_node_scores(A.s, dt, A.h, a_src, a_dst, n, const_cast<float*>(A.ssrc),
+                              const_cast<float*>(A.sdst), sm_count, stream)) != cudaSuccess)
+    return e;
+  if (ev) cudaEventRecord(ev[1], stream);
   if (A.n_items + A.n_light > 0) {
     const size_t smem = size_t(A.col_off) + size_t(kWarps) * (2 * A.s.H + A.s.rv * V) * 4;
     if (smem > 48 * 1024 &&
@@ -390,12 +391,12 @@ cudaError_t launch_t(const FwdArgs& A, int sm_count, cudaStream_t stream,
     fwd_main<T, NV><<<unsigned(blocks), kThreads, smem, stream>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (ev) cudaEventRecord(ev[1], stream);
+  if (ev) cudaEventRecord(ev[2], stream);
   if (A.n_hubs > 0) {
     fwd_merge<T, NV><<<unsigned((A.n_hubs + kWarps - 1) / kWarps), kThreads, 0, stream>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (ev) cudaEventRecord(ev[2], stream);
+  if (ev) cudaEventRecord(ev[3], stream);
   return cudaGetLastError();
 }
 
@@ -416,8 +417,8 @@ cudaError_t launch_forward(const gnn_graph* g, const Shape& s, gnn_dtype dt, con
   A.hubs = g->csr.hubs;
   A.n_hubs = g->csr.n_hubs;
   A.h = h;
-  A.a_src = a_src;
-  A.a_dst = a_dst;
+  A.ssrc = reinterpret_cast<const float*>(ws + L.fwd_scores);
+  A.sdst = A.ssrc + g->n * s.H;
   A.slope = slope;
   A.out = out;
   A.lse = lse;
@@ -428,15 +429,15 @@ cudaError_t launch_forward(const gnn_graph* g, const Shape& s, gnn_dtype dt, con
   A.col_off = int(16 + align_up(size_t(g->csr.max_item + 4) * 4, 16));
   if (dt == GNN_F32) {
     switch (s.nv) {
-      case 1: return launch_t<float, 1>(A, g->sm_count, st, ev);
-      case 2: return launch_t<float, 2>(A, g->sm_count, st, ev);
-      case 4: return launch_t<float, 4>(A, g->sm_count, st, ev);
+      case 1: return launch_t<float, 1>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+      case 2: return launch_t<float, 2>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+      case 4: return launch_t<float, 4>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
     }
   } else {
     switch (s.nv) {
-      case 1: return launch_t<__nv_bfloat16, 1>(A, g->sm_count, st, ev);
-      case 2: return launch_t<__nv_bfloat16, 2>(A, g->sm_count, st, ev);
-      case 4: return launch_t<__nv_bfloat16, 4>(A, g->sm_count, st, ev);
+      case 1: return launch_t<__nv_bfloat16, 1>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+      case 2: return launch_t<__nv_bfloat16, 2>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+      case 4: return launch_t<__nv_bfloat16, 4>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
     }
   }
   return cudaErrorInvalidValue;

@@ -59,9 +59,9 @@ struct Shape {
 
 // Workspace layout of one call (byte offsets into ws, 256-aligned).
 struct WsLayout {
-  size_t fwd_ctr = 0, fwd_acc = 0, fwd_ml = 0, fwd_total = 0;
-  size_t bwd_ctr = 0, stats = 0, ds_src = 0, dst_part = 0, src_acc = 0, src_sum = 0, da_part = 0,
-         bwd_total = 0;
+  size_t fwd_ctr = 0, fwd_scores = 0, fwd_acc = 0, fwd_ml = 0, fwd_total = 0;
+  size_t bwd_ctr = 0, bwd_scores = 0, stats = 0, ds_src = 0, dst_part = 0, src_acc = 0,
+         src_sum = 0, da_part = 0, bwd_total = 0;
   int da_blocks = 0;
 };
 
@@ -82,6 +82,11 @@ cudaError_t launch_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt, co
                             const float* lse, const void* dout, void* dh, float* da_src,
                             float* da_dst, char* ws, const WsLayout& L, cudaStream_t st,
                             const cudaEvent_t* ev);
+
+// Per-node base-2 score halves s_src, s_dst [N][H] (scores.cu).
+cudaError_t launch_node_scores(const Shape& s, gnn_dtype dt, const void* h, const float* a_src,
+                               const float* a_dst, int64_t n, float* ssrc, float* sdst,
+                               int sm_count, cudaStream_t st);
 
 // Graph preparation (prepare.cu).
 gnn_status prepare_graph(gnn_graph* g, const int32_t* row_ptr, const int32_t* col,

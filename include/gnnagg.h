@@ -163,8 +163,9 @@ gnn_status gat_agg_backward(const gnn_graph* g, int H, int D, gnn_dtype dtype, c
 
 /* gat_agg_forward / gat_agg_backward that also record the caller's CUDA
  * events (cudaEvent_t passed as void*) on `stream` between their kernels, for
- * per-kernel timing.  Forward: n_events = 3 -- before the main kernel, after
- * it, after the hub merge.  Backward: n_events = 7 -- before the
+ * per-kernel timing.  Forward: n_events = 4 -- before the per-node score
+ * pre-pass, before the main kernel, after it, after the hub merge.
+ * Backward: n_events = 8 -- before the score pre-pass, before the
  * destination-side pass, after its main kernel, after its hub merge, after
  * the source-side main kernel, after its hub merge, after the
  * attention-vector partial sums, at the end.  A kernel with no work records
@@ -186,21 +187,22 @@ gnn_status gat_agg_backward_timed(const gnn_graph* g, int H, int D, gnn_dtype dt
  * latency-critical path where an allocation (and the synchronisation it can
  * imply) is not allowed.  Such callers still pass h, a_src, a_dst, out and
  * lse, exactly as for gat_agg_forward, and get the same results.
- * The hub partial states that gat_agg_forward keeps in `ws` go instead to a
- * fixed array inside this library of gat_agg_forward_noalloc_capacity()
- * bytes (16 MiB) on each GPU that loads the library, held until the process
- * exits.  A graph whose forward workspace (gat_agg_workspace_bytes' forward
- * part: hub chunks * H * (D + 2) * 4 bytes) exceeds that size is rejected
- * with GNN_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ * The per-node scores and hub partial states that gat_agg_forward keeps in
+ * `ws` go instead to a fixed array inside this library of
+ * gat_agg_forward_noalloc_capacity() bytes (16 MiB) on each GPU that loads
+ * the library, held until the process exits.  A graph whose forward workspace (gat_agg_workspace_bytes' forward
+ * part: about 8 * N * H bytes of per-node scores plus hub chunks * H *
+ * (D + 2) * 4 bytes) exceeds that size is rejected with
+ * GNN_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  * The first call on a device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress) and caches it; make that
  * first call before any stream capture.  The device must be the one the
  * graph was prepared on (else GNN_ERR_INVALID_ARG).
  * Every call shares the one array: calls that overlap on the GPU (on
  * different streams, or from several threads) race and must be serialised
- * by the caller.  The array keeps the last call's contents; nothing in it
- * needs to start at zero, as each call writes every partial before reading
- * it. */
+ * by the caller.  The array keeps the last call's contents; the call zeroes
+ * the few work counters it needs and writes every score and partial before
+ * reading it. */
 gnn_status gat_agg_forward_noalloc(const gnn_graph* g, int H, int D, gnn_dtype dtype,
                                    const void* h, const float* a_src, const float* a_dst,
                                    float slope, void* out, float* lse, void* stream);
