@@ -1,9 +1,10 @@
-"""fp64 CPU oracle for the fused GAT neighbour aggregation (ctypes wrapper).
+"""fp64 CPU oracles of the neighbour aggregations (ctypes wrapper).
 
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the smoke check in
 ``__graft_entry__`` and by the CPU-baseline leg of ``bench.py``; never by the
 product package.  It shares no code with the CUDA library.  See
-``gat_oracle.c`` for what it computes and which passages it follows.
+``gat_oracle.c`` (fused GAT attention) and ``spmm_oracle.c`` (GCN / GraphConv
+propagation) for what each computes and which passages it follows.
 
 Arrays: ``h`` and ``dout`` are float32 ``[N, H, D]``, uint16 bit patterns of
 bfloat16 ``[N, H, D]``, or float64 (finite-difference checks); ``a_src`` /
@@ -21,6 +22,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gat_oracle.c")
+_SOURCES = ["gat_oracle.c", "spmm_oracle.c"]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -28,12 +30,13 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile ``liboracle.so`` (gcc, OpenMP) next to this file when stale."""
+    srcs = [os.path.join(_HERE, f) for f in _SOURCES]
     if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB) >= os.path.getmtime(f) for f in srcs)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared",
-                           _SRC, "-o", tmp, "-lm"])
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared"] + srcs +
+                          ["-o", tmp, "-lm"])
     os.replace(tmp, _LIB)
     return _LIB
 
@@ -52,6 +55,13 @@ def _bind(path: str):
     lib.oracle_gat_backward_rows.restype = i32
     lib.oracle_gat_att_grads.argtypes = common + [P, P, P, P]
     lib.oracle_gat_att_grads.restype = i32
+    spmm = [i64, P, P, i64, i32, P, i32]
+    lib.oracle_spmm_forward.argtypes = spmm + [i64, P, P, P]
+    lib.oracle_spmm_forward.restype = i32
+    lib.oracle_spmm_backward.argtypes = spmm + [P, P]
+    lib.oracle_spmm_backward.restype = i32
+    lib.oracle_spmm_backward_rows.argtypes = spmm + [i64, P, P, P]
+    lib.oracle_spmm_backward_rows.restype = i32
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     return lib
@@ -66,19 +76,26 @@ def _load():
         return _lib
 
 
-def compile_variant(source_text: str, out_path: str) -> str:
-    """Compile a modified copy of the oracle source (used by tests that plant a
-    mistake in the oracle to show that the pins catch it)."""
-    src = out_path + ".c"
-    with open(src, "w") as f:
-        f.write(source_text)
-    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared",
-                           src, "-o", out_path, "-lm"])
+def compile_variant(source_text: str, out_path: str, name: str = "gat_oracle.c") -> str:
+    """Compile the oracle library with the source file `name` replaced by a
+    modified copy (used by tests that plant a mistake in the oracle to show
+    that the pins catch it)."""
+    srcs = []
+    for f in _SOURCES:
+        if f == name:
+            src = out_path + "." + f
+            with open(src, "w") as fh:
+                fh.write(source_text)
+            srcs.append(src)
+        else:
+            srcs.append(os.path.join(_HERE, f))
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared"] + srcs +
+                          ["-o", out_path, "-lm"])
     return out_path
 
 
-def source_text() -> str:
-    with open(_SRC) as f:
+def source_text(name: str = "gat_oracle.c") -> str:
+    with open(os.path.join(_HERE, name)) as f:
         return f.read()
 
 
@@ -176,6 +193,60 @@ class Oracle:
         return dict(dh=dh, dh_mag=dh_mag)
 
 
+    # ---- SpMM family (spmm_oracle.c) ----------------------------------------
+
+    NORMS = {"sum": 0, "mean": 1, "sym": 2}
+
+    def spmm_forward(self, row_ptr, col, x, norm, sel=None, with_mag=False):
+        """out = A~ x for x [N, F] (or [N, H, D], flattened per node)."""
+        row_ptr, col, x, n, F, dt = _prep_rows(row_ptr, col, x)
+        sel = _sel(sel)
+        m = n if sel is None else len(sel)
+        out = np.empty((m, F), np.float64)
+        mag = np.empty((m, F), np.float64) if with_mag else None
+        rc = self.lib.oracle_spmm_forward(n, _p(row_ptr), _p(col), F, dt, _p(x),
+                                          self.NORMS[norm], 0 if sel is None else len(sel),
+                                          _p(sel), _p(out), _p(mag))
+        _check(rc, "spmm_forward")
+        return dict(out=out, out_mag=mag)
+
+    def spmm_backward(self, row_ptr, col, dout, norm, with_mag=False):
+        """dx = A~^T dout over the whole graph."""
+        row_ptr, col, dout, n, F, dt = _prep_rows(row_ptr, col, dout)
+        dx = np.empty((n, F), np.float64)
+        mag = np.empty((n, F), np.float64) if with_mag else None
+        rc = self.lib.oracle_spmm_backward(n, _p(row_ptr), _p(col), F, dt, _p(dout),
+                                           self.NORMS[norm], _p(dx), _p(mag))
+        _check(rc, "spmm_backward")
+        return dict(dx=dx, dx_mag=mag)
+
+    def spmm_backward_rows(self, row_ptr, col, dout, norm, sel, with_mag=False):
+        """dx rows of the listed (distinct) nodes only."""
+        row_ptr, col, dout, n, F, dt = _prep_rows(row_ptr, col, dout)
+        sel = _sel(sel)
+        dx = np.empty((len(sel), F), np.float64)
+        mag = np.empty((len(sel), F), np.float64) if with_mag else None
+        rc = self.lib.oracle_spmm_backward_rows(n, _p(row_ptr), _p(col), F, dt, _p(dout),
+                                                self.NORMS[norm], len(sel), _p(sel), _p(dx),
+                                                _p(mag))
+        _check(rc, "spmm_backward_rows")
+        return dict(dx=dx, dx_mag=mag)
+
+
+def _prep_rows(row_ptr, col, x):
+    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    col = np.ascontiguousarray(col, dtype=np.int32)
+    x = np.ascontiguousarray(x)
+    dt = {np.dtype(np.float32): 0, np.dtype(np.uint16): 1, np.dtype(np.float64): 2}.get(x.dtype)
+    if dt is None:
+        raise TypeError("features must be float32, float64 or bfloat16 bit patterns (uint16)")
+    n = x.shape[0]
+    F = int(np.prod(x.shape[1:])) if x.ndim > 1 else 1
+    if len(row_ptr) != n + 1:
+        raise ValueError("row_ptr must have N + 1 entries")
+    return row_ptr, col, x.reshape(n, F), n, F, dt
+
+
 def _p(a):
     return None if a is None else ctypes.c_void_p(a.ctypes.data)
 
@@ -219,3 +290,6 @@ forward = _default.forward
 node_stats = _default.node_stats
 backward = _default.backward
 backward_rows = _default.backward_rows
+spmm_forward = _default.spmm_forward
+spmm_backward = _default.spmm_backward
+spmm_backward_rows = _default.spmm_backward_rows
