@@ -58,11 +58,12 @@ WsLayout ws_layout(const gnn_graph* g, const Shape& s) {
   L.dst_part = take(size_t(g->csr.n_hub_chunks) * s.H * 16);
   L.src_acc = take(size_t(g->csc.n_hub_chunks) * HD * 4);
   L.src_sum = take(size_t(g->csc.n_hub_chunks) * s.H * 4);
-  // enough blocks to fill the GPU (8 per SM on 152 SMs), each summing at
-  // least 64 nodes per warp before its float64 fold
-  int64_t blocks = (g->n + 511) / 512;
+  // attention-vector partial sums: up to 8 blocks per SM, each warp summing
+  // at least 16 nodes before its block's float64 fold
+  const int64_t cap = int64_t(g->sm_count > 0 ? g->sm_count : 1) * 8;
+  int64_t blocks = (g->n + 127) / 128;
   if (blocks < 1) blocks = 1;
-  if (blocks > 1216) blocks = 1216;
+  if (blocks > cap) blocks = cap;
   L.da_blocks = int(blocks);
   L.da_part = take(size_t(blocks) * 2 * HD * 8);
   L.bwd_total = off;
@@ -288,6 +289,57 @@ gnn_status gat_agg_backward(const gnn_graph* g, int H, int D, gnn_dtype dtype, c
                             float* da_dst, void* ws, size_t ws_bytes, void* stream) {
   return gat_agg_backward_timed(g, H, D, dtype, h, a_src, a_dst, slope, lse, dout, dh, da_src,
                                 da_dst, ws, ws_bytes, stream, nullptr, 0);
+}
+
+}  // extern "C"
+
+// ---- SpMM-family propagation ---------------------------------------------
+
+namespace {
+
+// A row of F elements as F * size / 16 one-vector "heads".
+gnn_status spmm_shape(const gnn_graph* g, int F, gnn_dtype dt, Shape* s) {
+  if (!g || F < 1 || (dt != GNN_F32 && dt != GNN_BF16)) return GNN_ERR_INVALID_ARG;
+  const int64_t bytes = int64_t(F) * (dt == GNN_F32 ? 4 : 2);
+  if (bytes % 16 || bytes > 2048) return GNN_ERR_UNSUPPORTED;
+  return gnn::make_shape(int(bytes / 16), dt == GNN_F32 ? 4 : 8, dt, s) ? GNN_OK
+                                                                         : GNN_ERR_UNSUPPORTED;
+}
+
+gnn_status spmm_call(const gnn_graph* g, int F, gnn_dtype dt, gnn_norm norm, const void* x,
+                     void* out, void* ws, size_t ws_bytes, void* stream, bool transpose) {
+  Shape s;
+  gnn_status r = spmm_shape(g, F, dt, &s);
+  if (r != GNN_OK) return r;
+  if (norm != GNN_NORM_SUM && norm != GNN_NORM_MEAN && norm != GNN_NORM_SYM)
+    return GNN_ERR_INVALID_ARG;
+  if (g->n == 0) return GNN_OK;
+  if (!x || !out || !aligned(x, 16) || !aligned(out, 16)) return GNN_ERR_INVALID_ARG;
+  if (ws_bytes < gnn::spmm_ws_bytes(g, s)) return GNN_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned(ws, 256)) return GNN_ERR_INVALID_ARG;
+  return from_cuda(gnn::launch_spmm(g, s, dt, int(norm), transpose, x, out,
+                                    static_cast<char*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gcn_agg_workspace_bytes(const gnn_graph* g, int F, gnn_dtype dtype) {
+  Shape s;
+  if (spmm_shape(g, F, dtype, &s) != GNN_OK) return 0;
+  return gnn::spmm_ws_bytes(g, s);
+}
+
+gnn_status gcn_agg_forward(const gnn_graph* g, int F, gnn_dtype dtype, gnn_norm norm,
+                           const void* x, void* out, void* ws, size_t ws_bytes, void* stream) {
+  return spmm_call(g, F, dtype, norm, x, out, ws, ws_bytes, stream, false);
+}
+
+gnn_status gcn_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, gnn_norm norm,
+                            const void* dout, void* dx, void* ws, size_t ws_bytes,
+                            void* stream) {
+  return spmm_call(g, F, dtype, norm, dout, dx, ws, ws_bytes, stream, true);
 }
 
 gnn_status gnn_check_device_error(const gnn_graph* g, void* stream, int32_t* info) {

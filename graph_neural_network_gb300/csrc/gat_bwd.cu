@@ -546,11 +546,15 @@ __global__ void __launch_bounds__(kThreads) bwd_src_merge(const BwdArgs A) {
 // ---------------------------------------------------------------------------
 
 // Block b sums ds_src(n) h_n and ds_dst(n) h_n over its nodes n = b, b + B,
-// ... (per sub-group: every G-th of them) in float32, then folds its warps'
-// and sub-groups' sums in float64 in a fixed order into da_part[b].
+// ... (per sub-group: every G-th of them, kDaRows rows in flight) in
+// float32, then folds its warps' and sub-groups' sums in float64 in a fixed
+// order into da_part[b].
+constexpr int kDaRows = 4;
+
 template <typename T, int NV>
 __global__ void __launch_bounds__(kThreads) da_partial(const BwdArgs A) {
   constexpr int V = VecOf<T>::n;
+  constexpr int U = kDaRows;
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
   const int H = A.s.H;
@@ -560,21 +564,32 @@ __global__ void __launch_bounds__(kThreads) da_partial(const BwdArgs A) {
   for (int v = 0; v < NV; ++v)
 #pragma unroll
     for (int c = 0; c < V; ++c) s_acc[v][c] = d_acc[v][c] = 0.f;
-  const int64_t lanes_per_step = int64_t(A.da_blocks) * kWarps * L.G;
-  for (int64_t n = (int64_t(blockIdx.x) * kWarps + wid) * L.G + L.g; n < A.n; n += lanes_per_step) {
-    float x[NV][V];
-    load_row<T, NV>(A.h, n, A.s, L, x);
+  const float* dsd = reinterpret_cast<const float*>(A.stats);  // .w of each record
+  const int64_t stride = int64_t(A.da_blocks) * kWarps * L.G;
+  for (int64_t n0 = (int64_t(blockIdx.x) * kWarps + wid) * L.G + L.g; n0 < A.n;
+       n0 += U * stride) {
+    uint4 raw[U][NV];
+    float ds[U][NV], dd[U][NV];
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      if (!L.ok[v]) continue;
-      const float ds = A.ds_src[n * H + L.k[v]];
-      const float dd = A.stats[n * H + L.k[v]].w;
+    for (int u = 0; u < U; ++u) {
+      const int64_t n = n0 + u * stride;
 #pragma unroll
-      for (int c = 0; c < V; ++c) {
-        s_acc[v][c] = fmaf(ds, x[v][c], s_acc[v][c]);
-        d_acc[v][c] = fmaf(dd, x[v][c], d_acc[v][c]);
+      for (int v = 0; v < NV; ++v) {
+        const bool ok = n < A.n && L.ok[v];
+        raw[u][v] = ok ? ld16(row_base<T>(A.h, n, A.s.rv) + 16 * L.q[v]) : make_uint4(0, 0, 0, 0);
+        ds[u][v] = ok ? __ldg(A.ds_src + n * H + L.k[v]) : 0.f;
+        dd[u][v] = ok ? __ldg(dsd + (n * H + L.k[v]) * 4 + 3) : 0.f;
       }
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        float x[V];
+        unpack<T>(raw[u][v], x);
+        axpy<V>(s_acc[v], ds[u][v], x);
+        axpy<V>(d_acc[v], dd[u][v], x);
+      }
   }
   extern __shared__ __align__(16) unsigned char smem[];
   float* buf = reinterpret_cast<float*>(smem);  // [kWarps * G][2][row_f]
@@ -598,15 +613,24 @@ __global__ void __launch_bounds__(kThreads) da_partial(const BwdArgs A) {
   }
 }
 
-__global__ void da_final(const double* part, int blocks, int row_f, float* da_src, float* da_dst) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+// One warp per output element: lane l sums the block partials l, l + 32, ...
+// in order, then a fixed butterfly adds the 32 lane sums.
+__global__ void __launch_bounds__(kThreads) da_final(const double* part, int blocks, int row_f,
+                                                     float* da_src, float* da_dst) {
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (t >= 2 * row_f) return;
   double s = 0.0;
-  for (int b = 0; b < blocks; ++b) s += part[int64_t(b) * 2 * row_f + t];
-  if (t < row_f)
-    da_src[t] = float(s);
-  else
-    da_dst[t - row_f] = float(s);
+#pragma unroll 8
+  for (int b = lane; b < blocks; b += 32) s += part[int64_t(b) * 2 * row_f + t];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+  if (lane == 0) {
+    if (t < row_f)
+      da_src[t] = float(s);
+    else
+      da_dst[t - row_f] = float(s);
+  }
 }
 
 template <typename K>
@@ -673,8 +697,8 @@ cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t 
     da_partial<T, NV><<<unsigned(A.da_blocks), kThreads, smem, st>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark(6);
-    da_final<<<unsigned((2 * row_f + 127) / 128), 128, 0, st>>>(A.da_part, A.da_blocks, row_f,
-                                                                A.da_src, A.da_dst);
+    da_final<<<unsigned((2 * row_f + kWarps - 1) / kWarps), kThreads, 0, st>>>(
+        A.da_part, A.da_blocks, row_f, A.da_src, A.da_dst);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark(7);
   }
