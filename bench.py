@@ -52,6 +52,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     p.add_argument("--impl", choices=["gnnagg", "reference"], default="gnnagg")
+    p.add_argument("--op", choices=["gat", "gcn"], default="gat",
+                   help="gat: fused GAT attention aggregation (the headline); "
+                        "gcn: SpMM-family propagation A~ x with the symmetric normalisation")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=12.0,
@@ -485,6 +488,76 @@ def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev,
             "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+def run_gcn(args, rank, world):
+    """SpMM-family propagation on the same workload: a step is out = A~ x
+    (CSR) plus dx = A~^T dout (cached CSC), norm "sym", features [N, H*D]."""
+    import torch
+    import graph_neural_network_gb300 as gnn
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w, rp, ci, h_np, _, _, dout_np = load_workload(args.config)
+    n, e, F = len(rp) - 1, len(ci), w.H * w.D
+    s = 4 if w.dtype == "f32" else 2
+
+    def dev_feat(x):
+        x = np.ascontiguousarray(x).reshape(n, F)
+        t = torch.from_numpy(x.view(np.int16) if w.dtype == "bf16" else x).to(dev)
+        return t.view(torch.bfloat16) if w.dtype == "bf16" else t
+
+    g = gnn.Graph(torch.from_numpy(rp).to(dev), torch.from_numpy(ci).to(dev))
+    x, dout = dev_feat(h_np), dev_feat(dout_np)
+    out, dx = torch.empty_like(x), torch.empty_like(x)
+    ws = torch.empty(g._lib.gcn_agg_workspace_bytes(g.handle, F, 0 if w.dtype == "f32" else 1),
+                     dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        gnn.gcn_forward(g, x, "sym", out=out, ws=ws)
+        gnn.gcn_backward(g, dout, "sym", dx=dx, ws=ws)
+    torch.cuda.synchronize()
+    gnn.check_device_error(g)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.2)
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        gnn.gcn_forward(g, x, "sym", out=out, ws=ws)
+        ev[k][1].record(stream)
+        gnn.gcn_backward(g, dout, "sym", dx=dx, ws=ws)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    gnn.check_device_error(g)
+    t_f = sum(a.elapsed_time(b) for a, b, _ in ev) / K
+    t_b = sum(b.elapsed_time(c) for _, b, c in ev) / K
+    per_call = 4 * (n + 1) + 4 * e + s * e * F + s * n * F   # indices, gathered rows, written rows
+    peak, peak_kind = peaks()
+    line = {"metric": "GEdge/s fwd and fwd+bwd GCN propagation (sym); achieved HBM GB/s vs roofline",
+            "op": "gcn", "value": world * e / ((t_f + t_b) * 1e-3) / 1e9, "unit": "GEdge/s",
+            "fwd_value": world * e / (t_f * 1e-3) / 1e9, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": t_f + t_b, "fwd_ms": t_f, "bwd_ms": t_b,
+            "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "n_nodes": n, "n_edges": e, "F": F,
+                       "feature_dtype": w.dtype,
+                       "l2": f"flushed before every step ({flush.numel() >> 20} MiB write)"},
+            "roofline": {"bound": "hbm", "kernel": "gcn_agg_forward / gcn_agg_backward calls",
+                         "achieved_fwd": per_call / (t_f * 1e-3) / 1e9,
+                         "achieved_bwd": per_call / (t_b * 1e-3) / 1e9, "peak": peak,
+                         "unit": "GB/s", "frac_fwd": per_call / (t_f * 1e-3) / 1e9 / peak,
+                         "frac_bwd": per_call / (t_b * 1e-3) / 1e9 / peak,
+                         "algorithmic_bytes": per_call, "peak_source": peak_kind},
+            "clocks": clocks}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -497,6 +570,8 @@ def main(argv=None):
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
     try:
+        if args.op == "gcn":
+            return run_gcn(args, rank, world)
         return run_gnnagg(args, rank, world)
     finally:
         if world > 1:

@@ -9,6 +9,12 @@ kernels do all the work.
     dh, da_src, da_dst = gat_backward(g, h, a_src, a_dst, 0.2, lse, dout)
 
 ``GATAggregate`` wraps the pair as a torch.autograd.Function.
+
+The SpMM-family propagation of GCN / GraphConv layers (out = A~ x, norm
+"sum", "mean" or "sym") runs on the same prepared graph:
+
+    out = gcn_forward(g, x, "sym")                 # x [N, F]
+    dx = gcn_backward(g, dout, "sym")              # A~^T dout over the cached CSC
 """
 from __future__ import annotations
 
@@ -20,7 +26,8 @@ from . import _native
 from ._native import GnnError, Tiling
 
 __all__ = ["Graph", "gat_forward", "gat_backward", "GATAggregate", "GnnError", "Tiling",
-           "check_device_error", "default_tiling"]
+           "check_device_error", "default_tiling", "gcn_forward", "gcn_backward",
+           "GCNAggregate"]
 
 
 def _ptr(t):
@@ -184,6 +191,57 @@ def gat_backward(g: Graph, h: torch.Tensor, a_src: torch.Tensor, a_dst: torch.Te
                                  _ptr(da_dst), _ptr(ws), ws.numel(), _stream(stream, h.device))
     _native.check(rc, "gat_agg_backward")
     return dh, da_src, da_dst
+
+
+def _row_width(g: Graph, x: torch.Tensor, name: str) -> int:
+    if x.dim() < 2 or x.shape[0] != g.n or not x.is_cuda or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor [N, ...] with N = {g.n}")
+    F = 1
+    for d in x.shape[1:]:
+        F *= d
+    return F
+
+
+def _gcn_call(fn, g, x, norm, out, ws, stream, what):
+    F = _row_width(g, x, "features")
+    dt = _dtype_code(x.dtype)
+    if norm not in _native.NORMS:
+        raise ValueError(f"norm must be one of {sorted(_native.NORMS)}")
+    if out is None:
+        out = torch.empty_like(x)
+    if ws is None:
+        n = g._lib.gcn_agg_workspace_bytes(g.handle, F, dt)
+        if n == 0:
+            raise GnnError(_native.ERR_UNSUPPORTED, f"(F={F}, {x.dtype})")
+        ws = torch.empty(n, dtype=torch.uint8, device=x.device)
+    rc = fn(g.handle, F, dt, _native.NORMS[norm], _ptr(x), _ptr(out), _ptr(ws), ws.numel(),
+            _stream(stream, x.device))
+    _native.check(rc, what)
+    return out
+
+
+def gcn_forward(g: Graph, x: torch.Tensor, norm: str = "sym", out=None, ws=None, stream=None):
+    """out = A~ x (x [N, ...] float32 or bfloat16, features flattened per node)."""
+    return _gcn_call(g._lib.gcn_agg_forward, g, x, norm, out, ws, stream, "gcn_agg_forward")
+
+
+def gcn_backward(g: Graph, dout: torch.Tensor, norm: str = "sym", dx=None, ws=None, stream=None):
+    """dx = A~^T dout."""
+    return _gcn_call(g._lib.gcn_agg_backward, g, dout, norm, dx, ws, stream, "gcn_agg_backward")
+
+
+class GCNAggregate(torch.autograd.Function):
+    """out = GCNAggregate.apply(graph, x, norm)."""
+
+    @staticmethod
+    def forward(ctx, g, x, norm):
+        ctx.g = g
+        ctx.norm = norm
+        return gcn_forward(g, x.contiguous(), norm)
+
+    @staticmethod
+    def backward(ctx, dout):
+        return None, gcn_backward(ctx.g, dout.contiguous(), ctx.norm), None
 
 
 def check_device_error(g: Graph, stream=None) -> int:

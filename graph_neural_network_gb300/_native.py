@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(HERE, "libgnnagg.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_INVALID_GRAPH = 0, 1, 2, 3
 ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_DEVICE_ASSERT, ERR_TIMEOUT = 4, 5, 6, 7
 F32, BF16 = 0, 1
+NORMS = {"sum": 0, "mean": 1, "sym": 2}  # gnn_norm
 
 # (name, restype, argtypes) of every exported symbol, in header order
 _P, _I64, _I32, _SZ, _F = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t,
@@ -40,6 +41,9 @@ SIGNATURES = [
                                       _P, _SZ, _P, _P, _I32]),
     ("gat_agg_forward_noalloc", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _F, _P, _P, _P]),
     ("gat_agg_forward_noalloc_capacity", _SZ, []),
+    ("gcn_agg_workspace_bytes", _SZ, [_P, _I32, _I32]),
+    ("gcn_agg_forward", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    ("gcn_agg_backward", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]),
     ("gnn_check_device_error", _I32, [_P, _P, _P]),
     ("gnn_status_string", ctypes.c_char_p, [_I32]),
     ("gnn_abi_version", _I32, []),

@@ -88,6 +88,14 @@ cudaError_t launch_node_scores(const Shape& s, gnn_dtype dt, const void* h, cons
                                const float* a_dst, int64_t n, float* ssrc, float* sdst,
                                int sm_count, cudaStream_t st);
 
+// SpMM-family propagation (spmm.cu): out = A~ x over the CSR, or A~^T x
+// over the CSC (transpose).  Workspace: counters, then the per-node
+// coefficients at kSpmmCoefOffset, then the hub partial sums.
+constexpr size_t kSpmmCoefOffset = 256;
+cudaError_t launch_spmm(const gnn_graph* g, const Shape& s, gnn_dtype dt, int norm, bool transpose,
+                        const void* x, void* out, char* ws, cudaStream_t st);
+size_t spmm_ws_bytes(const gnn_graph* g, const Shape& s);
+
 // Graph preparation (prepare.cu).
 gnn_status prepare_graph(gnn_graph* g, const int32_t* row_ptr, const int32_t* col,
                          char* buffer, size_t buffer_bytes, char* scratch, size_t scratch_bytes,

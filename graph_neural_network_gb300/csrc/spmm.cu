@@ -1,0 +1,356 @@
+// SpMM-family neighbour aggregation: the propagation out = A~ x of GCN /
+// GraphConv layers, H' = sigma(A~ H W) ("On Efficient Scaling of GNNs via
+// IO-Aware Layers Implementations", Technical Summary > Methodology,
+// SpMM-based convolutions), with W and sigma outside.  For the edge j -> i
+//   sum:  A~_ij = 1      mean: A~_ij = 1 / deg(i)
+//   sym:  A~_ij = 1 / sqrt(deg(i) deg(j))   (Kipf & Welling's D^-1/2 A D^-1/2)
+// deg = in-degree (CSR row length); a degree of 0 gives a coefficient of 0.
+// The backward pass dx = A~^T dout runs the same kernel over the cached CSC
+// transpose (same page: transposed adjacency cached for the backward pass),
+// so no atomics or scatters are needed and results are reproducible bit for
+// bit.
+//
+// A~ factors as diag(c_out) A diag(c_in) with per-node coefficients (1/deg
+// or deg^-1/2) computed once per call from row_ptr; each edge gathers one
+// feature row and one float.  Degree-aware tiling as in the attention
+// kernels: light nodes get a warp, mid nodes a block (edge list staged in
+// shared memory by a bulk copy), hubs are split into edge chunks whose
+// partial sums a second kernel adds in chunk order.
+#include "device.cuh"
+
+namespace gnn {
+namespace {
+
+constexpr int kGrab = 4;  // light nodes a warp takes per counter access
+
+struct SpmmArgs {
+  Shape s;           // one 16-byte vector per "head": no per-head arithmetic
+  const int32_t* ptr;
+  const int32_t* idx;
+  const int32_t* light;
+  int64_t n_light;
+  const int4* items;
+  int64_t n_items;
+  const int4* hubs;
+  int64_t n_hubs;
+  const void* x;
+  void* out;
+  const float* c_out;  // [N] coefficient of the output node, or null (= 1)
+  const float* c_in;   // [N] coefficient of the gathered node, or null (= 1)
+  float* part;         // [hub chunks][row floats]
+  int* ctr;            // [0] block items taken, [1] light nodes taken
+  int32_t* err;
+  int col_off;         // bytes of shared memory before the per-warp sums
+};
+
+// Per-node coefficient from the in-degree: mode 1 -> 1/deg, mode 2 -> deg^-1/2
+// (0 where deg = 0).
+__global__ void spmm_coef(const int32_t* ptr, int64_t n, int mode, float* c) {
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < n;
+       v += int64_t(gridDim.x) * blockDim.x) {
+    const int d = ptr[v + 1] - ptr[v];
+    c[v] = d <= 0 ? 0.f : (mode == 1 ? 1.f / float(d) : rsqrtf(float(d)));
+  }
+}
+
+template <int U>
+__device__ __forceinline__ void batch_ids(const int32_t* cols, int colbase, int beg, int end,
+                                          int g, int G, int (&j)[U]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = beg + u * G + g;
+    j[u] = e < end ? cols[e - colbase] : -1;
+  }
+}
+
+// acc += c_in(j) x_j over the edges beg + g, beg + g + G, ... < end.
+template <typename T, int NV>
+__device__ __forceinline__ void spmm_edges(const SpmmArgs& A, const Lane<NV>& L,
+                                           const int32_t* cols, int colbase, int beg, int end,
+                                           int (&jn)[kUnroll], float (&acc)[NV][VecOf<T>::n]) {
+  constexpr int V = VecOf<T>::n;
+  constexpr int U = kUnroll;
+  const int step = L.G * U;
+  for (int base = beg; base < end; base += step) {
+    int j[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) j[u] = jn[u];
+    uint4 raw[U][NV];
+    float w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+        raw[u][v] = (j[u] >= 0 && L.ok[v]) ? ld16(row_base<T>(A.x, j[u], A.s.rv) + 16 * L.q[v])
+                                           : make_uint4(0, 0, 0, 0);
+      w[u] = j[u] < 0 ? 0.f : (A.c_in ? __ldg(A.c_in + j[u]) : 1.f);
+    }
+    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        float xv[V];
+        unpack<T>(raw[u][v], xv);
+        axpy<V>(acc[v], w[u], xv);
+      }
+  }
+}
+
+template <typename T, int NV>
+__device__ __forceinline__ void zero(float (&acc)[NV][VecOf<T>::n]) {
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int c = 0; c < VecOf<T>::n; ++c) acc[v][c] = 0.f;
+}
+
+// Sum the accumulators of the warp's sub-groups (every lane ends with the total).
+template <typename T, int NV>
+__device__ __forceinline__ void subgroup_sums(const Shape& s, float (&acc)[NV][VecOf<T>::n]) {
+  for (int o = s.lpr; o < 32; o <<= 1)
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int c = 0; c < VecOf<T>::n; ++c) acc[v][c] += __shfl_xor_sync(kFull, acc[v][c], o);
+}
+
+// out_node = c_out(node) * acc.
+template <typename T, int NV>
+__device__ __forceinline__ void write_row(const SpmmArgs& A, const Lane<NV>& L, int64_t node,
+                                          const float (&acc)[NV][VecOf<T>::n]) {
+  constexpr int V = VecOf<T>::n;
+  const float c = A.c_out ? __ldg(A.c_out + node) : 1.f;
+  char* orow = reinterpret_cast<char*>(A.out) + node * int64_t(A.s.rv) * 16;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    if (!L.ok[v]) continue;
+    float y[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) y[k] = acc[v][k];
+    scale<V>(y, c);
+    st16(orow + 16 * L.q[v], pack<T>(y));
+  }
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) spmm_main(const SpmmArgs A) {
+  constexpr int V = VecOf<T>::n;
+  const Lane<NV> L(A.s);
+  const int wid = threadIdx.x >> 5;
+  const int row_f = A.s.rv * V;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_item;
+  float acc[NV][V];
+
+  // ---- block items: mid nodes and hub chunks -----------------------------
+  if (A.n_items > 0) {
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int32_t* cols = reinterpret_cast<int32_t*>(smem + 16);
+    float* wacc = reinterpret_cast<float*>(smem + A.col_off);  // [kWarps][row_f]
+    uint32_t parity = 0;
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    for (;;) {
+      if (threadIdx.x == 0) s_item = atomicAdd(A.ctr + 0, 1);
+      __syncthreads();
+      const int it_i = s_item;
+      if (it_i >= A.n_items) break;
+      const int4 it = A.items[it_i];
+      if (!stage_edges(cols, A.idx, it.y, it.z, bar, parity, A.err)) return;
+      const int per = (it.z - it.y + kWarps - 1) / kWarps;
+      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      const int colbase = it.y & ~3;
+      int jn[kUnroll];
+      batch_ids<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
+      zero<T, NV>(acc);
+      spmm_edges<T, NV>(A, L, cols, colbase, wb, we, jn, acc);
+      subgroup_sums<T, NV>(A.s, acc);
+      if (L.g == 0)
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+          if (L.ok[v])
+#pragma unroll
+            for (int c = 0; c < V; ++c) wacc[wid * row_f + L.q[v] * V + c] = acc[v][c];
+      __syncthreads();
+      if (wid == 0 && L.g == 0) {
+        // warp 0 adds the warps' sums in warp order
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+          for (int c = 0; c < V; ++c) {
+            float t = 0.f;
+            if (L.ok[v])
+              for (int w = 0; w < kWarps; ++w) t += wacc[w * row_f + L.q[v] * V + c];
+            acc[v][c] = t;
+          }
+        if (it.w < 0) {
+          write_row<T, NV>(A, L, it.x, acc);
+        } else {
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            if (!L.ok[v]) continue;
+            float* pa = A.part + int64_t(it.w) * row_f + L.q[v] * V;
+#pragma unroll
+            for (int c4 = 0; c4 < V; c4 += 4)
+              *reinterpret_cast<float4*>(pa + c4) =
+                  make_float4(acc[v][c4], acc[v][c4 + 1], acc[v][c4 + 2], acc[v][c4 + 3]);
+          }
+        }
+      }
+      __syncthreads();  // shared memory is reused by the next item
+    }
+  }
+
+  // ---- light nodes: one warp each, pulled kGrab at a time ----------------
+  for (;;) {
+    int t0 = 0;
+    if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
+    t0 = __shfl_sync(kFull, t0, 0);
+    if (t0 >= A.n_light) break;
+    int my_i = -1, my_b = 0, my_e = 0;
+    if (L.lane < kGrab && t0 + L.lane < A.n_light) {
+      my_i = A.light[t0 + L.lane];
+      my_b = A.ptr[my_i];
+      my_e = A.ptr[my_i + 1];
+    }
+    int i = __shfl_sync(kFull, my_i, 0);
+    int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
+    int jn[kUnroll];
+    batch_ids<kUnroll>(A.idx, 0, beg, end, L.g, L.G, jn);
+    for (int q = 0; q < kGrab && i >= 0; ++q) {
+      const int nq = (q + 1) & (kGrab - 1);
+      const int i2 = q + 1 < kGrab ? __shfl_sync(kFull, my_i, nq) : -1;
+      const int b2 = __shfl_sync(kFull, my_b, nq);
+      const int e2 = __shfl_sync(kFull, my_e, nq);
+      int jn2[kUnroll];
+      batch_ids<kUnroll>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
+      zero<T, NV>(acc);
+      spmm_edges<T, NV>(A, L, A.idx, 0, beg, end, jn, acc);
+      subgroup_sums<T, NV>(A.s, acc);
+      if (L.g == 0) write_row<T, NV>(A, L, i, acc);
+      i = i2;
+      beg = b2;
+      end = e2;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) jn[u] = jn2[u];
+    }
+  }
+}
+
+// One warp per hub: add its chunk partials in chunk order.
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads) spmm_merge(const SpmmArgs A) {
+  constexpr int V = VecOf<T>::n;
+  const Lane<NV> L(A.s);
+  const int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (t >= A.n_hubs || L.g != 0) return;
+  const int4 hb = A.hubs[t];
+  const int row_f = A.s.rv * V;
+  float acc[NV][V];
+  zero<T, NV>(acc);
+  for (int c = 0; c < hb.z; ++c) {
+    const int64_t slot = int64_t(hb.y) + c;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      if (!L.ok[v]) continue;
+      const float* pa = A.part + slot * row_f + L.q[v] * V;
+#pragma unroll
+      for (int c4 = 0; c4 < V; c4 += 4) {
+        const float4 p = *reinterpret_cast<const float4*>(pa + c4);
+        acc[v][c4] += p.x;
+        acc[v][c4 + 1] += p.y;
+        acc[v][c4 + 2] += p.z;
+        acc[v][c4 + 3] += p.w;
+      }
+    }
+  }
+  write_row<T, NV>(A, L, hb.x, acc);
+}
+
+template <typename T, int NV>
+cudaError_t launch_t(const SpmmArgs& A, int sm_count, cudaStream_t st) {
+  constexpr int V = VecOf<T>::n;
+  cudaError_t e;
+  if (A.n_items + A.n_light > 0) {
+    const size_t smem = size_t(A.col_off) + size_t(kWarps) * A.s.rv * V * 4;
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(spmm_main<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(smem))) != cudaSuccess)
+      return e;
+    const int64_t work = A.n_items + (A.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
+    const int64_t cap = persistent_blocks(spmm_main<T, NV>, smem, sm_count);
+    const int64_t blocks = work < cap ? work : cap;
+    spmm_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (A.n_hubs > 0) {
+    spmm_merge<T, NV><<<unsigned((A.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_spmm(const gnn_graph* g, const Shape& s, gnn_dtype dt, int norm, bool transpose,
+                        const void* x, void* out, char* ws, cudaStream_t st) {
+  const Dir& d = transpose ? g->csc : g->csr;
+  SpmmArgs A{};
+  A.s = s;
+  A.ptr = d.ptr;
+  A.idx = d.idx;
+  A.light = d.light;
+  A.n_light = d.n_light;
+  A.items = d.items;
+  A.n_items = d.n_items;
+  A.hubs = d.hubs;
+  A.n_hubs = d.n_hubs;
+  A.x = x;
+  A.out = out;
+  A.ctr = reinterpret_cast<int*>(ws);
+  float* coef = reinterpret_cast<float*>(ws + kSpmmCoefOffset);
+  A.part = reinterpret_cast<float*>(ws + kSpmmCoefOffset + align_up(size_t(g->n) * 4, 256));
+  A.err = g->err;
+  A.col_off = int(16 + align_up(size_t(d.max_item + 4) * 4, 16));
+  // A~ = diag(c_out) A diag(c_in): forward over the CSR, A~^T over the CSC
+  if (norm == GNN_NORM_MEAN) {
+    (transpose ? A.c_in : A.c_out) = coef;
+  } else if (norm == GNN_NORM_SYM) {
+    A.c_in = coef;
+    A.c_out = coef;
+  }
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), st)) != cudaSuccess) return e;
+  if (norm != GNN_NORM_SUM && g->n > 0) {
+    int64_t blocks = (g->n + kThreads - 1) / kThreads;
+    const int64_t cap = int64_t(g->sm_count > 0 ? g->sm_count : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    spmm_coef<<<unsigned(blocks), kThreads, 0, st>>>(g->csr.ptr, g->n,
+                                                     norm == GNN_NORM_MEAN ? 1 : 2, coef);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (dt == GNN_F32) {
+    switch (s.nv) {
+      case 1: return launch_t<float, 1>(A, g->sm_count, st);
+      case 2: return launch_t<float, 2>(A, g->sm_count, st);
+      case 4: return launch_t<float, 4>(A, g->sm_count, st);
+    }
+  } else {
+    switch (s.nv) {
+      case 1: return launch_t<__nv_bfloat16, 1>(A, g->sm_count, st);
+      case 2: return launch_t<__nv_bfloat16, 2>(A, g->sm_count, st);
+      case 4: return launch_t<__nv_bfloat16, 4>(A, g->sm_count, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+size_t spmm_ws_bytes(const gnn_graph* g, const Shape& s) {
+  int64_t chunks = g->csr.n_hub_chunks > g->csc.n_hub_chunks ? g->csr.n_hub_chunks
+                                                             : g->csc.n_hub_chunks;
+  const size_t row_f = size_t(s.rv) * 16 / s.esize;
+  return kSpmmCoefOffset + align_up(size_t(g->n) * 4, 256) +
+         align_up(size_t(chunks) * row_f * 4 + 1, 256);
+}
+
+}  // namespace gnn

@@ -210,6 +210,43 @@ gnn_status gat_agg_forward_noalloc(const gnn_graph* g, int H, int D, gnn_dtype d
 /* Size in bytes of the array gat_agg_forward_noalloc uses. */
 size_t gat_agg_forward_noalloc_capacity(void);
 
+/* ---- SpMM-family propagation (GCN / GraphConv) --------------------------
+ *
+ * out = A~ x for node features x[N][F], the propagation step of the layer
+ * H' = sigma(A~ H W) ("On Efficient Scaling of GNNs via IO-Aware Layers
+ * Implementations", Technical Summary > Methodology, SpMM-based
+ * convolutions; W and sigma are the caller's).  For each edge j -> i of the
+ * prepared graph (multi-edges with multiplicity):
+ *   GNN_NORM_SUM:  A~_ij = 1
+ *   GNN_NORM_MEAN: A~_ij = 1 / deg(i)
+ *   GNN_NORM_SYM:  A~_ij = 1 / sqrt(deg(i) deg(j))  (D^-1/2 A D^-1/2 of
+ *                  Kipf & Welling, ICLR 2017; add self-loops to the graph
+ *                  for their A + I)
+ * deg(v) = in-degree of v (length of CSR row v); a degree of 0 makes the
+ * coefficient 0.  The backward pass dx = A~^T dout walks the cached CSC
+ * transpose (same page: transposed adjacency cached for the backward
+ * pass); it is the only gradient (A~ does not depend on x).  Both passes
+ * use the degree-aware tiling of the attention kernels, write every output
+ * element, use no atomics on values and are bitwise reproducible.
+ * Shapes: F * sizeof(dtype) a multiple of 16 bytes, at most 2048 bytes.
+ * x, out, dout, dx: [N][F] dtype, device, 16-byte aligned; ws: device,
+ * 256-byte aligned, >= gcn_agg_workspace_bytes (counters, N per-node
+ * coefficients, hub-chunk partial sums).  Asynchronous on `stream`. */
+typedef enum { GNN_NORM_SUM = 0, GNN_NORM_MEAN = 1, GNN_NORM_SYM = 2 } gnn_norm;
+
+/* Workspace bytes of gcn_agg_forward / gcn_agg_backward (the same for both);
+ * 0 for an unsupported (F, dtype). */
+size_t gcn_agg_workspace_bytes(const gnn_graph* g, int F, gnn_dtype dtype);
+
+/* out [N][F] = A~ x. */
+gnn_status gcn_agg_forward(const gnn_graph* g, int F, gnn_dtype dtype, gnn_norm norm,
+                           const void* x, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* dx [N][F] = A~^T dout. */
+gnn_status gcn_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, gnn_norm norm,
+                            const void* dout, void* dx, void* ws, size_t ws_bytes,
+                            void* stream);
+
 /* Synchronises `stream`, reads and clears the graph's device status word.
  * Returns GNN_OK, GNN_ERR_TIMEOUT (a bounded wait on an asynchronous copy ran
  * out) or GNN_ERR_DEVICE_ASSERT; *info (may be NULL) receives the raw word. */

@@ -7,6 +7,7 @@ import torch
 
 import oracle
 import workload
+import gpu_util
 from gpu_util import assert_close, run_gpu, to_f64
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -54,3 +55,16 @@ def test_full_size_sampled_parity(idx):
     assert_close(to_f64(gpu["da_src_t"]), ag["da_src"], w.dtype, ag["da_src_mag"], "da_src")
     assert_close(to_f64(gpu["da_dst_t"]), ag["da_dst"], w.dtype, ag["da_dst_mag"], "da_dst")
     assert outdeg[top].max() > 4096 or idx == 2      # the CSC hub path was sampled
+    # SpMM-family propagation (symmetric normalisation) on the same graph and rows
+    import graph_neural_network_gb300 as gnn
+    g = gpu["graph"]
+    F = w.H * w.D
+    x = gpu_util.to_device(h.reshape(n, F), w.dtype)
+    dy = gpu_util.to_device(dout.reshape(n, F), w.dtype)
+    out = gnn.gcn_forward(g, x, "sym")
+    dx = gnn.gcn_backward(g, dy, "sym")
+    torch.cuda.synchronize()
+    sf = oracle.spmm_forward(rp, ci, h.reshape(n, F), "sym", sel=sel_f, with_mag=True)
+    assert_close(_rows(out, sel_f), sf["out"], w.dtype, sf["out_mag"], f"cfg{idx} gcn out")
+    sb = oracle.spmm_backward_rows(rp, ci, dout.reshape(n, F), "sym", sel_b, with_mag=True)
+    assert_close(_rows(dx, sel_b), sb["dx"], w.dtype, sb["dx_mag"], f"cfg{idx} gcn dx")
