@@ -3,8 +3,9 @@
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the smoke check in
 ``__graft_entry__`` and by the CPU-baseline leg of ``bench.py``; never by the
 product package.  It shares no code with the CUDA library.  See
-``gat_oracle.c`` (fused GAT attention) and ``spmm_oracle.c`` (GCN / GraphConv
-propagation) for what each computes and which passages it follows.
+``gat_oracle.c`` (fused GAT attention), ``spmm_oracle.c`` (GCN / GraphConv
+propagation) and ``reduce_oracle.c`` (max / min neighbourhood reduction) for
+what each computes and which passages it follows.
 
 Arrays: ``h`` and ``dout`` are float32 ``[N, H, D]``, uint16 bit patterns of
 bfloat16 ``[N, H, D]``, or float64 (finite-difference checks); ``a_src`` /
@@ -22,7 +23,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gat_oracle.c")
-_SOURCES = ["gat_oracle.c", "spmm_oracle.c"]
+_SOURCES = ["gat_oracle.c", "spmm_oracle.c", "reduce_oracle.c"]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +63,12 @@ def _bind(path: str):
     lib.oracle_spmm_backward.restype = i32
     lib.oracle_spmm_backward_rows.argtypes = spmm + [i64, P, P, P]
     lib.oracle_spmm_backward_rows.restype = i32
+    lib.oracle_reduce_forward.argtypes = [i64, P, P, i64, i32, P, i32, i64, P, P, P]
+    lib.oracle_reduce_forward.restype = i32
+    lib.oracle_reduce_backward.argtypes = [i64, i64, i32, P, P, P, P]
+    lib.oracle_reduce_backward.restype = i32
+    lib.oracle_reduce_backward_rows.argtypes = [i64, P, P, i64, i32, P, i32, P, i64, P, P, P]
+    lib.oracle_reduce_backward_rows.restype = i32
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     return lib
@@ -232,6 +239,51 @@ class Oracle:
         _check(rc, "spmm_backward_rows")
         return dict(dx=dx, dx_mag=mag)
 
+    # ---- reduction family (reduce_oracle.c) ---------------------------------
+
+    OPS = {"max": 0, "min": 1}
+
+    def reduce_forward(self, row_ptr, col, x, op, sel=None):
+        """out [N, F] (float64) and arg [N, F] (int32, -1 for no in-neighbours)."""
+        row_ptr, col, x, n, F, dt = _prep_rows(row_ptr, col, x)
+        sel = _sel(sel)
+        m = n if sel is None else len(sel)
+        out = np.empty((m, F), np.float64)
+        arg = np.empty((m, F), np.int32)
+        rc = self.lib.oracle_reduce_forward(n, _p(row_ptr), _p(col), F, dt, _p(x), self.OPS[op],
+                                            0 if sel is None else len(sel), _p(sel), _p(out),
+                                            _p(arg))
+        _check(rc, "reduce_forward")
+        return dict(out=out, arg=arg)
+
+    def reduce_backward(self, arg, dout, with_mag=False):
+        """dx [N, F] from the forward's arg and dout [N, F]."""
+        arg = np.ascontiguousarray(arg, np.int32)
+        dout = np.ascontiguousarray(dout)
+        n = arg.shape[0]
+        F = arg.size // max(1, n)
+        dt = {np.dtype(np.float32): 0, np.dtype(np.uint16): 1, np.dtype(np.float64): 2}[dout.dtype]
+        assert dout.size == arg.size
+        dx = np.empty((n, F), np.float64)
+        mag = np.empty((n, F), np.float64) if with_mag else None
+        rc = self.lib.oracle_reduce_backward(n, F, dt, _p(arg), _p(dout), _p(dx), _p(mag))
+        _check(rc, "reduce_backward")
+        return dict(dx=dx, dx_mag=mag)
+
+    def reduce_backward_rows(self, row_ptr, col, x, op, dout, sel, with_mag=False):
+        """dx rows of the listed (distinct) sources, recomputing the reductions."""
+        row_ptr, col, x, n, F, dt = _prep_rows(row_ptr, col, x)
+        dout = np.ascontiguousarray(dout).reshape(n, F)
+        assert dout.dtype == x.dtype
+        sel = _sel(sel)
+        dx = np.empty((len(sel), F), np.float64)
+        mag = np.empty((len(sel), F), np.float64) if with_mag else None
+        rc = self.lib.oracle_reduce_backward_rows(n, _p(row_ptr), _p(col), F, dt, _p(x),
+                                                  self.OPS[op], _p(dout), len(sel), _p(sel),
+                                                  _p(dx), _p(mag))
+        _check(rc, "reduce_backward_rows")
+        return dict(dx=dx, dx_mag=mag)
+
 
 def _prep_rows(row_ptr, col, x):
     row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int32)
@@ -293,3 +345,6 @@ backward_rows = _default.backward_rows
 spmm_forward = _default.spmm_forward
 spmm_backward = _default.spmm_backward
 spmm_backward_rows = _default.spmm_backward_rows
+reduce_forward = _default.reduce_forward
+reduce_backward = _default.reduce_backward
+reduce_backward_rows = _default.reduce_backward_rows
