@@ -3,9 +3,10 @@
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the smoke check in
 ``__graft_entry__`` and by the CPU-baseline leg of ``bench.py``; never by the
 product package.  It shares no code with the CUDA library.  See
-``gat_oracle.c`` (fused GAT attention), ``spmm_oracle.c`` (GCN / GraphConv
-propagation) and ``reduce_oracle.c`` (max / min neighbourhood reduction) for
-what each computes and which passages it follows.
+``gat_oracle.c`` (fused GAT attention), ``gatv2_oracle.c`` (fused GATv2
+attention), ``spmm_oracle.c`` (GCN / GraphConv propagation) and
+``reduce_oracle.c`` (max / min neighbourhood reduction) for what each
+computes and which passages it follows.
 
 Arrays: ``h`` and ``dout`` are float32 ``[N, H, D]``, uint16 bit patterns of
 bfloat16 ``[N, H, D]``, or float64 (finite-difference checks); ``a_src`` /
@@ -23,7 +24,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gat_oracle.c")
-_SOURCES = ["gat_oracle.c", "spmm_oracle.c", "reduce_oracle.c"]
+_SOURCES = ["gat_oracle.c", "spmm_oracle.c", "reduce_oracle.c", "gatv2_oracle.c"]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +70,13 @@ def _bind(path: str):
     lib.oracle_reduce_backward.restype = i32
     lib.oracle_reduce_backward_rows.argtypes = [i64, P, P, i64, i32, P, i32, P, i64, P, P, P]
     lib.oracle_reduce_backward_rows.restype = i32
+    v2 = [i64, P, P, i32, i32, i32, P, P, P, f64]
+    lib.oracle_gatv2_forward.argtypes = v2 + [i64, P, P, P, P, P]
+    lib.oracle_gatv2_forward.restype = i32
+    lib.oracle_gatv2_delta.argtypes = v2 + [P, i64, P, P]
+    lib.oracle_gatv2_delta.restype = i32
+    lib.oracle_gatv2_backward.argtypes = v2 + [P, i64, P, P, P, P, P, P, P]
+    lib.oracle_gatv2_backward.restype = i32
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     return lib
@@ -284,6 +292,61 @@ class Oracle:
         _check(rc, "reduce_backward_rows")
         return dict(dx=dx, dx_mag=mag)
 
+    # ---- GATv2 (gatv2_oracle.c) ---------------------------------------------
+
+    def gatv2_forward(self, row_ptr, col, xl, xr, att, slope, sel=None, with_mag=False,
+                      with_alpha_sum=False):
+        row_ptr, col, xl, att, _, n, H, D, dt = _prep(row_ptr, col, xl, att, att)
+        xr = _same(xr, xl)
+        sel = _sel(sel)
+        m = n if sel is None else len(sel)
+        out = np.empty((m, H, D), np.float64)
+        lse = np.empty((m, H), np.float64)
+        mag = np.empty((m, H, D), np.float64) if with_mag else None
+        asum = np.empty((m, H), np.float64) if with_alpha_sum else None
+        rc = self.lib.oracle_gatv2_forward(n, _p(row_ptr), _p(col), H, D, dt, _p(xl), _p(xr),
+                                           _p(att), float(slope), 0 if sel is None else len(sel),
+                                           _p(sel), _p(out), _p(lse), _p(mag), _p(asum))
+        _check(rc, "gatv2_forward")
+        return dict(out=out, lse=lse, out_mag=mag, alpha_sum=asum)
+
+    def gatv2_delta(self, row_ptr, col, xl, xr, att, slope, dout, sel=None):
+        row_ptr, col, xl, att, _, n, H, D, dt = _prep(row_ptr, col, xl, att, att)
+        xr, dout = _same(xr, xl), _same(dout, xl)
+        sel = _sel(sel)
+        m = n if sel is None else len(sel)
+        delta = np.empty((m, H), np.float64)
+        rc = self.lib.oracle_gatv2_delta(n, _p(row_ptr), _p(col), H, D, dt, _p(xl), _p(xr),
+                                         _p(att), float(slope), _p(dout),
+                                         0 if sel is None else len(sel), _p(sel), _p(delta))
+        _check(rc, "gatv2_delta")
+        return delta
+
+    def gatv2_backward(self, row_ptr, col, xl, xr, att, slope, dout, sel=None, with_mag=False):
+        """dxl, dxr (rows of sel, or all), datt (whole graph)."""
+        row_ptr, col, xl, att, _, n, H, D, dt = _prep(row_ptr, col, xl, att, att)
+        xr, dout = _same(xr, xl), _same(dout, xl)
+        sel = _sel(sel)
+        m = n if sel is None else len(sel)
+        dxl, dxr = np.empty((m, H, D)), np.empty((m, H, D))
+        datt = np.empty((H, D))
+        mags = [np.empty((m, H, D)), np.empty((m, H, D)), np.empty((H, D))] if with_mag \
+            else [None, None, None]
+        rc = self.lib.oracle_gatv2_backward(n, _p(row_ptr), _p(col), H, D, dt, _p(xl), _p(xr),
+                                            _p(att), float(slope), _p(dout),
+                                            0 if sel is None else len(sel), _p(sel), _p(dxl),
+                                            _p(dxr), _p(datt), *[_p(x) for x in mags])
+        _check(rc, "gatv2_backward")
+        return dict(dxl=dxl, dxr=dxr, datt=datt, dxl_mag=mags[0], dxr_mag=mags[1],
+                    datt_mag=mags[2])
+
+
+def _same(x, like):
+    x = np.ascontiguousarray(x)
+    if x.shape != like.shape or x.dtype != like.dtype:
+        raise ValueError("arrays must share shape and dtype")
+    return x
+
 
 def _prep_rows(row_ptr, col, x):
     row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int32)
@@ -348,3 +411,6 @@ spmm_backward_rows = _default.spmm_backward_rows
 reduce_forward = _default.reduce_forward
 reduce_backward = _default.reduce_backward
 reduce_backward_rows = _default.reduce_backward_rows
+gatv2_forward = _default.gatv2_forward
+gatv2_delta = _default.gatv2_delta
+gatv2_backward = _default.gatv2_backward
