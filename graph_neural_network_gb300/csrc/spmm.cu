@@ -237,6 +237,16 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) spmm_main(cons
   }
 }
 
+// s += x with the rounding error of the addition carried in c (Kahan's
+// compensated summation): a hub may have thousands of chunk partials, and
+// a plain running sum would lose accuracy with their number.
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
+  const float y = __fsub_rn(x, c);
+  const float t = __fadd_rn(s, y);
+  c = __fsub_rn(__fsub_rn(t, s), y);
+  s = t;
+}
+
 // One warp per hub: add its chunk partials in chunk order.
 template <typename T, int NV>
 __global__ void __launch_bounds__(kThreads) spmm_merge(const SpmmArgs A) {
@@ -246,8 +256,9 @@ __global__ void __launch_bounds__(kThreads) spmm_merge(const SpmmArgs A) {
   if (t >= A.n_hubs || L.g != 0) return;
   const int4 hb = A.hubs[t];
   const int row_f = A.s.rv * V;
-  float acc[NV][V];
+  float acc[NV][V], cmp[NV][V];
   zero<T, NV>(acc);
+  zero<T, NV>(cmp);
   for (int c = 0; c < hb.z; ++c) {
     const int64_t slot = int64_t(hb.y) + c;
 #pragma unroll
@@ -257,10 +268,10 @@ __global__ void __launch_bounds__(kThreads) spmm_merge(const SpmmArgs A) {
 #pragma unroll
       for (int c4 = 0; c4 < V; c4 += 4) {
         const float4 p = *reinterpret_cast<const float4*>(pa + c4);
-        acc[v][c4] += p.x;
-        acc[v][c4 + 1] += p.y;
-        acc[v][c4 + 2] += p.z;
-        acc[v][c4 + 3] += p.w;
+        kahan_add(acc[v][c4], cmp[v][c4], p.x);
+        kahan_add(acc[v][c4 + 1], cmp[v][c4 + 1], p.y);
+        kahan_add(acc[v][c4 + 2], cmp[v][c4 + 2], p.z);
+        kahan_add(acc[v][c4 + 3], cmp[v][c4 + 3], p.w);
       }
     }
   }
