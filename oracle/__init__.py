@@ -4,9 +4,10 @@ TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the smoke check in
 ``__graft_entry__`` and by the CPU-baseline leg of ``bench.py``; never by the
 product package.  It shares no code with the CUDA library.  See
 ``gat_oracle.c`` (fused GAT attention), ``gatv2_oracle.c`` (fused GATv2
-attention), ``spmm_oracle.c`` (GCN / GraphConv propagation) and
-``reduce_oracle.c`` (max / min neighbourhood reduction) for what each
-computes and which passages it follows.
+attention), ``transformer_oracle.c`` (graph-transformer attention),
+``spmm_oracle.c`` (GCN / GraphConv propagation) and ``reduce_oracle.c`` (max /
+min neighbourhood reduction) for what each computes and which passages it
+follows.
 
 Arrays: ``h`` and ``dout`` are float32 ``[N, H, D]``, uint16 bit patterns of
 bfloat16 ``[N, H, D]``, or float64 (finite-difference checks); ``a_src`` /
@@ -24,7 +25,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gat_oracle.c")
-_SOURCES = ["gat_oracle.c", "spmm_oracle.c", "reduce_oracle.c", "gatv2_oracle.c"]
+_SOURCES = ["gat_oracle.c", "spmm_oracle.c", "reduce_oracle.c", "gatv2_oracle.c",
+            "transformer_oracle.c"]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +79,11 @@ def _bind(path: str):
     lib.oracle_gatv2_delta.restype = i32
     lib.oracle_gatv2_backward.argtypes = v2 + [P, i64, P, P, P, P, P, P, P]
     lib.oracle_gatv2_backward.restype = i32
+    gt = [i64, P, P, i32, i32, i32, P, P, P, f64]
+    lib.oracle_gt_forward.argtypes = gt + [i64, P, P, P, P, P]
+    lib.oracle_gt_forward.restype = i32
+    lib.oracle_gt_backward.argtypes = gt + [P, i64, P, P, P, P, P, P, P]
+    lib.oracle_gt_backward.restype = i32
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     return lib
@@ -340,6 +347,42 @@ class Oracle:
         return dict(dxl=dxl, dxr=dxr, datt=datt, dxl_mag=mags[0], dxr_mag=mags[1],
                     datt_mag=mags[2])
 
+    # ---- graph transformer (transformer_oracle.c) ---------------------------
+
+    def gt_forward(self, row_ptr, col, q, key, val, scale, sel=None, with_mag=False,
+                   with_alpha_sum=False):
+        row_ptr, col, q, _, _, n, H, D, dt = _prep(row_ptr, col, q, np.zeros(q.shape[1:]),
+                                                   np.zeros(q.shape[1:]))
+        key, val = _same(key, q), _same(val, q)
+        sel = _sel(sel)
+        m = n if sel is None else len(sel)
+        out = np.empty((m, H, D), np.float64)
+        lse = np.empty((m, H), np.float64)
+        mag = np.empty((m, H, D), np.float64) if with_mag else None
+        asum = np.empty((m, H), np.float64) if with_alpha_sum else None
+        rc = self.lib.oracle_gt_forward(n, _p(row_ptr), _p(col), H, D, dt, _p(q), _p(key),
+                                        _p(val), float(scale), 0 if sel is None else len(sel),
+                                        _p(sel), _p(out), _p(lse), _p(mag), _p(asum))
+        _check(rc, "gt_forward")
+        return dict(out=out, lse=lse, out_mag=mag, alpha_sum=asum)
+
+    def gt_backward(self, row_ptr, col, q, key, val, scale, dout, sel=None, with_mag=False):
+        """dq, dkey, dval (rows of sel, or all nodes)."""
+        row_ptr, col, q, _, _, n, H, D, dt = _prep(row_ptr, col, q, np.zeros(q.shape[1:]),
+                                                   np.zeros(q.shape[1:]))
+        key, val, dout = _same(key, q), _same(val, q), _same(dout, q)
+        sel = _sel(sel)
+        m = n if sel is None else len(sel)
+        outs = [np.empty((m, H, D)) for _ in range(3)]
+        mags = [np.empty((m, H, D)) for _ in range(3)] if with_mag else [None] * 3
+        rc = self.lib.oracle_gt_backward(n, _p(row_ptr), _p(col), H, D, dt, _p(q), _p(key),
+                                         _p(val), float(scale), _p(dout),
+                                         0 if sel is None else len(sel), _p(sel),
+                                         *[_p(x) for x in outs], *[_p(x) for x in mags])
+        _check(rc, "gt_backward")
+        return dict(dq=outs[0], dkey=outs[1], dval=outs[2], dq_mag=mags[0], dkey_mag=mags[1],
+                    dval_mag=mags[2])
+
 
 def _same(x, like):
     x = np.ascontiguousarray(x)
@@ -414,3 +457,5 @@ reduce_backward_rows = _default.reduce_backward_rows
 gatv2_forward = _default.gatv2_forward
 gatv2_delta = _default.gatv2_delta
 gatv2_backward = _default.gatv2_backward
+gt_forward = _default.gt_forward
+gt_backward = _default.gt_backward
