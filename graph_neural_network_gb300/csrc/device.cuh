@@ -18,11 +18,19 @@ constexpr int kWarps = 8;      // warps per thread block in every aggregation ke
 constexpr int kThreads = kWarps * 32;
 constexpr int kUnroll = 4;     // edges in flight per lane and batch
 
-// Resident blocks per SM the main kernels are compiled for (register cap):
-// 3 blocks (24 warps, <= 80 registers) for rows up to 512 bytes.
+// Resident blocks per SM the main kernels are compiled for (register cap).
+// Rows up to 512 bytes: 4 blocks (32 warps, <= 64 registers) for the
+// kernels that gather one row per edge and keep little state, 3 blocks
+// (24 warps, <= 80 registers) for the source-side backward pass, which
+// gathers a row and a statistics record and keeps a row accumulator (at 64
+// registers it spills).  Measured on GB300 over the power-law workloads.
 template <int NV>
 struct MinBlocks {
   static constexpr int value = NV == 1 ? 3 : (NV == 2 ? 2 : 1);
+};
+template <int NV>
+struct MinBlocksLean {
+  static constexpr int value = NV == 1 ? 4 : (NV == 2 ? 2 : 1);
 };
 
 template <typename T>

@@ -172,7 +172,7 @@ __device__ __forceinline__ void dst_node(const BwdArgs& A, const Lane<NV>& L, in
 }
 
 template <typename T, int NV>
-__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_dst_main(const BwdArgs A) {
+__global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_main(const BwdArgs A) {
   constexpr int V = VecOf<T>::n;
   const DirArgs& D = A.csr;
   const Lane<NV> L(A.s);

@@ -276,7 +276,7 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, in
 }
 
 template <typename T, int NV>
-__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) fwd_main(const FwdArgs A) {
+__global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) fwd_main(const FwdArgs A) {
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
   extern __shared__ __align__(16) unsigned char smem[];
