@@ -52,9 +52,12 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     p.add_argument("--impl", choices=["gnnagg", "reference"], default="gnnagg")
-    p.add_argument("--op", choices=["gat", "gcn"], default="gat",
+    p.add_argument("--op", choices=["gat", "gatv2", "transformer", "gcn", "max"], default="gat",
                    help="gat: fused GAT attention aggregation (the headline); "
-                        "gcn: SpMM-family propagation A~ x with the symmetric normalisation")
+                        "gcn: SpMM-family propagation A~ x with the symmetric normalisation; "
+                        "max: max neighbourhood reduction with its winners; "
+                        "gatv2: GATv2 attention (xl = h, xr a second seeded feature array); "
+                        "transformer: graph-transformer attention (q = h, key and val seeded)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=12.0,
@@ -435,7 +438,11 @@ def run_gnnagg(args, rank, world):
 
 def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev, units):
     """Same metric through the public API with host buffers: every step copies
-    the step's inputs from pinned host memory and reads every result back."""
+    the step's inputs from pinned host memory and reads every result back.
+    Steps are pipelined the way a training loop with a prefetching loader
+    runs: inputs go up on one copy stream, results come back on another and
+    the kernels run on the compute stream, with two sets of device buffers
+    so that step k + 1's upload and step k - 1's download overlap step k."""
     import torch
     import torch.distributed as dist
     import graph_neural_network_gb300 as gnn
@@ -450,34 +457,55 @@ def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev,
     das_host, dad_host = pin(da_s), pin(da_d)
     h2d = sum(t.numel() * t.element_size() for t in (h_host, d_host, as_host, ad_host))
     d2h = sum(t.numel() * t.element_size() for t in (o_host, l_host, dh_host, das_host, dad_host))
-    stream = torch.cuda.current_stream(dev)
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    names = ("h", "dout", "a_s", "a_d", "out", "lse", "dh", "da_s", "da_d")
+    first = (h, dout, a_s, a_d, out, lse, dh, da_s, da_d)
+    bufs = [dict(zip(names, first)), {n: torch.empty_like(t) for n, t in zip(names, first)}]
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    for ev in comp_done + out_done:
+        ev.record(comp)
 
-    def one():
-        h.copy_(h_host, non_blocking=True)
-        dout.copy_(d_host, non_blocking=True)
-        a_s.copy_(as_host, non_blocking=True)
-        a_d.copy_(ad_host, non_blocking=True)
-        gnn.gat_forward(g, h, a_s, a_d, w.slope, out=out, lse=lse, ws=ws)
-        gnn.gat_backward(g, h, a_s, a_d, w.slope, lse, dout, dh=dh, da_src=da_s, da_dst=da_d,
-                         ws=ws)
-        o_host.copy_(out, non_blocking=True)
-        l_host.copy_(lse, non_blocking=True)
-        dh_host.copy_(dh, non_blocking=True)
-        das_host.copy_(da_s, non_blocking=True)
-        dad_host.copy_(da_d, non_blocking=True)
+    def one(k):
+        i = k % 2
+        b = bufs[i]
+        s_in.wait_event(comp_done[i])          # step k - 2 no longer reads these inputs
+        with torch.cuda.stream(s_in):
+            b["h"].copy_(h_host, non_blocking=True)
+            b["dout"].copy_(d_host, non_blocking=True)
+            b["a_s"].copy_(as_host, non_blocking=True)
+            b["a_d"].copy_(ad_host, non_blocking=True)
+        in_ready[i].record(s_in)
+        comp.wait_event(in_ready[i])
+        comp.wait_event(out_done[i])           # step k - 2's results have left these buffers
+        gnn.gat_forward(g, b["h"], b["a_s"], b["a_d"], w.slope, out=b["out"], lse=b["lse"],
+                        ws=ws, stream=comp)
+        gnn.gat_backward(g, b["h"], b["a_s"], b["a_d"], w.slope, b["lse"], b["dout"],
+                         dh=b["dh"], da_src=b["da_s"], da_dst=b["da_d"], ws=ws, stream=comp)
+        comp_done[i].record(comp)
+        s_out.wait_event(comp_done[i])
+        with torch.cuda.stream(s_out):
+            o_host.copy_(b["out"], non_blocking=True)
+            l_host.copy_(b["lse"], non_blocking=True)
+            dh_host.copy_(b["dh"], non_blocking=True)
+            das_host.copy_(b["da_s"], non_blocking=True)
+            dad_host.copy_(b["da_d"], non_blocking=True)
+        out_done[i].record(s_out)
 
-    for _ in range(3):
-        one()
+    for k in range(4):
+        one(k)
     K = max(1, min(args.steps, 200))
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K):
-        one()
-    e1.record(stream)
+    e0.record(s_in)
+    for k in range(K):
+        one(k)
+    e1.record(s_out)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / K
     if world > 1:
@@ -485,12 +513,15 @@ def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev,
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt[0])
     return {"value": world * units / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
-            "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": "H2D, compute and D2H on three streams, two device buffer sets"}
 
 
-def run_gcn(args, rank, world):
-    """SpMM-family propagation on the same workload: a step is out = A~ x
-    (CSR) plus dx = A~^T dout (cached CSC), norm "sym", features [N, H*D]."""
+def run_layer(args, rank, world):
+    """The other aggregation families on the same workload (features [N, H*D]).
+    gcn: a step is out = A~ x (CSR) plus dx = A~^T dout (cached CSC), norm
+    "sym".  max: a step is (out, arg) = max over in-neighbours plus dx from
+    arg and dout."""
     import torch
     import graph_neural_network_gb300 as gnn
 
@@ -508,15 +539,99 @@ def run_gcn(args, rank, world):
     g = gnn.Graph(torch.from_numpy(rp).to(dev), torch.from_numpy(ci).to(dev))
     x, dout = dev_feat(h_np), dev_feat(dout_np)
     out, dx = torch.empty_like(x), torch.empty_like(x)
-    ws = torch.empty(g._lib.gcn_agg_workspace_bytes(g.handle, F, 0 if w.dtype == "f32" else 1),
-                     dtype=torch.uint8, device=dev)
+    arg = torch.empty((n, F), dtype=torch.int32, device=dev)
+    dtc = 0 if w.dtype == "f32" else 1
+    units = e
+    if args.op == "gatv2":
+        import workload
+        H, D = w.H, w.D
+        xr_np = workload.normal_f32(w.seed, 5, (n, H, D), 1.0)
+        if w.dtype == "bf16":
+            xr_np = workload.f32_to_bf16_bits(xr_np)
+        xl3, xr3, dout3 = x.view(n, H, D), dev_feat(xr_np).view(n, H, D), dout.view(n, H, D)
+        att = torch.from_numpy(workload.normal_f32(w.seed, 2, (H, D), 0.1)).to(dev)
+        lse = torch.empty((n, H), dtype=torch.float32, device=dev)
+        dxr = torch.empty_like(xr3)
+        datt = torch.empty((H, D), dtype=torch.float32, device=dev)
+        ws = torch.empty(g._lib.gatv2_agg_workspace_bytes(g.handle, H, D, dtc),
+                         dtype=torch.uint8, device=dev)
+        out3, dx3 = out.view(n, H, D), dx.view(n, H, D)
+
+        def fwd():
+            gnn.gatv2_forward(g, xl3, xr3, att, w.slope, out=out3, lse=lse, ws=ws)
+
+        def bwd():
+            gnn.gatv2_backward(g, xl3, xr3, att, w.slope, lse, dout3, dxl=dx3, dxr=dxr,
+                               datt=datt, ws=ws)
+        idx = 4 * (n + 1) + 4 * e
+        row = s * n * F
+        b_fwd = idx + s * e * F + 2 * row + 4 * n * H            # xl_j gathered, xr_i, out, lse
+        # pass 1: xl_j gathered, xr_i and dout_i read, dxr written; pass 2: xr_i and
+        # dout_i gathered, xl_j read, dxl written
+        b_bwd = 2 * idx + 3 * s * e * F + 5 * row
+        units = e * H
+        metric = ("GEdge*head/s fwd and fwd+bwd GATv2 attention aggregation; "
+                  "achieved HBM GB/s vs roofline")
+    elif args.op == "transformer":
+        import workload
+        H, D = w.H, w.D
+
+        def seeded(stream_id):
+            a = workload.normal_f32(w.seed, stream_id, (n, H, D), 1.0)
+            return dev_feat(workload.f32_to_bf16_bits(a) if w.dtype == "bf16" else a).view(n, H, D)
+        q3, k3, v3, dout3 = x.view(n, H, D), seeded(5), seeded(6), dout.view(n, H, D)
+        lse = torch.empty((n, H), dtype=torch.float32, device=dev)
+        dq3, dk3, dv3 = dx.view(n, H, D), torch.empty_like(k3), torch.empty_like(v3)
+        out3 = out.view(n, H, D)
+        ws = torch.empty(g._lib.transformer_agg_workspace_bytes(g.handle, H, D, dtc),
+                         dtype=torch.uint8, device=dev)
+
+        def fwd():
+            gnn.transformer_forward(g, q3, k3, v3, out=out3, lse=lse, ws=ws)
+
+        def bwd():
+            gnn.transformer_backward(g, q3, k3, v3, lse, dout3, dq=dq3, dkey=dk3, dval=dv3,
+                                     ws=ws)
+        idx = 4 * (n + 1) + 4 * e
+        row = s * n * F
+        b_fwd = idx + 2 * s * e * F + 2 * row + 4 * n * H      # key_j, val_j gathered; q, out
+        # pass 1: key_j, val_j gathered, q_i and dout_i read, dq written; pass 2: q_i
+        # and dout_i gathered, key_j and val_j read, dkey and dval written
+        b_bwd = 2 * idx + 4 * s * e * F + 7 * row
+        units = e * H
+        metric = ("GEdge*head/s fwd and fwd+bwd graph-transformer attention aggregation; "
+                  "achieved HBM GB/s vs roofline")
+    elif args.op == "gcn":
+        ws = torch.empty(g._lib.gcn_agg_workspace_bytes(g.handle, F, dtc), dtype=torch.uint8,
+                         device=dev)
+
+        def fwd():
+            gnn.gcn_forward(g, x, "sym", out=out, ws=ws)
+
+        def bwd():
+            gnn.gcn_backward(g, dout, "sym", dx=dx, ws=ws)
+        idx = 4 * (n + 1) + 4 * e
+        b_fwd = b_bwd = idx + s * e * F + s * n * F    # indices, gathered rows, written rows
+        metric = "GEdge/s fwd and fwd+bwd GCN propagation (sym); achieved HBM GB/s vs roofline"
+    else:
+        ws = torch.empty(g._lib.reduce_agg_workspace_bytes(g.handle, F, dtc), dtype=torch.uint8,
+                         device=dev)
+
+        def fwd():
+            gnn.reduce_forward(g, x, "max", out=out, arg=arg, ws=ws)
+
+        def bwd():
+            gnn.reduce_backward(g, arg, dout, dx=dx, ws=ws)
+        b_fwd = 4 * (n + 1) + 4 * e + s * e * F + (s + 4) * n * F   # + out and arg written
+        b_bwd = (4 + 2 * s) * n * F                                  # arg, dout read; dx written
+        metric = "GEdge/s fwd and fwd+bwd max neighbourhood reduction; achieved HBM GB/s vs roofline"
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(3, args.warmup)):
         flush.zero_()
-        gnn.gcn_forward(g, x, "sym", out=out, ws=ws)
-        gnn.gcn_backward(g, dout, "sym", dx=dx, ws=ws)
+        fwd()
+        bwd()
     torch.cuda.synchronize()
     gnn.check_device_error(g)
     K = args.steps
@@ -527,31 +642,32 @@ def run_gcn(args, rank, world):
     for k in range(K):
         flush.zero_()
         ev[k][0].record(stream)
-        gnn.gcn_forward(g, x, "sym", out=out, ws=ws)
+        fwd()
         ev[k][1].record(stream)
-        gnn.gcn_backward(g, dout, "sym", dx=dx, ws=ws)
+        bwd()
         ev[k][2].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     gnn.check_device_error(g)
     t_f = sum(a.elapsed_time(b) for a, b, _ in ev) / K
     t_b = sum(b.elapsed_time(c) for _, b, c in ev) / K
-    per_call = 4 * (n + 1) + 4 * e + s * e * F + s * n * F   # indices, gathered rows, written rows
     peak, peak_kind = peaks()
-    line = {"metric": "GEdge/s fwd and fwd+bwd GCN propagation (sym); achieved HBM GB/s vs roofline",
-            "op": "gcn", "value": world * e / ((t_f + t_b) * 1e-3) / 1e9, "unit": "GEdge/s",
-            "fwd_value": world * e / (t_f * 1e-3) / 1e9, "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": t_f + t_b, "fwd_ms": t_f, "bwd_ms": t_b,
-            "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
+    line = {"metric": metric, "op": args.op,
+            "value": world * units / ((t_f + t_b) * 1e-3) / 1e9,
+            "unit": "GEdge*head/s" if args.op in ("gatv2", "transformer") else "GEdge/s",
+            "fwd_value": world * units / (t_f * 1e-3) / 1e9, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": t_f + t_b, "fwd_ms": t_f,
+            "bwd_ms": t_b, "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "n_nodes": n, "n_edges": e, "F": F,
                        "feature_dtype": w.dtype,
                        "l2": f"flushed before every step ({flush.numel() >> 20} MiB write)"},
-            "roofline": {"bound": "hbm", "kernel": "gcn_agg_forward / gcn_agg_backward calls",
-                         "achieved_fwd": per_call / (t_f * 1e-3) / 1e9,
-                         "achieved_bwd": per_call / (t_b * 1e-3) / 1e9, "peak": peak,
-                         "unit": "GB/s", "frac_fwd": per_call / (t_f * 1e-3) / 1e9 / peak,
-                         "frac_bwd": per_call / (t_b * 1e-3) / 1e9 / peak,
-                         "algorithmic_bytes": per_call, "peak_source": peak_kind},
+            "roofline": {"bound": "hbm", "kernel": f"{args.op} forward / backward calls",
+                         "achieved_fwd": b_fwd / (t_f * 1e-3) / 1e9,
+                         "achieved_bwd": b_bwd / (t_b * 1e-3) / 1e9, "peak": peak,
+                         "unit": "GB/s", "frac_fwd": b_fwd / (t_f * 1e-3) / 1e9 / peak,
+                         "frac_bwd": b_bwd / (t_b * 1e-3) / 1e9 / peak,
+                         "algorithmic_bytes_fwd": b_fwd, "algorithmic_bytes_bwd": b_bwd,
+                         "peak_source": peak_kind},
             "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -570,8 +686,8 @@ def main(argv=None):
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
     try:
-        if args.op == "gcn":
-            return run_gcn(args, rank, world)
+        if args.op != "gat":
+            return run_layer(args, rank, world)
         return run_gnnagg(args, rank, world)
     finally:
         if world > 1:

@@ -15,6 +15,21 @@ The SpMM-family propagation of GCN / GraphConv layers (out = A~ x, norm
 
     out = gcn_forward(g, x, "sym")                 # x [N, F]
     dx = gcn_backward(g, dout, "sym")              # A~^T dout over the cached CSC
+
+the GATv2 attention (score att . LeakyReLU(xr_i + xl_j), value xl_j):
+
+    out, lse = gatv2_forward(g, xl, xr, att, 0.2)
+    dxl, dxr, datt = gatv2_backward(g, xl, xr, att, 0.2, lse, dout)
+
+the graph-transformer attention (score scale * q_i . key_j, value val_j):
+
+    out, lse = transformer_forward(g, q, key, val)     # scale defaults to 1/sqrt(D)
+    dq, dkey, dval = transformer_backward(g, q, key, val, lse, dout)
+
+and the max / min neighbourhood reduction with its winners:
+
+    out, arg = reduce_forward(g, x, "max")         # arg [N, F] int32, -1 if no in-edges
+    dx = reduce_backward(g, arg, dout)
 """
 from __future__ import annotations
 
@@ -27,7 +42,9 @@ from ._native import GnnError, Tiling
 
 __all__ = ["Graph", "gat_forward", "gat_backward", "GATAggregate", "GnnError", "Tiling",
            "check_device_error", "default_tiling", "gcn_forward", "gcn_backward",
-           "GCNAggregate"]
+           "GCNAggregate", "reduce_forward", "reduce_backward", "ReduceAggregate",
+           "gatv2_forward", "gatv2_backward", "GATv2Aggregate", "transformer_forward",
+           "transformer_backward", "TransformerAggregate"]
 
 
 def _ptr(t):
@@ -242,6 +259,204 @@ class GCNAggregate(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dout):
         return None, gcn_backward(ctx.g, dout.contiguous(), ctx.norm), None
+
+
+def _gatv2_ws(g, H, D, dtype, ws, device):
+    if ws is not None:
+        return ws
+    n = g._lib.gatv2_agg_workspace_bytes(g.handle, H, D, _dtype_code(dtype))
+    if n == 0:
+        raise GnnError(_native.ERR_UNSUPPORTED, f"(H={H}, D={D}, {dtype})")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def gatv2_forward(g: Graph, xl: torch.Tensor, xr: torch.Tensor, att: torch.Tensor,
+                  slope: float = 0.2, out=None, lse=None, ws=None, stream=None):
+    """out [N,H,D] (xl's dtype) and lse [N,H] float32."""
+    _check_features(g, xl, "xl")
+    _check_features(g, xr, "xr")
+    if xr.shape != xl.shape or xr.dtype != xl.dtype:
+        raise ValueError("xr must match xl in shape and dtype")
+    N, H, D = xl.shape
+    att = att.to(torch.float32).contiguous()
+    out = torch.empty_like(xl) if out is None else out
+    lse = torch.empty((N, H), dtype=torch.float32, device=xl.device) if lse is None else lse
+    ws = _gatv2_ws(g, H, D, xl.dtype, ws, xl.device)
+    rc = g._lib.gatv2_agg_forward(g.handle, H, D, _dtype_code(xl.dtype), _ptr(xl), _ptr(xr),
+                                  _ptr(att), float(slope), _ptr(out), _ptr(lse), _ptr(ws),
+                                  ws.numel(), _stream(stream, xl.device))
+    _native.check(rc, "gatv2_agg_forward")
+    return out, lse
+
+
+def gatv2_backward(g: Graph, xl: torch.Tensor, xr: torch.Tensor, att: torch.Tensor,
+                   slope: float, lse: torch.Tensor, dout: torch.Tensor, dxl=None, dxr=None,
+                   datt=None, ws=None, stream=None):
+    """dxl, dxr [N,H,D] (xl's dtype) and datt [H,D] float32."""
+    _check_features(g, xl, "xl")
+    _check_features(g, xr, "xr")
+    _check_features(g, dout, "dout")
+    if xr.shape != xl.shape or dout.shape != xl.shape or dout.dtype != xl.dtype:
+        raise ValueError("xr and dout must match xl")
+    N, H, D = xl.shape
+    att = att.to(torch.float32).contiguous()
+    dxl = torch.empty_like(xl) if dxl is None else dxl
+    dxr = torch.empty_like(xl) if dxr is None else dxr
+    datt = torch.empty((H, D), dtype=torch.float32, device=xl.device) if datt is None else datt
+    ws = _gatv2_ws(g, H, D, xl.dtype, ws, xl.device)
+    rc = g._lib.gatv2_agg_backward(g.handle, H, D, _dtype_code(xl.dtype), _ptr(xl), _ptr(xr),
+                                   _ptr(att), float(slope), _ptr(lse.contiguous()), _ptr(dout),
+                                   _ptr(dxl), _ptr(dxr), _ptr(datt), _ptr(ws), ws.numel(),
+                                   _stream(stream, xl.device))
+    _native.check(rc, "gatv2_agg_backward")
+    return dxl, dxr, datt
+
+
+class GATv2Aggregate(torch.autograd.Function):
+    """out = GATv2Aggregate.apply(graph, xl, xr, att, slope)."""
+
+    @staticmethod
+    def forward(ctx, g, xl, xr, att, slope):
+        xl, xr = xl.contiguous(), xr.contiguous()
+        out, lse = gatv2_forward(g, xl, xr, att, slope)
+        ctx.g, ctx.slope = g, slope
+        ctx.save_for_backward(xl, xr, att, lse)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        xl, xr, att, lse = ctx.saved_tensors
+        dxl, dxr, datt = gatv2_backward(ctx.g, xl, xr, att, ctx.slope, lse, dout.contiguous())
+        return None, dxl, dxr, datt.to(att.dtype), None
+
+
+def _gt_ws(g, H, D, dtype, ws, device):
+    if ws is not None:
+        return ws
+    n = g._lib.transformer_agg_workspace_bytes(g.handle, H, D, _dtype_code(dtype))
+    if n == 0:
+        raise GnnError(_native.ERR_UNSUPPORTED, f"(H={H}, D={D}, {dtype})")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _gt_inputs(g, q, key, val):
+    for name, x in (("q", q), ("key", key), ("val", val)):
+        _check_features(g, x, name)
+        if x.shape != q.shape or x.dtype != q.dtype:
+            raise ValueError("q, key and val must share shape and dtype")
+    return q.shape
+
+
+def transformer_forward(g: Graph, q: torch.Tensor, key: torch.Tensor, val: torch.Tensor,
+                        scale: float | None = None, out=None, lse=None, ws=None, stream=None):
+    """out [N,H,D] (q's dtype) and lse [N,H] float32; scale defaults to 1/sqrt(D)."""
+    N, H, D = _gt_inputs(g, q, key, val)
+    scale = D ** -0.5 if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((N, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = _gt_ws(g, H, D, q.dtype, ws, q.device)
+    rc = g._lib.transformer_agg_forward(g.handle, H, D, _dtype_code(q.dtype), _ptr(q), _ptr(key),
+                                        _ptr(val), scale, _ptr(out), _ptr(lse), _ptr(ws),
+                                        ws.numel(), _stream(stream, q.device))
+    _native.check(rc, "transformer_agg_forward")
+    return out, lse
+
+
+def transformer_backward(g: Graph, q: torch.Tensor, key: torch.Tensor, val: torch.Tensor,
+                         lse: torch.Tensor, dout: torch.Tensor, scale: float | None = None,
+                         dq=None, dkey=None, dval=None, ws=None, stream=None):
+    """dq, dkey, dval [N,H,D] (q's dtype)."""
+    N, H, D = _gt_inputs(g, q, key, val)
+    _check_features(g, dout, "dout")
+    if dout.shape != q.shape or dout.dtype != q.dtype:
+        raise ValueError("dout must match q")
+    scale = D ** -0.5 if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dkey = torch.empty_like(q) if dkey is None else dkey
+    dval = torch.empty_like(q) if dval is None else dval
+    ws = _gt_ws(g, H, D, q.dtype, ws, q.device)
+    rc = g._lib.transformer_agg_backward(g.handle, H, D, _dtype_code(q.dtype), _ptr(q),
+                                         _ptr(key), _ptr(val), scale, _ptr(lse.contiguous()),
+                                         _ptr(dout), _ptr(dq), _ptr(dkey), _ptr(dval), _ptr(ws),
+                                         ws.numel(), _stream(stream, q.device))
+    _native.check(rc, "transformer_agg_backward")
+    return dq, dkey, dval
+
+
+class TransformerAggregate(torch.autograd.Function):
+    """out = TransformerAggregate.apply(graph, q, key, val, scale)."""
+
+    @staticmethod
+    def forward(ctx, g, q, key, val, scale):
+        q, key, val = q.contiguous(), key.contiguous(), val.contiguous()
+        out, lse = transformer_forward(g, q, key, val, scale)
+        ctx.g, ctx.scale = g, scale
+        ctx.save_for_backward(q, key, val, lse)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, key, val, lse = ctx.saved_tensors
+        dq, dk, dv = transformer_backward(ctx.g, q, key, val, lse, dout.contiguous(), ctx.scale)
+        return None, dq, dk, dv, None
+
+
+def _reduce_ws(g, F, dt, ws, device):
+    if ws is not None:
+        return ws
+    n = g._lib.reduce_agg_workspace_bytes(g.handle, F, dt)
+    if n == 0:
+        raise GnnError(_native.ERR_UNSUPPORTED, f"(F={F})")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def reduce_forward(g: Graph, x: torch.Tensor, op: str = "max", out=None, arg=None, ws=None,
+                   stream=None):
+    """out [N, ...] (x's dtype) = max or min over in-neighbours, feature by
+    feature; arg int32 of the same shape = the winning source (-1: none)."""
+    F = _row_width(g, x, "x")
+    dt = _dtype_code(x.dtype)
+    if op not in _native.REDUCE_OPS:
+        raise ValueError(f"op must be one of {sorted(_native.REDUCE_OPS)}")
+    out = torch.empty_like(x) if out is None else out
+    arg = torch.empty(x.shape, dtype=torch.int32, device=x.device) if arg is None else arg
+    ws = _reduce_ws(g, F, dt, ws, x.device)
+    rc = g._lib.reduce_agg_forward(g.handle, F, dt, _native.REDUCE_OPS[op], _ptr(x), _ptr(out),
+                                   _ptr(arg), _ptr(ws), ws.numel(), _stream(stream, x.device))
+    _native.check(rc, "reduce_agg_forward")
+    return out, arg
+
+
+def reduce_backward(g: Graph, arg: torch.Tensor, dout: torch.Tensor, dx=None, ws=None,
+                    stream=None):
+    """dx = the gradient of sum(out * dout) w.r.t. x, from the forward's arg."""
+    F = _row_width(g, dout, "dout")
+    if arg.dtype != torch.int32 or arg.shape != dout.shape or not arg.is_contiguous():
+        raise ValueError("arg must be a contiguous int32 tensor shaped like dout")
+    dt = _dtype_code(dout.dtype)
+    dx = torch.empty_like(dout) if dx is None else dx
+    ws = _reduce_ws(g, F, dt, ws, dout.device)
+    rc = g._lib.reduce_agg_backward(g.handle, F, dt, _ptr(arg), _ptr(dout), _ptr(dx), _ptr(ws),
+                                    ws.numel(), _stream(stream, dout.device))
+    _native.check(rc, "reduce_agg_backward")
+    return dx
+
+
+class ReduceAggregate(torch.autograd.Function):
+    """out = ReduceAggregate.apply(graph, x, op)."""
+
+    @staticmethod
+    def forward(ctx, g, x, op):
+        out, arg = reduce_forward(g, x.contiguous(), op)
+        ctx.g = g
+        ctx.save_for_backward(arg)
+        ctx.mark_non_differentiable(arg)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        (arg,) = ctx.saved_tensors
+        return None, reduce_backward(ctx.g, arg, dout.contiguous()), None
 
 
 def check_device_error(g: Graph, stream=None) -> int:

@@ -19,6 +19,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_INVALID_GRAPH = 0, 1, 2, 3
 ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_DEVICE_ASSERT, ERR_TIMEOUT = 4, 5, 6, 7
 F32, BF16 = 0, 1
 NORMS = {"sum": 0, "mean": 1, "sym": 2}  # gnn_norm
+REDUCE_OPS = {"max": 0, "min": 1}        # gnn_reduce_op
 
 # (name, restype, argtypes) of every exported symbol, in header order
 _P, _I64, _I32, _SZ, _F = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t,
@@ -44,6 +45,18 @@ SIGNATURES = [
     ("gcn_agg_workspace_bytes", _SZ, [_P, _I32, _I32]),
     ("gcn_agg_forward", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]),
     ("gcn_agg_backward", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    ("gatv2_agg_workspace_bytes", _SZ, [_P, _I32, _I32, _I32]),
+    ("gatv2_agg_forward", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _F, _P, _P, _P, _SZ, _P]),
+    ("gatv2_agg_backward", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _F, _P, _P, _P, _P, _P,
+                                  _P, _SZ, _P]),
+    ("transformer_agg_workspace_bytes", _SZ, [_P, _I32, _I32, _I32]),
+    ("transformer_agg_forward", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _F, _P, _P, _P, _SZ,
+                                       _P]),
+    ("transformer_agg_backward", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _F, _P, _P, _P, _P,
+                                        _P, _P, _SZ, _P]),
+    ("reduce_agg_workspace_bytes", _SZ, [_P, _I32, _I32]),
+    ("reduce_agg_forward", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    ("reduce_agg_backward", _I32, [_P, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     ("gnn_check_device_error", _I32, [_P, _P, _P]),
     ("gnn_status_string", ctypes.c_char_p, [_I32]),
     ("gnn_abi_version", _I32, []),

@@ -342,6 +342,148 @@ gnn_status gcn_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, gnn_norm
   return spmm_call(g, F, dtype, norm, dout, dx, ws, ws_bytes, stream, true);
 }
 
+}  // extern "C"
+
+namespace {
+
+gnn_status gatv2_shape(const gnn_graph* g, int H, int D, gnn_dtype dt, Shape* s) {
+  gnn_status r = check_call(g, H, D, dt, s);
+  if (r != GNN_OK) return r;
+  return s->nv == 1 ? GNN_OK : GNN_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gatv2_agg_workspace_bytes(const gnn_graph* g, int H, int D, gnn_dtype dtype) {
+  Shape s;
+  if (gatv2_shape(g, H, D, dtype, &s) != GNN_OK) return 0;
+  return gnn::gatv2_ws_bytes(g, s);
+}
+
+gnn_status gatv2_agg_forward(const gnn_graph* g, int H, int D, gnn_dtype dtype, const void* xl,
+                             const void* xr, const float* att, float slope, void* out,
+                             float* lse, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  gnn_status r = gatv2_shape(g, H, D, dtype, &s);
+  if (r != GNN_OK) return r;
+  if (g->n == 0) return GNN_OK;
+  if (!xl || !xr || !att || !out || !lse) return GNN_ERR_INVALID_ARG;
+  if (!aligned(xl, 16) || !aligned(xr, 16) || !aligned(att, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4))
+    return GNN_ERR_INVALID_ARG;
+  if (ws_bytes < gnn::gatv2_ws_bytes(g, s)) return GNN_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned(ws, 256)) return GNN_ERR_INVALID_ARG;
+  return from_cuda(gnn::launch_gatv2_forward(g, s, dtype, xl, xr, att, slope, out, lse,
+                                             static_cast<char*>(ws),
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+gnn_status gatv2_agg_backward(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                              const void* xl, const void* xr, const float* att, float slope,
+                              const float* lse, const void* dout, void* dxl, void* dxr,
+                              float* datt, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  gnn_status r = gatv2_shape(g, H, D, dtype, &s);
+  if (r != GNN_OK) return r;
+  if (!att || !datt || !aligned(att, 16) || !aligned(datt, 4)) return GNN_ERR_INVALID_ARG;
+  if (g->n > 0) {
+    if (!xl || !xr || !lse || !dout || !dxl || !dxr) return GNN_ERR_INVALID_ARG;
+    if (!aligned(xl, 16) || !aligned(xr, 16) || !aligned(dout, 16) || !aligned(dxl, 16) ||
+        !aligned(dxr, 16) || !aligned(lse, 4))
+      return GNN_ERR_INVALID_ARG;
+  }
+  if (ws_bytes < gnn::gatv2_ws_bytes(g, s)) return GNN_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned(ws, 256)) return GNN_ERR_INVALID_ARG;
+  return from_cuda(gnn::launch_gatv2_backward(g, s, dtype, xl, xr, att, slope, lse, dout, dxl,
+                                              dxr, datt, static_cast<char*>(ws),
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+size_t transformer_agg_workspace_bytes(const gnn_graph* g, int H, int D, gnn_dtype dtype) {
+  Shape s;
+  if (gatv2_shape(g, H, D, dtype, &s) != GNN_OK) return 0;
+  return gnn::transformer_ws_bytes(g, s);
+}
+
+gnn_status transformer_agg_forward(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                                   const void* q, const void* key, const void* val, float scale,
+                                   void* out, float* lse, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  Shape s;
+  gnn_status r = gatv2_shape(g, H, D, dtype, &s);
+  if (r != GNN_OK) return r;
+  if (g->n == 0) return GNN_OK;
+  if (!q || !key || !val || !out || !lse) return GNN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(key, 16) || !aligned(val, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4))
+    return GNN_ERR_INVALID_ARG;
+  if (ws_bytes < gnn::transformer_ws_bytes(g, s)) return GNN_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned(ws, 256)) return GNN_ERR_INVALID_ARG;
+  return from_cuda(gnn::launch_transformer_forward(g, s, dtype, q, key, val, scale, out, lse,
+                                                   static_cast<char*>(ws),
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+gnn_status transformer_agg_backward(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                                    const void* q, const void* key, const void* val, float scale,
+                                    const float* lse, const void* dout, void* dq, void* dkey,
+                                    void* dval, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  gnn_status r = gatv2_shape(g, H, D, dtype, &s);
+  if (r != GNN_OK) return r;
+  if (g->n == 0) return GNN_OK;
+  if (!q || !key || !val || !lse || !dout || !dq || !dkey || !dval) return GNN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(key, 16) || !aligned(val, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dkey, 16) || !aligned(dval, 16) || !aligned(lse, 4))
+    return GNN_ERR_INVALID_ARG;
+  if (ws_bytes < gnn::transformer_ws_bytes(g, s)) return GNN_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned(ws, 256)) return GNN_ERR_INVALID_ARG;
+  return from_cuda(gnn::launch_transformer_backward(g, s, dtype, q, key, val, scale, lse, dout,
+                                                    dq, dkey, dval, static_cast<char*>(ws),
+                                                    static_cast<cudaStream_t>(stream)));
+}
+
+size_t reduce_agg_workspace_bytes(const gnn_graph* g, int F, gnn_dtype dtype) {
+  Shape s;
+  if (spmm_shape(g, F, dtype, &s) != GNN_OK) return 0;
+  return gnn::reduce_ws_bytes(g, s);
+}
+
+gnn_status reduce_agg_forward(const gnn_graph* g, int F, gnn_dtype dtype, gnn_reduce_op op,
+                              const void* x, void* out, int32_t* arg, void* ws, size_t ws_bytes,
+                              void* stream) {
+  Shape s;
+  gnn_status r = spmm_shape(g, F, dtype, &s);
+  if (r != GNN_OK) return r;
+  if (op != GNN_REDUCE_MAX && op != GNN_REDUCE_MIN) return GNN_ERR_INVALID_ARG;
+  if (g->n == 0) return GNN_OK;
+  if (!x || !out || !arg || !aligned(x, 16) || !aligned(out, 16) || !aligned(arg, 16))
+    return GNN_ERR_INVALID_ARG;
+  if (ws_bytes < gnn::reduce_ws_bytes(g, s)) return GNN_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned(ws, 256)) return GNN_ERR_INVALID_ARG;
+  return from_cuda(gnn::launch_reduce_forward(g, s, dtype, int(op), x, out, arg,
+                                              static_cast<char*>(ws),
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+gnn_status reduce_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, const int32_t* arg,
+                               const void* dout, void* dx, void* ws, size_t ws_bytes,
+                               void* stream) {
+  Shape s;
+  gnn_status r = spmm_shape(g, F, dtype, &s);
+  if (r != GNN_OK) return r;
+  if (g->n == 0) return GNN_OK;
+  if (!arg || !dout || !dx || !aligned(arg, 16) || !aligned(dout, 16) || !aligned(dx, 16))
+    return GNN_ERR_INVALID_ARG;
+  if (ws_bytes < gnn::reduce_ws_bytes(g, s)) return GNN_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned(ws, 256)) return GNN_ERR_INVALID_ARG;
+  return from_cuda(gnn::launch_reduce_backward(g, s, dtype, arg, dout, dx,
+                                               static_cast<char*>(ws),
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 gnn_status gnn_check_device_error(const gnn_graph* g, void* stream, int32_t* info) {
   if (!g || !g->err) return GNN_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -1,0 +1,1011 @@
+// Fused GATv2 neighbour aggregation, forward and backward.
+//
+// Per destination i and head k, with xl = W_l h (source side, also the
+// aggregated value) and xr = W_r h (destination side) given by the caller:
+//   e_ij = att[k] . LeakyReLU(xr_i[k] + xl_j[k]),  alpha = softmax_j e_ij,
+//   out_i[k] = sum_j alpha_ij xl_j[k],  lse_i[k] = log sum_j exp e_ij
+// (Brody et al., "How Attentive are Graph Attention Networks?", eq. 7; the
+// GATv2 layer of "On Efficient Scaling of GNNs via IO-Aware Layers
+// Implementations", Technical Summary > Methodology, attention-based layers:
+// fused CSR kernel, one streaming pass, online softmax, log-sum-exp kept for
+// the backward pass).  Unlike the GAT score, this one does not split into
+// per-node halves: every edge evaluates LeakyReLU on a D-vector, so the
+// score is computed from the gathered row inside the edge loop.
+//
+// Backward, with da_ij = dout_i . xl_j, Delta_i = sum_j alpha_ij da_ij,
+// de_ij = alpha_ij (da_ij - Delta_i), g = LeakyReLU'(z) and l = LeakyReLU(z):
+//   pass 1, destination side (CSR), one streaming pass per node that sums
+//     Delta, P = sum alpha da g, Q = sum alpha g, R = sum alpha da l,
+//     S = sum alpha l  (D-vectors), so that
+//     dxr_i = att (P - Delta Q) and node i's share of datt is R - Delta S;
+//     the per-node record {lse, Delta} goes to the workspace.
+//   pass 2, source side (cached CSC): dxl_j = sum_i alpha_ij dout_i +
+//     de_ij att g(z_ij), gathering xr_i, dout_i and i's record per edge.
+// datt is summed deterministically: pass 1 assigns work to blocks and warps
+// statically, each block folds its warps' sums in a fixed order, and a last
+// kernel adds the block sums in a fixed order in float64.
+//
+// Rows up to 512 bytes (one 16-byte vector per lane).  Degree-aware tiling
+// and hub merges as in the GAT kernels.
+#include "device.cuh"
+
+namespace gnn {
+namespace {
+
+constexpr int kGrab = 4;
+
+struct V2Dir {
+  const int32_t* ptr;
+  const int32_t* idx;
+  const int32_t* light;
+  int64_t n_light;
+  const int4* items;
+  int64_t n_items;
+  const int4* hubs;
+  int64_t n_hubs;
+  int col_off;
+};
+
+struct V2Args {
+  Shape s;
+  V2Dir csr, csc;
+  int64_t n;
+  const void* xl;
+  const void* xr;
+  const float* att;
+  float slope;
+  // forward
+  void* out;
+  float* lse;
+  float* f_acc;      // [CSR hub chunks][row_f]
+  float2* f_ml;      // [CSR hub chunks][H] (max in base 2, sum)
+  // backward
+  const float* lse_in;
+  const void* dout;
+  void* dxl;
+  void* dxr;
+  float* datt;
+  float2* stats;     // [N][H] {lse (base 2), Delta}
+  float* d_delta;    // [CSR hub chunks][H]
+  float* d_vec;      // [CSR hub chunks][4][row_f]  (P, Q, R, S)
+  float* s_acc;      // [CSC hub chunks][row_f]
+  double* da_part;   // [da rows][row_f]
+  int da_main_rows;  // rows of da_part written by pass 1 (one per block)
+  int* ctr;
+  int32_t* err;
+};
+
+__device__ __forceinline__ float leaky(float z, float s) { return z > 0.f ? z : s * z; }
+__device__ __forceinline__ float leaky_g(float z, float s) { return z > 0.f ? 1.f : s; }
+
+template <int U>
+__device__ __forceinline__ void batch_ids(const int32_t* cols, int colbase, int beg, int end,
+                                          int g, int G, int (&j)[U]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = beg + u * G + g;
+    j[u] = e < end ? cols[e - colbase] : -1;
+  }
+}
+
+// This lane's slice (vector q) of row `node`, widened (zeros when !ok).
+template <typename T>
+__device__ __forceinline__ void own_row(const void* x, int64_t node, const Shape& s,
+                                        const Lane<1>& L, float (&r)[VecOf<T>::n]) {
+  unpack<T>(L.ok[0] ? ld16(row_base<T>(x, node, s.rv) + 16 * L.q[0]) : make_uint4(0, 0, 0, 0),
+            r);
+}
+
+template <typename T>
+__device__ __forceinline__ void att_slice(const float* att, const Lane<1>& L, float scale,
+                                          float (&w)[VecOf<T>::n]) {
+  float tmp[1][VecOf<T>::n];
+  load_att<T, 1>(att, L, scale, tmp);
+#pragma unroll
+  for (int c = 0; c < VecOf<T>::n; ++c) w[c] = tmp[0][c];
+}
+
+template <int V>
+__device__ __forceinline__ void zero(float (&x)[V]) {
+#pragma unroll
+  for (int c = 0; c < V; ++c) x[c] = 0.f;
+}
+
+__device__ __forceinline__ float subgroup_sum(float x, const Shape& s) {
+  for (int o = s.lpr; o < 32; o <<= 1) x += __shfl_xor_sync(kFull, x, o);
+  return x;
+}
+
+template <int V>
+__device__ __forceinline__ void subgroup_sums(float (&x)[V], const Shape& s) {
+#pragma unroll
+  for (int c = 0; c < V; ++c) x[c] = subgroup_sum(x[c], s);
+}
+
+// ---------------------------------------------------------------------------
+// forward
+// ---------------------------------------------------------------------------
+
+template <typename T>
+struct V2Online {
+  static constexpr int V = VecOf<T>::n;
+  float m, l, acc[V];
+  __device__ __forceinline__ void init() {
+    m = -INFINITY;
+    l = 0.f;
+    zero<V>(acc);
+  }
+  __device__ __forceinline__ void merge(float mb, float lb, const float (&ab)[V]) {
+    const float M = fmaxf(m, mb);
+    const float Mr = (M == -INFINITY) ? 0.f : M;
+    const float sa = ex2(m - Mr), sb = ex2(mb - Mr);
+    l = l * sa + lb * sb;
+    scale<V>(acc, sa);
+    axpy<V>(acc, sb, ab);
+    m = M;
+  }
+  __device__ __forceinline__ void merge_subgroups(const Shape& s) {
+    for (int o = s.lpr; o < 32; o <<= 1) {
+      const float mb = __shfl_xor_sync(kFull, m, o);
+      const float lb = __shfl_xor_sync(kFull, l, o);
+      float ab[V];
+#pragma unroll
+      for (int c = 0; c < V; ++c) ab[c] = __shfl_xor_sync(kFull, acc[c], o);
+      merge(mb, lb, ab);
+    }
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ void fwd_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
+                                          int colbase, int beg, int end, int (&jn)[kUnroll],
+                                          const float (&xr)[VecOf<T>::n],
+                                          const float (&a2)[VecOf<T>::n], V2Online<T>& st) {
+  constexpr int V = VecOf<T>::n;
+  constexpr int U = kUnroll;
+  const int step = L.G * U;
+  for (int base = beg; base < end; base += step) {
+    int j[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) j[u] = jn[u];
+    uint4 raw[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      raw[u] = (j[u] >= 0 && L.ok[0]) ? ld16(row_base<T>(A.xl, j[u], A.s.rv) + 16 * L.q[0])
+                                      : make_uint4(0, 0, 0, 0);
+    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+    float sc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float x[V];
+      unpack<T>(raw[u], x);
+      float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < V; c += 2) {
+        p0 = fmaf(a2[c], leaky(xr[c] + x[c], A.slope), p0);
+        p1 = fmaf(a2[c + 1], leaky(xr[c + 1] + x[c + 1], A.slope), p1);
+      }
+      sc[u] = p0 + p1;
+    }
+    head_sums<U>(sc, A.s.hv_log2);
+    float bm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      sc[u] = j[u] >= 0 ? sc[u] : -INFINITY;
+      bm = fmaxf(bm, sc[u]);
+    }
+    const float mn = fmaxf(st.m, bm);
+    const float mr = (mn == -INFINITY) ? 0.f : mn;
+    const float s0 = ex2(st.m - mr);
+    st.l *= s0;
+    scale<V>(st.acc, s0);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float p = ex2(sc[u] - mr);
+      st.l += p;
+      float x[V];
+      unpack_alt<T>(raw[u], x);
+      axpy<V>(st.acc, p, x);
+    }
+    st.m = mn;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void fwd_write(const V2Args& A, const Lane<1>& L, int64_t node,
+                                          const V2Online<T>& st) {
+  constexpr int V = VecOf<T>::n;
+  if (!L.ok[0]) return;
+  const float inv = st.l > 0.f ? __frcp_rn(st.l) : 0.f;
+  float x[V];
+#pragma unroll
+  for (int c = 0; c < V; ++c) x[c] = st.acc[c];
+  scale<V>(x, inv);
+  st16(reinterpret_cast<char*>(A.out) + node * int64_t(A.s.rv) * 16 + 16 * L.q[0], pack<T>(x));
+  if (L.head_leader(A.s, 0))
+    A.lse[node * A.s.H + L.k[0]] = st.l > 0.f ? (st.m + __log2f(st.l)) * kLn2 : -INFINITY;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) v2_fwd_main(const V2Args A) {
+  constexpr int V = VecOf<T>::n;
+  const V2Dir& D = A.csr;
+  const Lane<1> L(A.s);
+  const int wid = threadIdx.x >> 5;
+  const int row_f = A.s.rv * V;
+  const int H = A.s.H;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_item;
+  float a2[V], xr[V];
+  att_slice<T>(A.att, L, kLog2e, a2);
+
+  if (D.n_items > 0) {
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int32_t* cols = reinterpret_cast<int32_t*>(smem + 16);
+    float* wm = reinterpret_cast<float*>(smem + D.col_off);
+    float* wl = wm + kWarps * H;
+    float* wacc = wl + kWarps * H;
+    uint32_t parity = 0;
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    for (;;) {
+      if (threadIdx.x == 0) s_item = atomicAdd(A.ctr + 0, 1);
+      __syncthreads();
+      const int it_i = s_item;
+      if (it_i >= D.n_items) break;
+      const int4 it = D.items[it_i];
+      if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
+      const int per = (it.z - it.y + kWarps - 1) / kWarps;
+      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      const int colbase = it.y & ~3;
+      int jn[kUnroll];
+      batch_ids<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
+      own_row<T>(A.xr, it.x, A.s, L, xr);
+      V2Online<T> st;
+      st.init();
+      fwd_edges<T>(A, L, cols, colbase, wb, we, jn, xr, a2, st);
+      st.merge_subgroups(A.s);
+      if (L.g == 0 && L.ok[0]) {
+#pragma unroll
+        for (int c = 0; c < V; ++c) wacc[wid * row_f + L.q[0] * V + c] = st.acc[c];
+        if (L.head_leader(A.s, 0)) {
+          wm[wid * H + L.k[0]] = st.m;
+          wl[wid * H + L.k[0]] = st.l;
+        }
+      }
+      __syncthreads();
+      if (wid == 0 && L.g == 0 && L.ok[0]) {
+        V2Online<T> tot;
+        tot.m = wm[L.k[0]];
+        tot.l = wl[L.k[0]];
+#pragma unroll
+        for (int c = 0; c < V; ++c) tot.acc[c] = wacc[L.q[0] * V + c];
+        for (int w = 1; w < kWarps; ++w) {
+          float ab[V];
+#pragma unroll
+          for (int c = 0; c < V; ++c) ab[c] = wacc[w * row_f + L.q[0] * V + c];
+          tot.merge(wm[w * H + L.k[0]], wl[w * H + L.k[0]], ab);
+        }
+        if (it.w < 0) {
+          fwd_write<T>(A, L, it.x, tot);
+        } else {
+          float* pa = A.f_acc + int64_t(it.w) * row_f + L.q[0] * V;
+#pragma unroll
+          for (int c4 = 0; c4 < V; c4 += 4)
+            *reinterpret_cast<float4*>(pa + c4) =
+                make_float4(tot.acc[c4], tot.acc[c4 + 1], tot.acc[c4 + 2], tot.acc[c4 + 3]);
+          if (L.head_leader(A.s, 0)) A.f_ml[int64_t(it.w) * H + L.k[0]] = make_float2(tot.m, tot.l);
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  for (;;) {
+    int t0 = 0;
+    if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
+    t0 = __shfl_sync(kFull, t0, 0);
+    if (t0 >= D.n_light) break;
+    int my_i = -1, my_b = 0, my_e = 0;
+    if (L.lane < kGrab && t0 + L.lane < D.n_light) {
+      my_i = D.light[t0 + L.lane];
+      my_b = D.ptr[my_i];
+      my_e = D.ptr[my_i + 1];
+    }
+    int i = __shfl_sync(kFull, my_i, 0);
+    int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
+    int jn[kUnroll];
+    batch_ids<kUnroll>(D.idx, 0, beg, end, L.g, L.G, jn);
+    for (int q = 0; q < kGrab && i >= 0; ++q) {
+      const int nq = (q + 1) & (kGrab - 1);
+      const int i2 = q + 1 < kGrab ? __shfl_sync(kFull, my_i, nq) : -1;
+      const int b2 = __shfl_sync(kFull, my_b, nq);
+      const int e2 = __shfl_sync(kFull, my_e, nq);
+      int jn2[kUnroll];
+      batch_ids<kUnroll>(D.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
+      own_row<T>(A.xr, i, A.s, L, xr);
+      V2Online<T> st;
+      st.init();
+      fwd_edges<T>(A, L, D.idx, 0, beg, end, jn, xr, a2, st);
+      st.merge_subgroups(A.s);
+      if (L.g == 0) fwd_write<T>(A, L, i, st);
+      i = i2;
+      beg = b2;
+      end = e2;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) jn[u] = jn2[u];
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) v2_fwd_merge(const V2Args A) {
+  constexpr int V = VecOf<T>::n;
+  const Lane<1> L(A.s);
+  const int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (t >= A.csr.n_hubs || L.g != 0 || !L.ok[0]) return;
+  const int4 hb = A.csr.hubs[t];
+  const int row_f = A.s.rv * V;
+  V2Online<T> st;
+  st.init();
+  for (int c = 0; c < hb.z; ++c) {
+    const int64_t slot = int64_t(hb.y) + c;
+    const float2 ml = A.f_ml[slot * A.s.H + L.k[0]];
+    float ab[V];
+    const float* pa = A.f_acc + slot * row_f + L.q[0] * V;
+#pragma unroll
+    for (int c4 = 0; c4 < V; c4 += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(pa + c4);
+      ab[c4] = q.x;
+      ab[c4 + 1] = q.y;
+      ab[c4 + 2] = q.z;
+      ab[c4 + 3] = q.w;
+    }
+    st.merge(ml.x, ml.y, ab);
+  }
+  fwd_write<T>(A, L, hb.x, st);
+}
+
+// ---------------------------------------------------------------------------
+// backward pass 1: destination side
+// ---------------------------------------------------------------------------
+
+template <typename T>
+struct DstSums {
+  static constexpr int V = VecOf<T>::n;
+  float delta, P[V], Q[V], R[V], S[V];
+  __device__ __forceinline__ void init() {
+    delta = 0.f;
+    zero<V>(P);
+    zero<V>(Q);
+    zero<V>(R);
+    zero<V>(S);
+  }
+  __device__ __forceinline__ void subgroup_total(const Shape& s) {
+    delta = subgroup_sum(delta, s);
+    subgroup_sums<V>(P, s);
+    subgroup_sums<V>(Q, s);
+    subgroup_sums<V>(R, s);
+    subgroup_sums<V>(S, s);
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ void dst_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
+                                          int colbase, int beg, int end, int (&jn)[kUnroll],
+                                          const float (&xr)[VecOf<T>::n],
+                                          const float (&gi)[VecOf<T>::n],
+                                          const float (&a2)[VecOf<T>::n], float lse2,
+                                          DstSums<T>& sm) {
+  constexpr int V = VecOf<T>::n;
+  constexpr int U = kUnroll;
+  const int step = L.G * U;
+  for (int base = beg; base < end; base += step) {
+    int j[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) j[u] = jn[u];
+    uint4 raw[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      raw[u] = (j[u] >= 0 && L.ok[0]) ? ld16(row_base<T>(A.xl, j[u], A.s.rv) + 16 * L.q[0])
+                                      : make_uint4(0, 0, 0, 0);
+    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+    float red[2 * U];  // scores (base 2), then dout_i . xl_j
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float x[V];
+      unpack<T>(raw[u], x);
+      float p = 0.f, d = 0.f;
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        p = fmaf(a2[c], leaky(xr[c] + x[c], A.slope), p);
+        d = fmaf(gi[c], x[c], d);
+      }
+      red[u] = p;
+      red[U + u] = d;
+    }
+    head_sums<2 * U>(red, A.s.hv_log2);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float al = j[u] >= 0 ? ex2(red[u] - lse2) : 0.f;
+      const float ad = al * red[U + u];
+      sm.delta += ad;
+      float x[V];
+      unpack_alt<T>(raw[u], x);
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        const float z = xr[c] + x[c];
+        const float g = leaky_g(z, A.slope);
+        const float lz = z * g;
+        sm.P[c] = fmaf(ad, g, sm.P[c]);
+        sm.Q[c] = fmaf(al, g, sm.Q[c]);
+        sm.R[c] = fmaf(ad, lz, sm.R[c]);
+        sm.S[c] = fmaf(al, lz, sm.S[c]);
+      }
+    }
+  }
+}
+
+// From the totals of node i: write dxr_i and i's record, add i's share of datt
+// into dacc.
+template <typename T>
+__device__ __forceinline__ void dst_finish(const V2Args& A, const Lane<1>& L, int64_t i,
+                                           const DstSums<T>& sm, float lse2,
+                                           const float (&a)[VecOf<T>::n],
+                                           float (&dacc)[VecOf<T>::n]) {
+  constexpr int V = VecOf<T>::n;
+  if (!L.ok[0]) return;
+  float y[V];
+#pragma unroll
+  for (int c = 0; c < V; ++c) {
+    y[c] = a[c] * fmaf(-sm.delta, sm.Q[c], sm.P[c]);
+    dacc[c] += fmaf(-sm.delta, sm.S[c], sm.R[c]);
+  }
+  st16(reinterpret_cast<char*>(A.dxr) + i * int64_t(A.s.rv) * 16 + 16 * L.q[0], pack<T>(y));
+  if (L.head_leader(A.s, 0)) A.stats[i * A.s.H + L.k[0]] = make_float2(lse2, sm.delta);
+}
+
+// Fold the per-warp datt sums of this block (warp order) into da_part[row].
+template <int V>
+__device__ __forceinline__ void fold_da(const V2Args& A, const Lane<1>& L, int wid,
+                                        const float (&dacc)[V], float* buf, int64_t row) {
+  const int row_f = A.s.rv * V;
+  __syncthreads();
+  if (L.g == 0 && L.ok[0])
+#pragma unroll
+    for (int c = 0; c < V; ++c) buf[wid * row_f + L.q[0] * V + c] = dacc[c];
+  __syncthreads();
+  for (int t = threadIdx.x; t < row_f; t += blockDim.x) {
+    double s = 0.0;
+    for (int w = 0; w < kWarps; ++w) s += double(buf[w * row_f + t]);
+    A.da_part[row * row_f + t] = s;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) v2_dst_main(const V2Args A) {
+  constexpr int V = VecOf<T>::n;
+  const V2Dir& D = A.csr;
+  const Lane<1> L(A.s);
+  const int wid = threadIdx.x >> 5;
+  const int row_f = A.s.rv * V;
+  const int H = A.s.H;
+  extern __shared__ __align__(16) unsigned char smem[];
+  float a2[V], a[V], xr[V], gi[V], dacc[V];
+  att_slice<T>(A.att, L, kLog2e, a2);
+  att_slice<T>(A.att, L, 1.f, a);
+  zero<V>(dacc);
+  float* wbuf = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H + 4 row_f]
+
+  // ---- block items, assigned statically: item b, b + B, ... -------------
+  if (D.n_items > 0) {
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int32_t* cols = reinterpret_cast<int32_t*>(smem + 16);
+    uint32_t parity = 0;
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    __syncthreads();
+    for (int64_t it_i = blockIdx.x; it_i < D.n_items; it_i += gridDim.x) {
+      const int4 it = D.items[it_i];
+      if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
+      const int per = (it.z - it.y + kWarps - 1) / kWarps;
+      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      const int colbase = it.y & ~3;
+      int jn[kUnroll];
+      batch_ids<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
+      own_row<T>(A.xr, it.x, A.s, L, xr);
+      own_row<T>(A.dout, it.x, A.s, L, gi);
+      const float lse2 = L.ok[0] ? A.lse_in[int64_t(it.x) * H + L.k[0]] * kLog2e : 0.f;
+      DstSums<T> sm;
+      sm.init();
+      dst_edges<T>(A, L, cols, colbase, wb, we, jn, xr, gi, a2, lse2, sm);
+      sm.subgroup_total(A.s);
+      float* mine = wbuf + wid * (H + 4 * row_f);
+      if (L.g == 0 && L.ok[0]) {
+        if (L.head_leader(A.s, 0)) mine[L.k[0]] = sm.delta;
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          mine[H + 0 * row_f + L.q[0] * V + c] = sm.P[c];
+          mine[H + 1 * row_f + L.q[0] * V + c] = sm.Q[c];
+          mine[H + 2 * row_f + L.q[0] * V + c] = sm.R[c];
+          mine[H + 3 * row_f + L.q[0] * V + c] = sm.S[c];
+        }
+      }
+      __syncthreads();
+      if (wid == 0 && L.g == 0 && L.ok[0]) {
+        DstSums<T> tot;
+        tot.init();
+        for (int w = 0; w < kWarps; ++w) {
+          const float* o = wbuf + w * (H + 4 * row_f);
+          tot.delta += o[L.k[0]];
+#pragma unroll
+          for (int c = 0; c < V; ++c) {
+            tot.P[c] += o[H + 0 * row_f + L.q[0] * V + c];
+            tot.Q[c] += o[H + 1 * row_f + L.q[0] * V + c];
+            tot.R[c] += o[H + 2 * row_f + L.q[0] * V + c];
+            tot.S[c] += o[H + 3 * row_f + L.q[0] * V + c];
+          }
+        }
+        if (it.w < 0) {
+          dst_finish<T>(A, L, it.x, tot, lse2, a, dacc);
+        } else {
+          if (L.head_leader(A.s, 0)) A.d_delta[int64_t(it.w) * H + L.k[0]] = tot.delta;
+          float* pv = A.d_vec + int64_t(it.w) * 4 * row_f + L.q[0] * V;
+#pragma unroll
+          for (int c = 0; c < V; ++c) {
+            pv[0 * row_f + c] = tot.P[c];
+            pv[1 * row_f + c] = tot.Q[c];
+            pv[2 * row_f + c] = tot.R[c];
+            pv[3 * row_f + c] = tot.S[c];
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // ---- light nodes, assigned statically: groups of kGrab per warp ---------
+  const int64_t gw = int64_t(blockIdx.x) * kWarps + wid;
+  const int64_t W = int64_t(gridDim.x) * kWarps;
+  for (int64_t t0 = gw * kGrab; t0 < D.n_light; t0 += W * kGrab) {
+    int my_i = -1, my_b = 0, my_e = 0;
+    if (L.lane < kGrab && t0 + L.lane < D.n_light) {
+      my_i = D.light[t0 + L.lane];
+      my_b = D.ptr[my_i];
+      my_e = D.ptr[my_i + 1];
+    }
+    int i = __shfl_sync(kFull, my_i, 0);
+    int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
+    int jn[kUnroll];
+    batch_ids<kUnroll>(D.idx, 0, beg, end, L.g, L.G, jn);
+    for (int q = 0; q < kGrab && i >= 0; ++q) {
+      const int nq = (q + 1) & (kGrab - 1);
+      const int i2 = q + 1 < kGrab ? __shfl_sync(kFull, my_i, nq) : -1;
+      const int b2 = __shfl_sync(kFull, my_b, nq);
+      const int e2 = __shfl_sync(kFull, my_e, nq);
+      int jn2[kUnroll];
+      batch_ids<kUnroll>(D.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
+      own_row<T>(A.xr, i, A.s, L, xr);
+      own_row<T>(A.dout, i, A.s, L, gi);
+      const float lse2 = L.ok[0] ? A.lse_in[int64_t(i) * H + L.k[0]] * kLog2e : 0.f;
+      DstSums<T> sm;
+      sm.init();
+      dst_edges<T>(A, L, D.idx, 0, beg, end, jn, xr, gi, a2, lse2, sm);
+      sm.subgroup_total(A.s);
+      if (L.g == 0) dst_finish<T>(A, L, i, sm, lse2, a, dacc);
+      i = i2;
+      beg = b2;
+      end = e2;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) jn[u] = jn2[u];
+    }
+  }
+  fold_da<V>(A, L, wid, dacc, wbuf, blockIdx.x);
+}
+
+// One warp per CSR hub (static): add its chunk sums in chunk order, finish the
+// node; each block's datt shares go to da_part[da_main_rows + block].
+template <typename T>
+__global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
+  constexpr int V = VecOf<T>::n;
+  const Lane<1> L(A.s);
+  const int wid = threadIdx.x >> 5;
+  const int64_t t = int64_t(blockIdx.x) * kWarps + wid;
+  const int row_f = A.s.rv * V;
+  const int H = A.s.H;
+  __shared__ float buf[kWarps * 256];  // rows of at most 512 bytes: <= 256 floats
+  float a[V], dacc[V];
+  att_slice<T>(A.att, L, 1.f, a);
+  zero<V>(dacc);
+  if (t < A.csr.n_hubs && L.g == 0 && L.ok[0]) {
+    const int4 hb = A.csr.hubs[t];
+    DstSums<T> tot;
+    tot.init();
+    for (int c = 0; c < hb.z; ++c) {
+      const int64_t slot = int64_t(hb.y) + c;
+      tot.delta += A.d_delta[slot * H + L.k[0]];
+      const float* pv = A.d_vec + slot * 4 * row_f + L.q[0] * V;
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        tot.P[e] += pv[0 * row_f + e];
+        tot.Q[e] += pv[1 * row_f + e];
+        tot.R[e] += pv[2 * row_f + e];
+        tot.S[e] += pv[3 * row_f + e];
+      }
+    }
+    const float lse2 = A.lse_in[int64_t(hb.x) * H + L.k[0]] * kLog2e;
+    dst_finish<T>(A, L, hb.x, tot, lse2, a, dacc);
+  }
+  fold_da<V>(A, L, wid, dacc, buf, A.da_main_rows + blockIdx.x);
+}
+
+// ---------------------------------------------------------------------------
+// backward pass 2: source side
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
+                                          int colbase, int beg, int end, int (&in)[kUnroll],
+                                          const float (&xl)[VecOf<T>::n],
+                                          const float (&a2)[VecOf<T>::n],
+                                          const float (&a)[VecOf<T>::n],
+                                          float (&acc)[VecOf<T>::n]) {
+  constexpr int V = VecOf<T>::n;
+  constexpr int U = kUnroll;
+  const int step = L.G * U;
+  const int H = A.s.H;
+  for (int base = beg; base < end; base += step) {
+    int i[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) i[u] = in[u];
+    uint4 rr[U], rg[U];
+    float2 st[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool ok = i[u] >= 0 && L.ok[0];
+      rr[u] = ok ? ld16(row_base<T>(A.xr, i[u], A.s.rv) + 16 * L.q[0]) : make_uint4(0, 0, 0, 0);
+      rg[u] = ok ? ld16(row_base<T>(A.dout, i[u], A.s.rv) + 16 * L.q[0]) : make_uint4(0, 0, 0, 0);
+      st[u] = ok ? __ldg(A.stats + int64_t(i[u]) * H + L.k[0]) : make_float2(0.f, 0.f);
+    }
+    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, in);
+    float red[2 * U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float r[V], g[V];
+      unpack<T>(rr[u], r);
+      unpack<T>(rg[u], g);
+      float p = 0.f, d = 0.f;
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        p = fmaf(a2[c], leaky(r[c] + xl[c], A.slope), p);
+        d = fmaf(g[c], xl[c], d);
+      }
+      red[u] = p;
+      red[U + u] = d;
+    }
+    head_sums<2 * U>(red, A.s.hv_log2);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float al = i[u] >= 0 ? ex2(red[u] - st[u].x) : 0.f;
+      const float de = al * (red[U + u] - st[u].y);
+      float r[V], g[V];
+      unpack_alt<T>(rr[u], r);
+      unpack_alt<T>(rg[u], g);
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        const float gz = leaky_g(r[c] + xl[c], A.slope);
+        acc[c] = fmaf(al, g[c], fmaf(de * a[c], gz, acc[c]));
+      }
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void src_write(const V2Args& A, const Lane<1>& L, int64_t j,
+                                          const float (&acc)[VecOf<T>::n]) {
+  if (!L.ok[0]) return;
+  st16(reinterpret_cast<char*>(A.dxl) + j * int64_t(A.s.rv) * 16 + 16 * L.q[0], pack<T>(acc));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) v2_src_main(const V2Args A) {
+  constexpr int V = VecOf<T>::n;
+  const V2Dir& D = A.csc;
+  const Lane<1> L(A.s);
+  const int wid = threadIdx.x >> 5;
+  const int row_f = A.s.rv * V;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_item;
+  float a2[V], a[V], xl[V], acc[V];
+  att_slice<T>(A.att, L, kLog2e, a2);
+  att_slice<T>(A.att, L, 1.f, a);
+
+  if (D.n_items > 0) {
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int32_t* cols = reinterpret_cast<int32_t*>(smem + 16);
+    float* wacc = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][row_f]
+    uint32_t parity = 0;
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    for (;;) {
+      if (threadIdx.x == 0) s_item = atomicAdd(A.ctr + 2, 1);
+      __syncthreads();
+      const int it_i = s_item;
+      if (it_i >= D.n_items) break;
+      const int4 it = D.items[it_i];
+      if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
+      const int per = (it.z - it.y + kWarps - 1) / kWarps;
+      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      const int colbase = it.y & ~3;
+      int in[kUnroll];
+      batch_ids<kUnroll>(cols, colbase, wb, we, L.g, L.G, in);
+      own_row<T>(A.xl, it.x, A.s, L, xl);
+      zero<V>(acc);
+      src_edges<T>(A, L, cols, colbase, wb, we, in, xl, a2, a, acc);
+      subgroup_sums<V>(acc, A.s);
+      if (L.g == 0 && L.ok[0])
+#pragma unroll
+        for (int c = 0; c < V; ++c) wacc[wid * row_f + L.q[0] * V + c] = acc[c];
+      __syncthreads();
+      if (wid == 0 && L.g == 0 && L.ok[0]) {
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          float s = 0.f;
+          for (int w = 0; w < kWarps; ++w) s += wacc[w * row_f + L.q[0] * V + c];
+          acc[c] = s;
+        }
+        if (it.w < 0) {
+          src_write<T>(A, L, it.x, acc);
+        } else {
+          float* pa = A.s_acc + int64_t(it.w) * row_f + L.q[0] * V;
+#pragma unroll
+          for (int c4 = 0; c4 < V; c4 += 4)
+            *reinterpret_cast<float4*>(pa + c4) =
+                make_float4(acc[c4], acc[c4 + 1], acc[c4 + 2], acc[c4 + 3]);
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  for (;;) {
+    int t0 = 0;
+    if (L.lane == 0) t0 = atomicAdd(A.ctr + 3, kGrab);
+    t0 = __shfl_sync(kFull, t0, 0);
+    if (t0 >= D.n_light) break;
+    int my_j = -1, my_b = 0, my_e = 0;
+    if (L.lane < kGrab && t0 + L.lane < D.n_light) {
+      my_j = D.light[t0 + L.lane];
+      my_b = D.ptr[my_j];
+      my_e = D.ptr[my_j + 1];
+    }
+    int j = __shfl_sync(kFull, my_j, 0);
+    int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
+    int in[kUnroll];
+    batch_ids<kUnroll>(D.idx, 0, beg, end, L.g, L.G, in);
+    for (int q = 0; q < kGrab && j >= 0; ++q) {
+      const int nq = (q + 1) & (kGrab - 1);
+      const int j2 = q + 1 < kGrab ? __shfl_sync(kFull, my_j, nq) : -1;
+      const int b2 = __shfl_sync(kFull, my_b, nq);
+      const int e2 = __shfl_sync(kFull, my_e, nq);
+      int in2[kUnroll];
+      batch_ids<kUnroll>(D.idx, 0, b2, j2 >= 0 ? e2 : b2, L.g, L.G, in2);
+      own_row<T>(A.xl, j, A.s, L, xl);
+      zero<V>(acc);
+      src_edges<T>(A, L, D.idx, 0, beg, end, in, xl, a2, a, acc);
+      subgroup_sums<V>(acc, A.s);
+      if (L.g == 0) src_write<T>(A, L, j, acc);
+      j = j2;
+      beg = b2;
+      end = e2;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) in[u] = in2[u];
+    }
+  }
+}
+
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
+  const float y = __fsub_rn(x, c);
+  const float t = __fadd_rn(s, y);
+  c = __fsub_rn(__fsub_rn(t, s), y);
+  s = t;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) v2_src_merge(const V2Args A) {
+  constexpr int V = VecOf<T>::n;
+  const Lane<1> L(A.s);
+  const int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (t >= A.csc.n_hubs || L.g != 0 || !L.ok[0]) return;
+  const int4 hb = A.csc.hubs[t];
+  const int row_f = A.s.rv * V;
+  float acc[V], cmp[V];
+  zero<V>(acc);
+  zero<V>(cmp);
+  for (int c = 0; c < hb.z; ++c) {
+    const float* pa = A.s_acc + (int64_t(hb.y) + c) * row_f + L.q[0] * V;
+#pragma unroll
+    for (int e = 0; e < V; ++e) kahan_add(acc[e], cmp[e], pa[e]);
+  }
+  src_write<T>(A, L, hb.x, acc);
+}
+
+// datt = fixed-order float64 sum of the da_part rows (one warp per element).
+__global__ void __launch_bounds__(kThreads) v2_datt_final(const double* part, int rows,
+                                                          int row_f, float* datt) {
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= row_f) return;
+  double s = 0.0;
+#pragma unroll 8
+  for (int r = lane; r < rows; r += 32) s += part[int64_t(r) * row_f + t];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+  if (lane == 0) datt[t] = float(s);
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+}
+
+template <typename T>
+cudaError_t fwd_t(const V2Args& A, int sm_count, cudaStream_t st) {
+  constexpr int V = VecOf<T>::n;
+  const int row_f = A.s.rv * V;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), st)) != cudaSuccess) return e;
+  const V2Dir& D = A.csr;
+  if (D.n_items + D.n_light > 0) {
+    const size_t smem = size_t(D.col_off) + size_t(kWarps) * (2 * A.s.H + row_f) * 4;
+    if ((e = set_smem(v2_fwd_main<T>, smem)) != cudaSuccess) return e;
+    const int64_t work = D.n_items + (D.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
+    const int64_t cap = persistent_blocks(v2_fwd_main<T>, smem, sm_count);
+    v2_fwd_main<T><<<unsigned(work < cap ? work : cap), kThreads, smem, st>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (D.n_hubs > 0) {
+    v2_fwd_merge<T><<<unsigned((D.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t bwd_t(V2Args A, int sm_count, cudaStream_t st) {
+  constexpr int V = VecOf<T>::n;
+  const int row_f = A.s.rv * V;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), st)) != cudaSuccess) return e;
+  // pass 1: a fixed grid (static work assignment), one da_part row per block
+  {
+    const V2Dir& D = A.csr;
+    const size_t smem = size_t(D.col_off) + size_t(kWarps) * (A.s.H + 4 * row_f) * 4;
+    if ((e = set_smem(v2_dst_main<T>, smem)) != cudaSuccess) return e;
+    int64_t blocks = persistent_blocks(v2_dst_main<T>, smem, sm_count);
+    const int64_t cap = int64_t(sm_count > 0 ? sm_count : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    A.da_main_rows = int(blocks);
+    v2_dst_main<T><<<unsigned(blocks), kThreads, smem, st>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t mblocks = (D.n_hubs + kWarps - 1) / kWarps;
+    if (mblocks > 0) {
+      v2_dst_merge<T><<<unsigned(mblocks), kThreads, 0, st>>>(A);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    v2_datt_final<<<unsigned((row_f + kWarps - 1) / kWarps), kThreads, 0, st>>>(
+        A.da_part, int(blocks + mblocks), row_f, A.datt);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // pass 2
+  {
+    const V2Dir& D = A.csc;
+    if (D.n_items + D.n_light > 0) {
+      const size_t smem = size_t(D.col_off) + size_t(kWarps) * row_f * 4;
+      if ((e = set_smem(v2_src_main<T>, smem)) != cudaSuccess) return e;
+      const int64_t work = D.n_items + (D.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
+      const int64_t cap = persistent_blocks(v2_src_main<T>, smem, sm_count);
+      v2_src_main<T><<<unsigned(work < cap ? work : cap), kThreads, smem, st>>>(A);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (D.n_hubs > 0) {
+      v2_src_merge<T><<<unsigned((D.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+  }
+  return cudaSuccess;
+}
+
+V2Dir v2_dir(const Dir& d) {
+  V2Dir a{};
+  a.ptr = d.ptr;
+  a.idx = d.idx;
+  a.light = d.light;
+  a.n_light = d.n_light;
+  a.items = d.items;
+  a.n_items = d.n_items;
+  a.hubs = d.hubs;
+  a.n_hubs = d.n_hubs;
+  a.col_off = int(16 + align_up(size_t(d.max_item + 4) * 4, 16));
+  return a;
+}
+
+struct V2Layout {
+  size_t ctr, f_acc, f_ml, stats, d_delta, d_vec, s_acc, da_part, total;
+};
+
+V2Layout v2_layout(const gnn_graph* g, const Shape& s) {
+  const size_t row_f = size_t(s.rv) * 16 / s.esize;
+  const size_t cc = size_t(g->csr.n_hub_chunks), sc = size_t(g->csc.n_hub_chunks);
+  const size_t da_rows = size_t(g->sm_count > 0 ? g->sm_count : 1) * 8 +
+                         size_t((g->csr.n_hubs + kWarps - 1) / kWarps);
+  V2Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t r = off;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return r;
+  };
+  L.ctr = take(kCounters * 4);
+  L.f_acc = take(cc * row_f * 4);
+  L.f_ml = take(cc * s.H * 8);
+  L.stats = take(size_t(g->n) * s.H * 8);
+  L.d_delta = take(cc * s.H * 4);
+  L.d_vec = take(cc * 4 * row_f * 4);
+  L.s_acc = take(sc * row_f * 4);
+  L.da_part = take(da_rows * row_f * 8);
+  L.total = off;
+  return L;
+}
+
+V2Args v2_args(const gnn_graph* g, const Shape& s, const void* xl, const void* xr,
+               const float* att, float slope, char* ws) {
+  const V2Layout W = v2_layout(g, s);
+  V2Args A{};
+  A.s = s;
+  A.csr = v2_dir(g->csr);
+  A.csc = v2_dir(g->csc);
+  A.n = g->n;
+  A.xl = xl;
+  A.xr = xr;
+  A.att = att;
+  A.slope = slope;
+  A.ctr = reinterpret_cast<int*>(ws + W.ctr);
+  A.f_acc = reinterpret_cast<float*>(ws + W.f_acc);
+  A.f_ml = reinterpret_cast<float2*>(ws + W.f_ml);
+  A.stats = reinterpret_cast<float2*>(ws + W.stats);
+  A.d_delta = reinterpret_cast<float*>(ws + W.d_delta);
+  A.d_vec = reinterpret_cast<float*>(ws + W.d_vec);
+  A.s_acc = reinterpret_cast<float*>(ws + W.s_acc);
+  A.da_part = reinterpret_cast<double*>(ws + W.da_part);
+  A.err = g->err;
+  return A;
+}
+
+}  // namespace
+
+size_t gatv2_ws_bytes(const gnn_graph* g, const Shape& s) { return v2_layout(g, s).total; }
+
+cudaError_t launch_gatv2_forward(const gnn_graph* g, const Shape& s, gnn_dtype dt,
+                                 const void* xl, const void* xr, const float* att, float slope,
+                                 void* out, float* lse, char* ws, cudaStream_t st) {
+  V2Args A = v2_args(g, s, xl, xr, att, slope, ws);
+  A.out = out;
+  A.lse = lse;
+  return dt == GNN_F32 ? fwd_t<float>(A, g->sm_count, st)
+                       : fwd_t<__nv_bfloat16>(A, g->sm_count, st);
+}
+
+cudaError_t launch_gatv2_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt,
+                                  const void* xl, const void* xr, const float* att, float slope,
+                                  const float* lse, const void* dout, void* dxl, void* dxr,
+                                  float* datt, char* ws, cudaStream_t st) {
+  V2Args A = v2_args(g, s, xl, xr, att, slope, ws);
+  A.lse_in = lse;
+  A.dout = dout;
+  A.dxl = dxl;
+  A.dxr = dxr;
+  A.datt = datt;
+  return dt == GNN_F32 ? bwd_t<float>(A, g->sm_count, st)
+                       : bwd_t<__nv_bfloat16>(A, g->sm_count, st);
+}
+
+}  // namespace gnn

@@ -96,6 +96,38 @@ cudaError_t launch_spmm(const gnn_graph* g, const Shape& s, gnn_dtype dt, int no
                         const void* x, void* out, char* ws, cudaStream_t st);
 size_t spmm_ws_bytes(const gnn_graph* g, const Shape& s);
 
+// Max / min neighbourhood reduction (reduce.cu).  Workspace: counters,
+// packed hub keys, float32 gradient accumulator.
+size_t reduce_ws_bytes(const gnn_graph* g, const Shape& s);
+cudaError_t launch_reduce_forward(const gnn_graph* g, const Shape& s, gnn_dtype dt, int op,
+                                  const void* x, void* out, int32_t* arg, char* ws,
+                                  cudaStream_t st);
+cudaError_t launch_reduce_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt,
+                                   const int32_t* arg, const void* dout, void* dx, char* ws,
+                                   cudaStream_t st);
+
+// GATv2 attention (gatv2.cu), rows of at most 512 bytes.
+size_t gatv2_ws_bytes(const gnn_graph* g, const Shape& s);
+cudaError_t launch_gatv2_forward(const gnn_graph* g, const Shape& s, gnn_dtype dt,
+                                 const void* xl, const void* xr, const float* att, float slope,
+                                 void* out, float* lse, char* ws, cudaStream_t st);
+cudaError_t launch_gatv2_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt,
+                                  const void* xl, const void* xr, const float* att, float slope,
+                                  const float* lse, const void* dout, void* dxl, void* dxr,
+                                  float* datt, char* ws, cudaStream_t st);
+
+// Graph-transformer attention (transformer.cu), rows of at most 512 bytes.
+size_t transformer_ws_bytes(const gnn_graph* g, const Shape& s);
+cudaError_t launch_transformer_forward(const gnn_graph* g, const Shape& s, gnn_dtype dt,
+                                       const void* q, const void* key, const void* val,
+                                       float scale, void* out, float* lse, char* ws,
+                                       cudaStream_t st);
+cudaError_t launch_transformer_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt,
+                                        const void* q, const void* key, const void* val,
+                                        float scale, const float* lse, const void* dout,
+                                        void* dq, void* dkey, void* dval, char* ws,
+                                        cudaStream_t st);
+
 // Graph preparation (prepare.cu).
 gnn_status prepare_graph(gnn_graph* g, const int32_t* row_ptr, const int32_t* col,
                          char* buffer, size_t buffer_bytes, char* scratch, size_t scratch_bytes,

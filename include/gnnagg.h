@@ -247,6 +247,107 @@ gnn_status gcn_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, gnn_norm
                             const void* dout, void* dx, void* ws, size_t ws_bytes,
                             void* stream);
 
+/* ---- GATv2 attention -------------------------------------------------------
+ *
+ * For each destination i and head k, with xl = W_l h (source side; also the
+ * aggregated value) and xr = W_r h (destination side) computed by the caller:
+ *     e_ij     = att[k] . LeakyReLU(xr_i[k] + xl_j[k])
+ *     alpha    = softmax over the in-neighbours j of i of e_ij
+ *     out_i[k] = sum_j alpha_ij xl_j[k],   lse_i[k] = log sum_j exp(e_ij)
+ * (Brody et al., "How Attentive are Graph Attention Networks?", ICLR 2022,
+ * eq. 7; the GATv2 layer of "On Efficient Scaling of GNNs via IO-Aware
+ * Layers Implementations", Technical Summary > Methodology, attention-based
+ * layers).  Same streaming design as the GAT calls: one pass over each
+ * node's in-neighbours with an online softmax, no per-edge tensor in device
+ * memory, lse kept for the backward, which walks the CSR (destination side:
+ * dxr and datt) and the cached CSC (source side: dxl).  Results, datt
+ * included, are bitwise reproducible.
+ * Layout: xl, xr, out, dout, dxl, dxr [N][H][D] dtype; att, datt [H][D]
+ * float; lse [N][H] float.  Shapes as for the GAT calls, with the further
+ * limit H * D * sizeof(dtype) <= 512 bytes.  Pointers 16-byte aligned (lse
+ * 4), ws 256-byte aligned and >= gatv2_agg_workspace_bytes (hub-chunk
+ * partial states, an 8-byte per-(node, head) record, per-block float64
+ * datt sums).  Asynchronous on `stream`. */
+size_t gatv2_agg_workspace_bytes(const gnn_graph* g, int H, int D, gnn_dtype dtype);
+
+gnn_status gatv2_agg_forward(const gnn_graph* g, int H, int D, gnn_dtype dtype, const void* xl,
+                             const void* xr, const float* att, float slope, void* out,
+                             float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Gradients of L(out) given dout and the forward's lse: writes every element
+ * of dxl, dxr (dtype) and datt (float). */
+gnn_status gatv2_agg_backward(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                              const void* xl, const void* xr, const float* att, float slope,
+                              const float* lse, const void* dout, void* dxl, void* dxr,
+                              float* datt, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- Graph-transformer attention -------------------------------------------
+ *
+ * For each destination i and head k, with the query, key and value
+ * projections q, key, val computed by the caller:
+ *     e_ij     = scale * q_i[k] . key_j[k]        (scale = 1/sqrt(D) usually)
+ *     alpha    = softmax over the in-neighbours j of i of e_ij
+ *     out_i[k] = sum_j alpha_ij val_j[k],   lse_i[k] = log sum_j exp(e_ij)
+ * (Shi et al., "Masked Label Prediction: Unified Message Passing Model for
+ * Semi-Supervised Classification", IJCAI 2021, eqs. 3-4; the Graph
+ * Transformer layer of "On Efficient Scaling of GNNs via IO-Aware Layers
+ * Implementations", Technical Summary > Methodology, attention-based
+ * layers).  One streaming pass per node with an online softmax; no per-edge
+ * tensor in device memory; the backward recomputes alpha from lse, walking
+ * the CSR for dq and the cached CSC for dkey and dval.  Bitwise
+ * reproducible.
+ * Layout: q, key, val, out, dout, dq, dkey, dval [N][H][D] dtype; lse [N][H]
+ * float.  Shapes as for gatv2 (H * D * sizeof(dtype) <= 512 bytes).
+ * Pointers 16-byte aligned (lse 4), ws 256-byte aligned and >=
+ * transformer_agg_workspace_bytes.  Asynchronous on `stream`. */
+size_t transformer_agg_workspace_bytes(const gnn_graph* g, int H, int D, gnn_dtype dtype);
+
+gnn_status transformer_agg_forward(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                                   const void* q, const void* key, const void* val, float scale,
+                                   void* out, float* lse, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/* Writes every element of dq, dkey and dval. */
+gnn_status transformer_agg_backward(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                                    const void* q, const void* key, const void* val, float scale,
+                                    const float* lse, const void* dout, void* dq, void* dkey,
+                                    void* dval, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- Max / min neighbourhood reduction -----------------------------------
+ *
+ * out[i][f] = max (or min) over the in-neighbours j of i of x[j][f], and
+ * arg[i][f] = the winning j (the smallest j among equal values); a node with
+ * no in-neighbours gets out = 0 and arg = -1.  The reduction-based
+ * aggregation of "On Efficient Scaling of GNNs via IO-Aware Layers
+ * Implementations" (Technical Summary > Methodology, reduction-based
+ * aggregations: per-edge message, then a neighbourhood max or min) with the
+ * message x_j (per-node transforms are the caller's).  Degree-aware tiling
+ * as on that page: a warp per light node, a block per mid node, hubs split
+ * into edge chunks merged by 64-bit atomicMax on packed (value, source)
+ * keys.  out and arg are exact (out is always an input value) and bitwise
+ * reproducible.  Inputs must not hold NaN.
+ * Backward: dx[j][f] = sum of dout[i][f] over the i with arg[i][f] = j,
+ * accumulated with float32 atomic adds; where several destinations share a
+ * winner the order of those additions, and so the last bits of dx, may vary
+ * from run to run.
+ * Shapes as for the GCN calls (F * sizeof(dtype) a multiple of 16, at most
+ * 2048 bytes).  x, out, dout, dx: [N][F] dtype; arg: [N][F] int32; all
+ * device, 16-byte aligned; ws 256-byte aligned, >= reduce_agg_workspace_bytes
+ * (counters, N_hub_chunks * F packed keys, and N * F floats for the
+ * backward's accumulator).  Asynchronous on `stream`. */
+typedef enum { GNN_REDUCE_MAX = 0, GNN_REDUCE_MIN = 1 } gnn_reduce_op;
+
+size_t reduce_agg_workspace_bytes(const gnn_graph* g, int F, gnn_dtype dtype);
+
+gnn_status reduce_agg_forward(const gnn_graph* g, int F, gnn_dtype dtype, gnn_reduce_op op,
+                              const void* x, void* out, int32_t* arg, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* dx [N][F] from the forward's arg and dout; writes every element of dx. */
+gnn_status reduce_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, const int32_t* arg,
+                               const void* dout, void* dx, void* ws, size_t ws_bytes,
+                               void* stream);
+
 /* Synchronises `stream`, reads and clears the graph's device status word.
  * Returns GNN_OK, GNN_ERR_TIMEOUT (a bounded wait on an asynchronous copy ran
  * out) or GNN_ERR_DEVICE_ASSERT; *info (may be NULL) receives the raw word. */

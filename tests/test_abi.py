@@ -20,7 +20,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b((?:gnn|gat|gcn)_[a-z0-9_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:gnn|gat|gatv2|gcn|reduce|transformer)_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():

@@ -68,3 +68,15 @@ def test_full_size_sampled_parity(idx):
     assert_close(_rows(out, sel_f), sf["out"], w.dtype, sf["out_mag"], f"cfg{idx} gcn out")
     sb = oracle.spmm_backward_rows(rp, ci, dout.reshape(n, F), "sym", sel_b, with_mag=True)
     assert_close(_rows(dx, sel_b), sb["dx"], w.dtype, sb["dx_mag"], f"cfg{idx} gcn dx")
+    # max reduction: sampled rows bit for bit, sampled gradient rows
+    rout, rarg = gnn.reduce_forward(g, x, "max")
+    rdx = gnn.reduce_backward(g, rarg, dy)
+    torch.cuda.synchronize()
+    rf = oracle.reduce_forward(rp, ci, h.reshape(n, F), "max", sel=sel_f)
+    sel_t = torch.from_numpy(np.asarray(sel_f, np.int64)).to(rarg.device)
+    assert np.array_equal(rarg[sel_t].cpu().numpy(), rf["arg"]), f"cfg{idx} max arg"
+    assert np.array_equal(_rows(rout, sel_f), rf["out"]), f"cfg{idx} max out"
+    cheap_r = sel_b[cost[sel_b] < 2e4][:150]     # the oracle recomputes every row they win
+    rb = oracle.reduce_backward_rows(rp, ci, h.reshape(n, F), "max", dout.reshape(n, F), cheap_r,
+                                     with_mag=True)
+    assert_close(_rows(rdx, cheap_r), rb["dx"], w.dtype, rb["dx_mag"], f"cfg{idx} max dx")
