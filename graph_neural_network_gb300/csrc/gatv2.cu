@@ -78,6 +78,21 @@ struct V2Args {
 __device__ __forceinline__ float leaky(float z, float s) { return z > 0.f ? z : s * z; }
 __device__ __forceinline__ float leaky_g(float z, float s) { return z > 0.f ? 1.f : s; }
 
+// For z = r + x elementwise: g = LeakyReLU'(z) and lz = LeakyReLU(z) = g z,
+// with the additions and products done two lanes of data at a time.
+template <int V>
+__device__ __forceinline__ void leaky_terms(const float (&r)[V], const float (&x)[V],
+                                            float slope, float (&g)[V], float (&lz)[V]) {
+#pragma unroll
+  for (int c = 0; c < V; c += 2) {
+    float z0, z1;
+    add2(z0, z1, r[c], r[c + 1], x[c], x[c + 1]);
+    g[c] = leaky_g(z0, slope);
+    g[c + 1] = leaky_g(z1, slope);
+    mul2v(lz[c], lz[c + 1], z0, z1, g[c], g[c + 1]);
+  }
+}
+
 template <int U>
 __device__ __forceinline__ void batch_ids(const int32_t* cols, int colbase, int beg, int end,
                                           int g, int G, int (&j)[U]) {
@@ -177,15 +192,10 @@ __device__ __forceinline__ void fwd_edges(const V2Args& A, const Lane<1>& L, con
     float sc[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float x[V];
+      float x[V], g[V], lz[V];
       unpack<T>(raw[u], x);
-      float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < V; c += 2) {
-        p0 = fmaf(a2[c], leaky(xr[c] + x[c], A.slope), p0);
-        p1 = fmaf(a2[c + 1], leaky(xr[c + 1] + x[c + 1], A.slope), p1);
-      }
-      sc[u] = p0 + p1;
+      leaky_terms<V>(xr, x, A.slope, g, lz);
+      sc[u] = dot<V>(lz, a2);
     }
     head_sums<U>(sc, A.s.hv_log2);
     float bm = -INFINITY;
@@ -412,16 +422,11 @@ __device__ __forceinline__ void dst_edges(const V2Args& A, const Lane<1>& L, con
     float red[2 * U];  // scores (base 2), then dout_i . xl_j
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float x[V];
+      float x[V], g[V], lz[V];
       unpack<T>(raw[u], x);
-      float p = 0.f, d = 0.f;
-#pragma unroll
-      for (int c = 0; c < V; ++c) {
-        p = fmaf(a2[c], leaky(xr[c] + x[c], A.slope), p);
-        d = fmaf(gi[c], x[c], d);
-      }
-      red[u] = p;
-      red[U + u] = d;
+      leaky_terms<V>(xr, x, A.slope, g, lz);
+      red[u] = dot<V>(lz, a2);
+      red[U + u] = dot<V>(x, gi);
     }
     head_sums<2 * U>(red, A.s.hv_log2);
 #pragma unroll
@@ -429,50 +434,49 @@ __device__ __forceinline__ void dst_edges(const V2Args& A, const Lane<1>& L, con
       const float al = j[u] >= 0 ? ex2(red[u] - lse2) : 0.f;
       const float ad = al * red[U + u];
       sm.delta += ad;
-      float x[V];
+      float x[V], g[V], lz[V];
       unpack_alt<T>(raw[u], x);
-#pragma unroll
-      for (int c = 0; c < V; ++c) {
-        const float z = xr[c] + x[c];
-        const float g = leaky_g(z, A.slope);
-        const float lz = z * g;
-        sm.P[c] = fmaf(ad, g, sm.P[c]);
-        sm.Q[c] = fmaf(al, g, sm.Q[c]);
-        sm.R[c] = fmaf(ad, lz, sm.R[c]);
-        sm.S[c] = fmaf(al, lz, sm.S[c]);
-      }
+      leaky_terms<V>(xr, x, A.slope, g, lz);
+      axpy<V>(sm.P, ad, g);
+      axpy<V>(sm.Q, al, g);
+      axpy<V>(sm.R, ad, lz);
+      axpy<V>(sm.S, al, lz);
     }
   }
 }
 
 // From the totals of node i: write dxr_i and i's record, add i's share of datt
-// into dacc.
+// into this warp's datt sums dslot[row_f] (shared memory; the lane's own
+// elements, so no other lane touches them).
 template <typename T>
 __device__ __forceinline__ void dst_finish(const V2Args& A, const Lane<1>& L, int64_t i,
-                                           const DstSums<T>& sm, float lse2,
-                                           const float (&a)[VecOf<T>::n],
-                                           float (&dacc)[VecOf<T>::n]) {
+                                           const DstSums<T>& sm, float lse2, float* dslot) {
   constexpr int V = VecOf<T>::n;
   if (!L.ok[0]) return;
-  float y[V];
+  float a[V], y[V];
+  att_slice<T>(A.att, L, 1.f, a);
+  float* d = dslot + L.q[0] * V;
 #pragma unroll
   for (int c = 0; c < V; ++c) {
     y[c] = a[c] * fmaf(-sm.delta, sm.Q[c], sm.P[c]);
-    dacc[c] += fmaf(-sm.delta, sm.S[c], sm.R[c]);
+    d[c] += fmaf(-sm.delta, sm.S[c], sm.R[c]);
   }
   st16(reinterpret_cast<char*>(A.dxr) + i * int64_t(A.s.rv) * 16 + 16 * L.q[0], pack<T>(y));
   if (L.head_leader(A.s, 0)) A.stats[i * A.s.H + L.k[0]] = make_float2(lse2, sm.delta);
 }
 
-// Fold the per-warp datt sums of this block (warp order) into da_part[row].
+// Zero this warp's datt sums (its g == 0 lanes own them).
 template <int V>
-__device__ __forceinline__ void fold_da(const V2Args& A, const Lane<1>& L, int wid,
-                                        const float (&dacc)[V], float* buf, int64_t row) {
-  const int row_f = A.s.rv * V;
-  __syncthreads();
+__device__ __forceinline__ void zero_da(const Lane<1>& L, float* dslot) {
   if (L.g == 0 && L.ok[0])
 #pragma unroll
-    for (int c = 0; c < V; ++c) buf[wid * row_f + L.q[0] * V + c] = dacc[c];
+    for (int c = 0; c < V; ++c) dslot[L.q[0] * V + c] = 0.f;
+}
+
+// Fold the per-warp datt sums buf[kWarps][row_f] of this block (warp order)
+// into da_part[row].
+__device__ __forceinline__ void fold_da(const V2Args& A, int row_f, const float* buf,
+                                        int64_t row) {
   __syncthreads();
   for (int t = threadIdx.x; t < row_f; t += blockDim.x) {
     double s = 0.0;
@@ -490,11 +494,12 @@ __global__ void __launch_bounds__(kThreads, 2) v2_dst_main(const V2Args A) {
   const int row_f = A.s.rv * V;
   const int H = A.s.H;
   extern __shared__ __align__(16) unsigned char smem[];
-  float a2[V], a[V], xr[V], gi[V], dacc[V];
+  float a2[V], xr[V], gi[V];
   att_slice<T>(A.att, L, kLog2e, a2);
-  att_slice<T>(A.att, L, 1.f, a);
-  zero<V>(dacc);
   float* wbuf = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H + 4 row_f]
+  float* dsum = wbuf + kWarps * (H + 4 * row_f);              // [kWarps][row_f] datt sums
+  float* dslot = dsum + wid * row_f;
+  zero_da<V>(L, dslot);
 
   // ---- block items, assigned statically: item b, b + B, ... -------------
   if (D.n_items > 0) {
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 2) v2_dst_main(const V2Args A) {
           }
         }
         if (it.w < 0) {
-          dst_finish<T>(A, L, it.x, tot, lse2, a, dacc);
+          dst_finish<T>(A, L, it.x, tot, lse2, dslot);
         } else {
           if (L.head_leader(A.s, 0)) A.d_delta[int64_t(it.w) * H + L.k[0]] = tot.delta;
           float* pv = A.d_vec + int64_t(it.w) * 4 * row_f + L.q[0] * V;
@@ -590,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 2) v2_dst_main(const V2Args A) {
       sm.init();
       dst_edges<T>(A, L, D.idx, 0, beg, end, jn, xr, gi, a2, lse2, sm);
       sm.subgroup_total(A.s);
-      if (L.g == 0) dst_finish<T>(A, L, i, sm, lse2, a, dacc);
+      if (L.g == 0) dst_finish<T>(A, L, i, sm, lse2, dslot);
       i = i2;
       beg = b2;
       end = e2;
@@ -598,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 2) v2_dst_main(const V2Args A) {
       for (int u = 0; u < kUnroll; ++u) jn[u] = jn2[u];
     }
   }
-  fold_da<V>(A, L, wid, dacc, wbuf, blockIdx.x);
+  fold_da(A, row_f, dsum, blockIdx.x);
 }
 
 // One warp per CSR hub (static): add its chunk sums in chunk order, finish the
@@ -612,9 +617,8 @@ __global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
   const int row_f = A.s.rv * V;
   const int H = A.s.H;
   __shared__ float buf[kWarps * 256];  // rows of at most 512 bytes: <= 256 floats
-  float a[V], dacc[V];
-  att_slice<T>(A.att, L, 1.f, a);
-  zero<V>(dacc);
+  float* dslot = buf + wid * row_f;
+  zero_da<V>(L, dslot);
   if (t < A.csr.n_hubs && L.g == 0 && L.ok[0]) {
     const int4 hb = A.csr.hubs[t];
     DstSums<T> tot;
@@ -632,9 +636,9 @@ __global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
       }
     }
     const float lse2 = A.lse_in[int64_t(hb.x) * H + L.k[0]] * kLog2e;
-    dst_finish<T>(A, L, hb.x, tot, lse2, a, dacc);
+    dst_finish<T>(A, L, hb.x, tot, lse2, dslot);
   }
-  fold_da<V>(A, L, wid, dacc, buf, A.da_main_rows + blockIdx.x);
+  fold_da(A, row_f, buf, A.da_main_rows + blockIdx.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -669,31 +673,26 @@ __device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, con
     float red[2 * U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float r[V], g[V];
+      float r[V], gd[V], g[V], lz[V];
       unpack<T>(rr[u], r);
-      unpack<T>(rg[u], g);
-      float p = 0.f, d = 0.f;
-#pragma unroll
-      for (int c = 0; c < V; ++c) {
-        p = fmaf(a2[c], leaky(r[c] + xl[c], A.slope), p);
-        d = fmaf(g[c], xl[c], d);
-      }
-      red[u] = p;
-      red[U + u] = d;
+      unpack<T>(rg[u], gd);
+      leaky_terms<V>(r, xl, A.slope, g, lz);
+      red[u] = dot<V>(lz, a2);
+      red[U + u] = dot<V>(gd, xl);
     }
     head_sums<2 * U>(red, A.s.hv_log2);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const float al = i[u] >= 0 ? ex2(red[u] - st[u].x) : 0.f;
       const float de = al * (red[U + u] - st[u].y);
-      float r[V], g[V];
+      float r[V], gd[V], g[V], lz[V], dg[V];
       unpack_alt<T>(rr[u], r);
-      unpack_alt<T>(rg[u], g);
+      unpack_alt<T>(rg[u], gd);
+      leaky_terms<V>(r, xl, A.slope, g, lz);
 #pragma unroll
-      for (int c = 0; c < V; ++c) {
-        const float gz = leaky_g(r[c] + xl[c], A.slope);
-        acc[c] = fmaf(al, g[c], fmaf(de * a[c], gz, acc[c]));
-      }
+      for (int c = 0; c < V; c += 2) mul2v(dg[c], dg[c + 1], a[c], a[c + 1], g[c], g[c + 1]);
+      axpy<V>(acc, de, dg);
+      axpy<V>(acc, al, gd);
     }
   }
 }
@@ -878,7 +877,7 @@ cudaError_t bwd_t(V2Args A, int sm_count, cudaStream_t st) {
   // pass 1: a fixed grid (static work assignment), one da_part row per block
   {
     const V2Dir& D = A.csr;
-    const size_t smem = size_t(D.col_off) + size_t(kWarps) * (A.s.H + 4 * row_f) * 4;
+    const size_t smem = size_t(D.col_off) + size_t(kWarps) * (A.s.H + 5 * row_f) * 4;
     if ((e = set_smem(v2_dst_main<T>, smem)) != cudaSuccess) return e;
     int64_t blocks = persistent_blocks(v2_dst_main<T>, smem, sm_count);
     const int64_t cap = int64_t(sm_count > 0 ? sm_count : 1) * 8;
