@@ -157,6 +157,21 @@ __device__ __forceinline__ void mul2(float& d0, float& d1, float s) {
   upk(d, d0, d1);
 }
 
+// (d0, d1) = (a0, a1) + (b0, b1)
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0,
+                                     float b1) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a0, a1)), "l"(pk(b0, b1)));
+  upk(d, d0, d1);
+}
+// (d0, d1) = (a0, a1) * (b0, b1)
+__device__ __forceinline__ void mul2v(float& d0, float& d1, float a0, float a1, float b0,
+                                      float b1) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a0, a1)), "l"(pk(b0, b1)));
+  upk(d, d0, d1);
+}
+
 // x . w over V elements (two interleaved partial sums, added at the end).
 template <int V>
 __device__ __forceinline__ float dot(const float (&x)[V], const float (&w)[V]) {
