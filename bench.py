@@ -268,6 +268,25 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def max_over_ranks(values, world, device):
+    """Each value's maximum over the ranks (a job is as slow as its slowest
+    replica); the identity on one rank."""
+    values = [float(v) for v in values]
+    if world <= 1:
+        return values
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job throughput in G units/s: every rank processed units_per_rank
+    in at most ms milliseconds."""
+    return world * units_per_rank / (ms * 1e-3) / 1e9
+
+
 def run_gnnagg(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -377,14 +396,10 @@ def run_gnnagg(args, rank, world):
     t_fwd /= K
     t_bwd /= K
     kern = {k: v / K for k, v in kern.items()}
-    ms_step = t_fwd + t_bwd
-    if world > 1:
-        tt = torch.tensor([ms_step, t_fwd], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step, t_fwd = float(tt[0]), float(tt[1])
+    ms_step, t_fwd = max_over_ranks([t_fwd + t_bwd, t_fwd], world, dev)
     units = e * H
-    value = world * units / (ms_step * 1e-3) / 1e9
-    fwd_value = world * units / (t_fwd * 1e-3) / 1e9
+    value = job_rate(units, world, ms_step)
+    fwd_value = job_rate(units, world, t_fwd)
 
     # roofline of the dominant kernel
     ab = algorithmic_bytes(n, e, H, D, s)
@@ -507,12 +522,8 @@ def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev,
         one(k)
     e1.record(s_out)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / K
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt[0])
-    return {"value": world * units / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+    (ms,) = max_over_ranks([e0.elapsed_time(e1) / K], world, dev)
+    return {"value": job_rate(units, world, ms), "unit": UNIT, "ms_per_step": ms,
             "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "pipeline": "H2D, compute and D2H on three streams, two device buffer sets"}
 
@@ -651,11 +662,12 @@ def run_layer(args, rank, world):
     gnn.check_device_error(g)
     t_f = sum(a.elapsed_time(b) for a, b, _ in ev) / K
     t_b = sum(b.elapsed_time(c) for _, b, c in ev) / K
+    t_f, t_b = max_over_ranks([t_f, t_b], world, dev)
     peak, peak_kind = peaks()
     line = {"metric": metric, "op": args.op,
-            "value": world * units / ((t_f + t_b) * 1e-3) / 1e9,
+            "value": job_rate(units, world, t_f + t_b),
             "unit": "GEdge*head/s" if args.op in ("gatv2", "transformer") else "GEdge/s",
-            "fwd_value": world * units / (t_f * 1e-3) / 1e9, "n_gpus": world,
+            "fwd_value": job_rate(units, world, t_f), "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": t_f + t_b, "fwd_ms": t_f,
             "bwd_ms": t_b, "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "n_nodes": n, "n_edges": e, "F": F,
