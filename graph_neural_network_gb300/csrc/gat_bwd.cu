@@ -93,18 +93,22 @@ __device__ __forceinline__ float subgroup_sum(float x, const Shape& s) {
 // pass 1: destination side (CSR)
 // ---------------------------------------------------------------------------
 
-template <typename T, int NV>
+// Edges beg + sg, beg + sg + SG, ... < end, until end (kFixed false) or in
+// exactly `trips` batches (kFixed true; the same count on every lane of the
+// warp, batches past end add nothing).
+template <typename T, int NV, bool kFixed>
 __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
-                                          int (&jn)[kUnroll],
+                                          int sg, int SG, int trips, int (&jn)[kUnroll],
                                           const float (&gi)[NV][VecOf<T>::n],
                                           const float (&sd2)[NV], const float (&lse2)[NV],
                                           float (&SA)[NV], float (&SB)[NV], float (&SD)[NV]) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
-  const int step = L.G * U;
+  const int step = SG * U;
   const int H = A.s.H;
-  for (int base = beg; base < end; base += step) {
+  int base = beg;
+  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
@@ -118,7 +122,8 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
         raw[u][v] = ok ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v]) : make_uint4(0, 0, 0, 0);
         ss[u * NV + v] = ok ? __ldg(A.ssrc + int64_t(j[u]) * H + L.k[v]) : 0.f;
       }
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+    if (kFixed ? t + 1 < trips : base + step < end)
+      batch_ids<U>(cols, colbase, base + step, end, sg, SG, jn);
     float dd[U * NV];  // dout_i . h_j per head
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -145,14 +150,16 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
   }
 }
 
-// Destination-side sums of node i over its edges [beg, end) taken by this
-// warp (jn: sources of the first batch), summed over the warp's sub-groups.
+// Destination-side sums of node i over its edges [beg, end).  split: the
+// edges are spread over the warp's sub-groups (beg + g, beg + g + G, ...)
+// and the sums added over them; otherwise this lane's sub-group takes them
+// all in `trips` batches.  jn: sources of the first batch.
 template <typename T, int NV>
 __device__ __forceinline__ void dst_node(const BwdArgs& A, const Lane<NV>& L, int i,
                                          const int32_t* cols, int colbase, int beg, int end,
-                                         int (&jn)[kUnroll], float (&sd2)[NV],
-                                         float (&lse2)[NV], float (&SA)[NV], float (&SB)[NV],
-                                         float (&SD)[NV]) {
+                                         bool split, int trips, int (&jn)[kUnroll],
+                                         float (&sd2)[NV], float (&lse2)[NV], float (&SA)[NV],
+                                         float (&SB)[NV], float (&SD)[NV]) {
   constexpr int V = VecOf<T>::n;
   float gi[NV][V];
   load_row<T, NV>(A.dout, i, A.s, L, gi);
@@ -162,16 +169,24 @@ __device__ __forceinline__ void dst_node(const BwdArgs& A, const Lane<NV>& L, in
     lse2[v] = L.ok[v] ? A.lse[int64_t(i) * A.s.H + L.k[v]] * kLog2e : 0.f;
     SA[v] = SB[v] = SD[v] = 0.f;
   }
-  dst_edges<T, NV>(A, L, cols, colbase, beg, end, jn, gi, sd2, lse2, SA, SB, SD);
+  if (split) {
+    dst_edges<T, NV, false>(A, L, cols, colbase, beg, end, L.g, L.G, 0, jn, gi, sd2, lse2, SA,
+                            SB, SD);
 #pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    SA[v] = subgroup_sum(SA[v], A.s);
-    SB[v] = subgroup_sum(SB[v], A.s);
-    SD[v] = subgroup_sum(SD[v], A.s);
+    for (int v = 0; v < NV; ++v) {
+      SA[v] = subgroup_sum(SA[v], A.s);
+      SB[v] = subgroup_sum(SB[v], A.s);
+      SD[v] = subgroup_sum(SD[v], A.s);
+    }
+  } else {
+    dst_edges<T, NV, true>(A, L, cols, colbase, beg, end, 0, 1, trips, jn, gi, sd2, lse2, SA, SB,
+                           SD);
   }
 }
 
-template <typename T, int NV>
+// kSub: light nodes take one sub-group each (rows narrower than a warp);
+// otherwise one warp each.
+template <typename T, int NV, bool kSub>
 __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_main(const BwdArgs A) {
   constexpr int V = VecOf<T>::n;
   const DirArgs& D = A.csr;
@@ -200,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_ma
       const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
       int jn[kUnroll];
       batch_ids<kUnroll>(cols, it.y & ~3, wb, we, L.g, L.G, jn);
-      dst_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, jn, sd2, lse2, SA, SB, SD);
+      dst_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, true, 0, jn, sd2, lse2, SA, SB, SD);
       if (L.g == 0)
 #pragma unroll
         for (int v = 0; v < NV; ++v)
@@ -233,7 +248,47 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_ma
     }
   }
 
-  // ---- light nodes: one warp each ------------------------------------------
+  // ---- light nodes, rows narrower than a warp: one sub-group each --------
+  if (kSub) {
+    const int R = L.G >= 32 ? 1 : 2;  // nodes per sub-group per pull
+    const int npull = R * L.G;
+    for (;;) {
+      int t0 = 0;
+      if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, npull);
+      t0 = __shfl_sync(kFull, t0, 0);
+      if (t0 >= D.n_light) break;
+      int my_i = -1, my_b = 0, my_e = 0;
+      if (L.lane < npull && t0 + L.lane < D.n_light) {
+        my_i = D.light[t0 + L.lane];
+        my_b = D.ptr[my_i];
+        my_e = D.ptr[my_i + 1];
+      }
+      for (int r = 0; r < R; ++r) {
+        const int src = r * L.G + L.g;
+        const int i = __shfl_sync(kFull, my_i, src);
+        const int beg = __shfl_sync(kFull, my_b, src);
+        const int e0 = __shfl_sync(kFull, my_e, src);  // every lane shuffles
+        const int end = i >= 0 ? e0 : beg;
+        if (!__any_sync(kFull, i >= 0)) break;
+        int trips = (end - beg + kUnroll - 1) / kUnroll;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
+        int jn[kUnroll];
+        batch_ids<kUnroll>(D.idx, 0, beg, end, 0, 1, jn);
+        dst_node<T, NV>(A, L, i >= 0 ? i : 0, D.idx, 0, beg, end, false, trips, jn, sd2, lse2, SA,
+                        SB, SD);
+        if (i >= 0)
+#pragma unroll
+          for (int v = 0; v < NV; ++v)
+            if (L.head_leader(A.s, v))
+              A.stats[int64_t(i) * H + L.k[v]] =
+                  make_float4(sd2[v], lse2[v], SD[v], SA[v] - SD[v] * SB[v]);
+      }
+    }
+    return;
+  }
+
+  // ---- light nodes, rows of a whole warp: one warp each ---------------------
   for (;;) {
     int t0 = 0;
     if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
@@ -256,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_ma
       const int e2 = __shfl_sync(kFull, my_e, nq);
       int jn2[kUnroll];
       batch_ids<kUnroll>(D.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
-      dst_node<T, NV>(A, L, i, D.idx, 0, beg, end, jn, sd2, lse2, SA, SB, SD);
+      dst_node<T, NV>(A, L, i, D.idx, 0, beg, end, true, 0, jn, sd2, lse2, SA, SB, SD);
       if (L.g == 0)
 #pragma unroll
         for (int v = 0; v < NV; ++v)
@@ -299,18 +354,19 @@ __global__ void __launch_bounds__(kThreads) bwd_dst_merge(const BwdArgs A) {
 // pass 2: source side (CSC)
 // ---------------------------------------------------------------------------
 
-template <typename T, int NV>
+template <typename T, int NV, bool kFixed>
 __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
-                                          int (&in)[kUnroll],
+                                          int sg, int SG, int trips, int (&in)[kUnroll],
                                           const float (&xj)[NV][VecOf<T>::n],
                                           const float (&ss2)[NV], float (&acc)[NV][VecOf<T>::n],
                                           float (&SZ)[NV]) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
-  const int step = L.G * U;
+  const int step = SG * U;
   const int H = A.s.H;
-  for (int base = beg; base < end; base += step) {
+  int base = beg;
+  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int i[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) i[u] = in[u];
@@ -326,7 +382,8 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
         st[u][v] = ok ? ld16f(A.stats + int64_t(i[u]) * H + L.k[v])
                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, in);
+    if (kFixed ? t + 1 < trips : base + step < end)
+      batch_ids<U>(cols, colbase, base + step, end, sg, SG, in);
     float dd[U * NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -352,13 +409,13 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
   }
 }
 
-// Source-side sums of node j over its out-edges [beg, end) taken by this warp
-// (in: destinations of the first batch), summed over the warp's sub-groups.
+// Source-side sums of node j over its out-edges [beg, end) (in:
+// destinations of the first batch).  split / trips as for dst_node.
 template <typename T, int NV>
 __device__ __forceinline__ void src_node(const BwdArgs& A, const Lane<NV>& L, int j,
                                          const int32_t* cols, int colbase, int beg, int end,
-                                         int (&in)[kUnroll], float (&acc)[NV][VecOf<T>::n],
-                                         float (&SZ)[NV]) {
+                                         bool split, int trips, int (&in)[kUnroll],
+                                         float (&acc)[NV][VecOf<T>::n], float (&SZ)[NV]) {
   constexpr int V = VecOf<T>::n;
   float xj[NV][V], ss2[NV];
   load_row<T, NV>(A.h, j, A.s, L, xj);
@@ -369,12 +426,16 @@ __device__ __forceinline__ void src_node(const BwdArgs& A, const Lane<NV>& L, in
 #pragma unroll
     for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
   }
-  src_edges<T, NV>(A, L, cols, colbase, beg, end, in, xj, ss2, acc, SZ);
+  if (split) {
+    src_edges<T, NV, false>(A, L, cols, colbase, beg, end, L.g, L.G, 0, in, xj, ss2, acc, SZ);
 #pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    SZ[v] = subgroup_sum(SZ[v], A.s);
+    for (int v = 0; v < NV; ++v) {
+      SZ[v] = subgroup_sum(SZ[v], A.s);
 #pragma unroll
-    for (int c = 0; c < V; ++c) acc[v][c] = subgroup_sum(acc[v][c], A.s);
+      for (int c = 0; c < V; ++c) acc[v][c] = subgroup_sum(acc[v][c], A.s);
+    }
+  } else {
+    src_edges<T, NV, true>(A, L, cols, colbase, beg, end, 0, 1, trips, in, xj, ss2, acc, SZ);
   }
 }
 
@@ -400,7 +461,7 @@ __device__ __forceinline__ void write_src(const BwdArgs& A, const Lane<NV>& L, i
   }
 }
 
-template <typename T, int NV>
+template <typename T, int NV, bool kSub>
 __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(const BwdArgs A) {
   constexpr int V = VecOf<T>::n;
   const DirArgs& D = A.csc;
@@ -431,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
       const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
       int in[kUnroll];
       batch_ids<kUnroll>(cols, it.y & ~3, wb, we, L.g, L.G, in);
-      src_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, in, acc, SZ);
+      src_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, true, 0, in, acc, SZ);
       if (L.g == 0)
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
@@ -474,7 +535,41 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
     }
   }
 
-  // ---- light nodes: one warp each ------------------------------------------
+  // ---- light nodes, rows narrower than a warp: one sub-group each --------
+  if (kSub) {
+    const int R = L.G >= 32 ? 1 : 2;
+    const int npull = R * L.G;
+    for (;;) {
+      int t0 = 0;
+      if (L.lane == 0) t0 = atomicAdd(A.ctr + 3, npull);
+      t0 = __shfl_sync(kFull, t0, 0);
+      if (t0 >= D.n_light) break;
+      int my_j = -1, my_b = 0, my_e = 0;
+      if (L.lane < npull && t0 + L.lane < D.n_light) {
+        my_j = D.light[t0 + L.lane];
+        my_b = D.ptr[my_j];
+        my_e = D.ptr[my_j + 1];
+      }
+      for (int r = 0; r < R; ++r) {
+        const int src = r * L.G + L.g;
+        const int j = __shfl_sync(kFull, my_j, src);
+        const int beg = __shfl_sync(kFull, my_b, src);
+        const int e0 = __shfl_sync(kFull, my_e, src);  // every lane shuffles
+        const int end = j >= 0 ? e0 : beg;
+        if (!__any_sync(kFull, j >= 0)) break;
+        int trips = (end - beg + kUnroll - 1) / kUnroll;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
+        int in[kUnroll];
+        batch_ids<kUnroll>(D.idx, 0, beg, end, 0, 1, in);
+        src_node<T, NV>(A, L, j >= 0 ? j : 0, D.idx, 0, beg, end, false, trips, in, acc, SZ);
+        if (j >= 0) write_src<T, NV>(A, L, j, acc, SZ);
+      }
+    }
+    return;
+  }
+
+  // ---- light nodes, rows of a whole warp: one warp each ---------------------
   for (;;) {
     int t0 = 0;
     if (L.lane == 0) t0 = atomicAdd(A.ctr + 3, kGrab);
@@ -497,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
       const int e2 = __shfl_sync(kFull, my_e, nq);
       int in2[kUnroll];
       batch_ids<kUnroll>(D.idx, 0, b2, j2 >= 0 ? e2 : b2, L.g, L.G, in2);
-      src_node<T, NV>(A, L, j, D.idx, 0, beg, end, in, acc, SZ);
+      src_node<T, NV>(A, L, j, D.idx, 0, beg, end, true, 0, in, acc, SZ);
       if (L.g == 0) write_src<T, NV>(A, L, j, acc, SZ);
       j = j2;
       beg = b2;
@@ -649,6 +744,9 @@ cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t 
     if (ev) cudaEventRecord(ev[k], st);
   };
   if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), st)) != cudaSuccess) return e;
+  // rows narrower than a warp: light nodes one sub-group each (only NV = 1:
+  // rows of more than 512 bytes always fill the warp)
+  const bool sub = NV == 1 && A.s.lpr < 32;
   mark(0);
   if ((e = launch_node_scores(A.s, dt, A.h, A.a_src, A.a_dst, A.n, const_cast<float*>(A.ssrc),
                               const_cast<float*>(A.sdst), sm_count, st)) != cudaSuccess)
@@ -659,10 +757,11 @@ cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t 
     const int64_t work = A.csr.n_items + (A.csr.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
     const size_t smem = size_t(A.csr.col_off) + size_t(kWarps) * H * 3 * 4;
     if (work > 0) {
-      if ((e = set_smem(bwd_dst_main<T, NV>, smem)) != cudaSuccess) return e;
-      const int64_t cap = persistent_blocks(bwd_dst_main<T, NV>, smem, sm_count);
+      auto kernel = sub ? bwd_dst_main<T, NV, NV == 1> : bwd_dst_main<T, NV, false>;
+      if ((e = set_smem(kernel, smem)) != cudaSuccess) return e;
+      const int64_t cap = persistent_blocks(kernel, smem, sm_count);
       const int64_t blocks = work < cap ? work : cap;
-      bwd_dst_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
+      kernel<<<unsigned(blocks), kThreads, smem, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     mark(2);
@@ -677,10 +776,11 @@ cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t 
     const int64_t work = A.csc.n_items + (A.csc.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
     const size_t smem = size_t(A.csc.col_off) + size_t(kWarps) * (H + row_f) * 4;
     if (work > 0) {
-      if ((e = set_smem(bwd_src_main<T, NV>, smem)) != cudaSuccess) return e;
-      const int64_t cap = persistent_blocks(bwd_src_main<T, NV>, smem, sm_count);
+      auto kernel = sub ? bwd_src_main<T, NV, NV == 1> : bwd_src_main<T, NV, false>;
+      if ((e = set_smem(kernel, smem)) != cudaSuccess) return e;
+      const int64_t cap = persistent_blocks(kernel, smem, sm_count);
       const int64_t blocks = work < cap ? work : cap;
-      bwd_src_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
+      kernel<<<unsigned(blocks), kThreads, smem, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     mark(4);

@@ -110,19 +110,24 @@ __device__ __forceinline__ void batch_sources(const int32_t* cols, int colbase, 
   }
 }
 
-// Stream the edges beg + g, beg + g + G, ... < end through the online
-// softmax.  cols[x - colbase] is the source of edge x; jn holds the sources
-// of the first batch (already loaded).
-template <typename T, int NV>
+// Stream the edges beg + sg, beg + sg + SG, ... < end through the online
+// softmax, kUnroll edges per lane and batch: until end (kFixed false; every
+// lane of the warp then has the same beg and end), or for exactly `trips`
+// batches (kFixed true; the same count on every lane, batches past end
+// change nothing).
+// cols[x - colbase] is the source of edge x; jn holds the sources of the
+// first batch (already loaded).
+template <typename T, int NV, bool kFixed>
 __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
-                                          int (&jn)[kUnroll], const float (&sd2)[NV],
-                                          Online<T, NV>& st) {
+                                          int sg, int SG, int trips, int (&jn)[kUnroll],
+                                          const float (&sd2)[NV], Online<T, NV>& st) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
-  const int step = L.G * U;
+  const int step = SG * U;
   const int H = A.s.H;
-  for (int base = beg; base < end; base += step) {
+  int base = beg;
+  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
@@ -136,7 +141,8 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
         raw[u][v] = ok ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v]) : make_uint4(0, 0, 0, 0);
         sc[u * NV + v] = ok ? __ldg(A.ssrc + int64_t(j[u]) * H + L.k[v]) : 0.f;
       }
-    if (base + step < end) batch_sources<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+    if (kFixed ? t + 1 < trips : base + step < end)
+      batch_sources<U>(cols, colbase, base + step, end, sg, SG, jn);
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
@@ -166,6 +172,16 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
       st.m[v] = mn;
     }
   }
+}
+
+// The edges beg + g, beg + g + G, ... < end of one node, spread over the
+// warp's sub-groups (every lane sees the same beg and end).
+template <typename T, int NV>
+__device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
+                                          const int32_t* cols, int colbase, int beg, int end,
+                                          int (&jn)[kUnroll], const float (&sd2)[NV],
+                                          Online<T, NV>& st) {
+  fwd_edges<T, NV, false>(A, L, cols, colbase, beg, end, L.g, L.G, 0, jn, sd2, st);
 }
 
 // This lane's base-2 destination score halves of node i.
@@ -275,7 +291,10 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, in
   return true;
 }
 
-template <typename T, int NV>
+// kSub: light nodes take one sub-group each (rows narrower than a warp);
+// otherwise one warp each.  Two instantiations keep each loop's register
+// allocation its own.
+template <typename T, int NV, bool kSub>
 __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) fwd_main(const FwdArgs A) {
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
@@ -295,7 +314,47 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) fwd_main(c
     }
   }
 
-  // ---- light nodes: one warp each, pulled kGrab at a time ----------------
+  // ---- light nodes, rows narrower than a warp: one sub-group each --------
+  // (a node's edges stay in one sub-group, so no cross-sub-group merge; the
+  // sub-groups of a warp run as many batches as the longest of their nodes)
+  if (kSub) {
+    const int R = L.G >= 32 ? 1 : 2;  // nodes per sub-group per pull
+    const int npull = R * L.G;        // <= 32
+    for (;;) {
+      int t0 = 0;
+      if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, npull);
+      t0 = __shfl_sync(kFull, t0, 0);
+      if (t0 >= A.n_light) break;
+      int my_i = -1, my_b = 0, my_e = 0;
+      if (L.lane < npull && t0 + L.lane < A.n_light) {
+        my_i = A.light[t0 + L.lane];
+        my_b = A.ptr[my_i];
+        my_e = A.ptr[my_i + 1];
+      }
+      for (int r = 0; r < R; ++r) {
+        const int src = r * L.G + L.g;
+        const int i = __shfl_sync(kFull, my_i, src);
+        const int beg = __shfl_sync(kFull, my_b, src);
+        const int e0 = __shfl_sync(kFull, my_e, src);  // every lane shuffles
+        const int end = i >= 0 ? e0 : beg;
+        if (!__any_sync(kFull, i >= 0)) break;
+        int trips = (end - beg + kUnroll - 1) / kUnroll;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
+        int jn[kUnroll];
+        batch_sources<kUnroll>(A.idx, 0, beg, end, 0, 1, jn);
+        float sd2[NV];
+        node_sdst<NV>(A, L, i >= 0 ? i : 0, sd2);
+        Online<T, NV> st;
+        st.init();
+        fwd_edges<T, NV, true>(A, L, A.idx, 0, beg, end, 0, 1, trips, jn, sd2, st);
+        if (i >= 0) write_node<T, NV>(A, L, i, st);
+      }
+    }
+    return;
+  }
+
+  // ---- light nodes, rows of a whole warp: one warp each, kGrab per pull ---
   for (;;) {
     int t0 = 0;
     if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
@@ -381,14 +440,16 @@ cudaError_t launch_t(const FwdArgs& A, gnn_dtype dt, const float* a_src, const f
   if (ev) cudaEventRecord(ev[1], stream);
   if (A.n_items + A.n_light > 0) {
     const size_t smem = size_t(A.col_off) + size_t(kWarps) * (2 * A.s.H + A.s.rv * V) * 4;
+    // rows of more than 512 bytes always fill the warp (NV > 1)
+    auto kernel = (NV == 1 && A.s.lpr < 32) ? fwd_main<T, NV, NV == 1> : fwd_main<T, NV, false>;
     if (smem > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(fwd_main<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(smem))) != cudaSuccess)
       return e;
     const int64_t work = A.n_items + (A.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
-    const int64_t cap = persistent_blocks(fwd_main<T, NV>, smem, sm_count);
+    const int64_t cap = persistent_blocks(kernel, smem, sm_count);
     const int64_t blocks = work < cap ? work : cap;
-    fwd_main<T, NV><<<unsigned(blocks), kThreads, smem, stream>>>(A);
+    kernel<<<unsigned(blocks), kThreads, smem, stream>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (ev) cudaEventRecord(ev[2], stream);
