@@ -455,9 +455,10 @@ def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev,
     """Same metric through the public API with host buffers: every step copies
     the step's inputs from pinned host memory and reads every result back.
     Steps are pipelined the way a training loop with a prefetching loader
-    runs: inputs go up on one copy stream, results come back on another and
-    the kernels run on the compute stream, with two sets of device buffers
-    so that step k + 1's upload and step k - 1's download overlap step k."""
+    runs: inputs go up on two copy streams, results come back on two others
+    and the kernels run on the compute stream, with two sets of device
+    buffers so that step k + 1's upload and step k - 1's download overlap
+    step k."""
     import torch
     import torch.distributed as dist
     import graph_neural_network_gb300 as gnn
@@ -473,41 +474,49 @@ def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev,
     h2d = sum(t.numel() * t.element_size() for t in (h_host, d_host, as_host, ad_host))
     d2h = sum(t.numel() * t.element_size() for t in (o_host, l_host, dh_host, das_host, dad_host))
     comp = torch.cuda.current_stream(dev)
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    # two upload and two download streams, so that both copies of a direction
+    # can use separate copy engines
+    s_h, s_d = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_o, s_g = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     names = ("h", "dout", "a_s", "a_d", "out", "lse", "dh", "da_s", "da_d")
     first = (h, dout, a_s, a_d, out, lse, dh, da_s, da_d)
     bufs = [dict(zip(names, first)), {n: torch.empty_like(t) for n, t in zip(names, first)}]
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    comp_done = [torch.cuda.Event() for _ in range(2)]
-    out_done = [torch.cuda.Event() for _ in range(2)]
-    for ev in comp_done + out_done:
-        ev.record(comp)
+    ev = lambda: [torch.cuda.Event() for _ in range(2)]
+    h_ready, d_ready, fwd_done, comp_done, o_done, g_done = ev(), ev(), ev(), ev(), ev(), ev()
+    for e in comp_done + o_done + g_done:
+        e.record(comp)
 
     def one(k):
         i = k % 2
         b = bufs[i]
-        s_in.wait_event(comp_done[i])          # step k - 2 no longer reads these inputs
-        with torch.cuda.stream(s_in):
-            b["h"].copy_(h_host, non_blocking=True)
-            b["dout"].copy_(d_host, non_blocking=True)
-            b["a_s"].copy_(as_host, non_blocking=True)
-            b["a_d"].copy_(ad_host, non_blocking=True)
-        in_ready[i].record(s_in)
-        comp.wait_event(in_ready[i])
-        comp.wait_event(out_done[i])           # step k - 2's results have left these buffers
+        for st, ready, copies in ((s_h, h_ready, (("h", h_host), ("a_s", as_host),
+                                                   ("a_d", ad_host))),
+                                  (s_d, d_ready, (("dout", d_host),))):
+            st.wait_event(comp_done[i])        # step k - 2 no longer reads these inputs
+            with torch.cuda.stream(st):
+                for name, src in copies:
+                    b[name].copy_(src, non_blocking=True)
+                ready[i].record(st)
+        comp.wait_event(h_ready[i])
+        comp.wait_event(o_done[i])             # step k - 2's results have left these buffers
+        comp.wait_event(g_done[i])
         gnn.gat_forward(g, b["h"], b["a_s"], b["a_d"], w.slope, out=b["out"], lse=b["lse"],
                         ws=ws, stream=comp)
+        fwd_done[i].record(comp)
+        comp.wait_event(d_ready[i])            # dout arrived while the forward ran
         gnn.gat_backward(g, b["h"], b["a_s"], b["a_d"], w.slope, b["lse"], b["dout"],
                          dh=b["dh"], da_src=b["da_s"], da_dst=b["da_d"], ws=ws, stream=comp)
         comp_done[i].record(comp)
-        s_out.wait_event(comp_done[i])
-        with torch.cuda.stream(s_out):
-            o_host.copy_(b["out"], non_blocking=True)
-            l_host.copy_(b["lse"], non_blocking=True)
-            dh_host.copy_(b["dh"], non_blocking=True)
-            das_host.copy_(b["da_s"], non_blocking=True)
-            dad_host.copy_(b["da_d"], non_blocking=True)
-        out_done[i].record(s_out)
+        for st, after, done, copies in ((s_o, fwd_done, o_done, ((o_host, "out"),
+                                                                   (l_host, "lse"))),
+                                        (s_g, comp_done, g_done, ((dh_host, "dh"),
+                                                                   (das_host, "da_s"),
+                                                                   (dad_host, "da_d")))):
+            st.wait_event(after[i])            # out and lse leave while the backward runs
+            with torch.cuda.stream(st):
+                for dst, name in copies:
+                    dst.copy_(b[name], non_blocking=True)
+                done[i].record(st)
 
     for k in range(4):
         one(k)
@@ -517,15 +526,19 @@ def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev,
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
+    e0.record(s_h)
+    s_d.wait_event(e0)
     for k in range(K):
         one(k)
-    e1.record(s_out)
+    s_g.wait_event(o_done[(K - 1) % 2])
+    e1.record(s_g)
     torch.cuda.synchronize()
     (ms,) = max_over_ranks([e0.elapsed_time(e1) / K], world, dev)
     return {"value": job_rate(units, world, ms), "unit": UNIT, "ms_per_step": ms,
             "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipeline": "H2D, compute and D2H on three streams, two device buffer sets"}
+            "pipeline": "two upload, one compute and two download streams, two device buffer "
+                        "sets; dout uploads during the forward, out and lse download during "
+                        "the backward"}
 
 
 def run_layer(args, rank, world):
