@@ -237,7 +237,7 @@ __device__ __forceinline__ void fwd_write(const V2Args& A, const Lane<1>& L, int
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 2) v2_fwd_main(const V2Args A) {
+__global__ void __launch_bounds__(kThreads, 3) v2_fwd_main(const V2Args A) {
   constexpr int V = VecOf<T>::n;
   const V2Dir& D = A.csr;
   const Lane<1> L(A.s);

@@ -220,7 +220,7 @@ __device__ __forceinline__ void query(const GtArgs& A, const Lane<1>& L, int64_t
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 2) gt_fwd_main(const GtArgs A) {
+__global__ void __launch_bounds__(kThreads, 3) gt_fwd_main(const GtArgs A) {
   constexpr int V = VecOf<T>::n;
   const GtDir& D = A.csr;
   const Lane<1> L(A.s);
