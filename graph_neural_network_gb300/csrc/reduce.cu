@@ -168,7 +168,7 @@ __device__ __forceinline__ void write_best(const RedArgs& A, const Lane<NV>& L, 
 }
 
 template <typename T, int NV>
-__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) red_fwd_main(const RedArgs A) {
+__global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_main(const RedArgs A) {
   constexpr int V = VecOf<T>::n;
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;

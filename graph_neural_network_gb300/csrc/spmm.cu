@@ -134,7 +134,7 @@ __device__ __forceinline__ void write_row(const SpmmArgs& A, const Lane<NV>& L, 
 }
 
 template <typename T, int NV>
-__global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) spmm_main(const SpmmArgs A) {
+__global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(const SpmmArgs A) {
   constexpr int V = VecOf<T>::n;
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
