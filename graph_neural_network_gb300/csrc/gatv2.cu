@@ -78,7 +78,6 @@ struct V2Args {
   int32_t* err;
 };
 
-__device__ __forceinline__ float leaky(float z, float s) { return z > 0.f ? z : s * z; }
 __device__ __forceinline__ float leaky_g(float z, float s) { return z > 0.f ? 1.f : s; }
 
 // For z = r + x elementwise: g = LeakyReLU'(z) and lz = LeakyReLU(z) = g z,
@@ -174,15 +173,17 @@ struct V2Online {
   }
 };
 
-template <typename T>
+template <typename T, bool kFixed>
 __device__ __forceinline__ void fwd_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int (&jn)[kUnroll],
+                                          int colbase, int beg, int end, int sg, int SG,
+                                          int trips, int (&jn)[kUnroll],
                                           const float (&xr)[VecOf<T>::n],
                                           const float (&a2)[VecOf<T>::n], V2Online<T>& st) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
-  const int step = L.G * U;
-  for (int base = beg; base < end; base += step) {
+  const int step = SG * U;
+  int base = beg;
+  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
@@ -191,7 +192,8 @@ __device__ __forceinline__ void fwd_edges(const V2Args& A, const Lane<1>& L, con
     for (int u = 0; u < U; ++u)
       raw[u] = (j[u] >= 0 && L.ok[0]) ? ld16(row_base<T>(A.xl, j[u], A.s.rv) + 16 * L.q[0])
                                       : make_uint4(0, 0, 0, 0);
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+    if (kFixed ? t + 1 < trips : base + step < end)
+      batch_ids<U>(cols, colbase, base + step, end, sg, SG, jn);
     float sc[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -239,7 +241,8 @@ __device__ __forceinline__ void fwd_write(const V2Args& A, const Lane<1>& L, int
     A.lse[node * A.s.H + L.k[0]] = st.l > 0.f ? (st.m + __log2f(st.l)) * kLn2 : -INFINITY;
 }
 
-template <typename T>
+// kSub: light nodes take one sub-group each (rows narrower than a warp).
+template <typename T, bool kSub>
 __global__ void __launch_bounds__(kThreads, 3) v2_fwd_main(const V2Args A) {
   constexpr int V = VecOf<T>::n;
   const V2Dir& D = A.csr;
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_fwd_main(const V2Args A) {
       own_row<T>(A.xr, it.x, A.s, L, xr);
       V2Online<T> st;
       st.init();
-      fwd_edges<T>(A, L, cols, colbase, wb, we, jn, xr, a2, st);
+      fwd_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, 0, jn, xr, a2, st);
       st.merge_subgroups(A.s);
       if (L.g == 0 && L.ok[0]) {
 #pragma unroll
@@ -313,6 +316,44 @@ __global__ void __launch_bounds__(kThreads, 3) v2_fwd_main(const V2Args A) {
     }
   }
 
+  // ---- light nodes, rows narrower than a warp: one sub-group each --------
+  if (kSub) {
+    const int R = L.G >= 32 ? 1 : 2;  // nodes per sub-group per pull
+    const int npull = R * L.G;
+    for (;;) {
+      int t0 = 0;
+      if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, npull);
+      t0 = __shfl_sync(kFull, t0, 0);
+      if (t0 >= D.n_light) break;
+      int my_n = -1, my_b = 0, my_e = 0;
+      if (L.lane < npull && t0 + L.lane < D.n_light) {
+        my_n = D.light[t0 + L.lane];
+        my_b = D.ptr[my_n];
+        my_e = D.ptr[my_n + 1];
+      }
+      for (int r = 0; r < R; ++r) {
+        const int src = r * L.G + L.g;
+        const int i = __shfl_sync(kFull, my_n, src);
+        const int beg = __shfl_sync(kFull, my_b, src);
+        const int e0 = __shfl_sync(kFull, my_e, src);  // every lane shuffles
+        const int end = i >= 0 ? e0 : beg;
+        if (!__any_sync(kFull, i >= 0)) break;
+        int trips = (end - beg + kUnroll - 1) / kUnroll;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
+        int jn[kUnroll];
+        batch_ids<kUnroll>(D.idx, 0, beg, end, 0, 1, jn);
+        own_row<T>(A.xr, i >= 0 ? i : 0, A.s, L, xr);
+        V2Online<T> st;
+        st.init();
+        fwd_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, trips, jn, xr, a2, st);
+        if (i >= 0) fwd_write<T>(A, L, i, st);
+      }
+    }
+    return;
+  }
+
+  // ---- light nodes, rows of a whole warp: one warp each -----------------
   for (;;) {
     int t0 = 0;
     if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
@@ -338,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_fwd_main(const V2Args A) {
       own_row<T>(A.xr, i, A.s, L, xr);
       V2Online<T> st;
       st.init();
-      fwd_edges<T>(A, L, D.idx, 0, beg, end, jn, xr, a2, st);
+      fwd_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, 0, jn, xr, a2, st);
       st.merge_subgroups(A.s);
       if (L.g == 0) fwd_write<T>(A, L, i, st);
       i = i2;
@@ -648,18 +689,20 @@ __global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
 // backward pass 2: source side
 // ---------------------------------------------------------------------------
 
-template <typename T>
+template <typename T, bool kFixed>
 __device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int (&in)[kUB],
+                                          int colbase, int beg, int end, int sg, int SG,
+                                          int trips, int (&in)[kUB],
                                           const float (&xl)[VecOf<T>::n],
                                           const float (&a2)[VecOf<T>::n],
                                           const float (&a)[VecOf<T>::n],
                                           float (&acc)[VecOf<T>::n]) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUB;
-  const int step = L.G * U;
+  const int step = SG * U;
   const int H = A.s.H;
-  for (int base = beg; base < end; base += step) {
+  int base = beg;
+  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int i[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) i[u] = in[u];
@@ -672,7 +715,8 @@ __device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, con
       rg[u] = ok ? ld16(row_base<T>(A.dout, i[u], A.s.rv) + 16 * L.q[0]) : make_uint4(0, 0, 0, 0);
       st[u] = ok ? __ldg(A.stats + int64_t(i[u]) * H + L.k[0]) : make_float2(0.f, 0.f);
     }
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, in);
+    if (kFixed ? t + 1 < trips : base + step < end)
+      batch_ids<U>(cols, colbase, base + step, end, sg, SG, in);
     float red[2 * U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -740,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
       batch_ids<kUB>(cols, colbase, wb, we, L.g, L.G, in);
       own_row<T>(A.xl, it.x, A.s, L, xl);
       zero<V>(acc);
-      src_edges<T>(A, L, cols, colbase, wb, we, in, xl, a2, a, acc);
+      src_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, 0, in, xl, a2, a, acc);
       subgroup_sums<V>(acc, A.s);
       if (L.g == 0 && L.ok[0])
 #pragma unroll
@@ -767,6 +811,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
     }
   }
 
+  // ---- light nodes, rows of a whole warp: one warp each -----------------
   for (;;) {
     int t0 = 0;
     if (L.lane == 0) t0 = atomicAdd(A.ctr + 3, kGrab);
@@ -791,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
       batch_ids<kUB>(D.idx, 0, b2, j2 >= 0 ? e2 : b2, L.g, L.G, in2);
       own_row<T>(A.xl, j, A.s, L, xl);
       zero<V>(acc);
-      src_edges<T>(A, L, D.idx, 0, beg, end, in, xl, a2, a, acc);
+      src_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, 0, in, xl, a2, a, acc);
       subgroup_sums<V>(acc, A.s);
       if (L.g == 0) src_write<T>(A, L, j, acc);
       j = j2;
@@ -858,10 +903,11 @@ cudaError_t fwd_t(const V2Args& A, int sm_count, cudaStream_t st) {
   const V2Dir& D = A.csr;
   if (D.n_items + D.n_light > 0) {
     const size_t smem = size_t(D.col_off) + size_t(kWarps) * (2 * A.s.H + row_f) * 4;
-    if ((e = set_smem(v2_fwd_main<T>, smem)) != cudaSuccess) return e;
+    auto kernel = A.s.lpr < 32 ? v2_fwd_main<T, true> : v2_fwd_main<T, false>;
+    if ((e = set_smem(kernel, smem)) != cudaSuccess) return e;
     const int64_t work = D.n_items + (D.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
-    const int64_t cap = persistent_blocks(v2_fwd_main<T>, smem, sm_count);
-    v2_fwd_main<T><<<unsigned(work < cap ? work : cap), kThreads, smem, st>>>(A);
+    const int64_t cap = persistent_blocks(kernel, smem, sm_count);
+    kernel<<<unsigned(work < cap ? work : cap), kThreads, smem, st>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (D.n_hubs > 0) {
@@ -902,10 +948,11 @@ cudaError_t bwd_t(V2Args A, int sm_count, cudaStream_t st) {
     const V2Dir& D = A.csc;
     if (D.n_items + D.n_light > 0) {
       const size_t smem = size_t(D.col_off) + size_t(kWarps) * row_f * 4;
-      if ((e = set_smem(v2_src_main<T>, smem)) != cudaSuccess) return e;
+      auto kernel = v2_src_main<T>;
+      if ((e = set_smem(kernel, smem)) != cudaSuccess) return e;
       const int64_t work = D.n_items + (D.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
-      const int64_t cap = persistent_blocks(v2_src_main<T>, smem, sm_count);
-      v2_src_main<T><<<unsigned(work < cap ? work : cap), kThreads, smem, st>>>(A);
+      const int64_t cap = persistent_blocks(kernel, smem, sm_count);
+      kernel<<<unsigned(work < cap ? work : cap), kThreads, smem, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (D.n_hubs > 0) {

@@ -151,14 +151,16 @@ struct GtOnline {
   }
 };
 
-template <typename T>
+template <typename T, bool kFixed>
 __device__ __forceinline__ void fwd_edges(const GtArgs& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int (&jn)[kU],
+                                          int colbase, int beg, int end, int sg, int SG,
+                                          int trips, int (&jn)[kU],
                                           const float (&qs)[VecOf<T>::n], GtOnline<T>& st) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kU;
-  const int step = L.G * U;
-  for (int base = beg; base < end; base += step) {
+  const int step = SG * U;
+  int base = beg;
+  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
@@ -168,7 +170,8 @@ __device__ __forceinline__ void fwd_edges(const GtArgs& A, const Lane<1>& L, con
       rk[u] = gather<T>(A.key, j[u], A.s, L);
       rv[u] = gather<T>(A.val, j[u], A.s, L);
     }
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+    if (kFixed ? t + 1 < trips : base + step < end)
+      batch_ids<U>(cols, colbase, base + step, end, sg, SG, jn);
     float sc[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_fwd_main(const GtArgs A) {
       query<T>(A, L, it.x, qs);
       GtOnline<T> st;
       st.init();
-      fwd_edges<T>(A, L, cols, colbase, wb, we, jn, qs, st);
+      fwd_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, 0, jn, qs, st);
       st.merge_subgroups(A.s);
       if (L.g == 0 && L.ok[0]) {
 #pragma unroll
@@ -296,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_fwd_main(const GtArgs A) {
     }
   }
 
+  // ---- light nodes, rows of a whole warp: one warp each -----------------
   for (;;) {
     int t0 = 0;
     if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_fwd_main(const GtArgs A) {
       query<T>(A, L, i, qs);
       GtOnline<T> st;
       st.init();
-      fwd_edges<T>(A, L, D.idx, 0, beg, end, jn, qs, st);
+      fwd_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, 0, jn, qs, st);
       st.merge_subgroups(A.s);
       if (L.g == 0) fwd_write<T>(A, L, i, st);
       i = i2;
@@ -381,16 +385,18 @@ struct GtDst {
   }
 };
 
-template <typename T>
+template <typename T, bool kFixed>
 __device__ __forceinline__ void dst_edges(const GtArgs& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int (&jn)[kU],
+                                          int colbase, int beg, int end, int sg, int SG,
+                                          int trips, int (&jn)[kU],
                                           const float (&qs)[VecOf<T>::n],
                                           const float (&gi)[VecOf<T>::n], float lse2,
                                           GtDst<T>& sm) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kU;
-  const int step = L.G * U;
-  for (int base = beg; base < end; base += step) {
+  const int step = SG * U;
+  int base = beg;
+  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
@@ -400,7 +406,8 @@ __device__ __forceinline__ void dst_edges(const GtArgs& A, const Lane<1>& L, con
       rk[u] = gather<T>(A.key, j[u], A.s, L);
       rv[u] = gather<T>(A.val, j[u], A.s, L);
     }
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+    if (kFixed ? t + 1 < trips : base + step < end)
+      batch_ids<U>(cols, colbase, base + step, end, sg, SG, jn);
     float red[2 * U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -436,7 +443,8 @@ __device__ __forceinline__ void dst_finish(const GtArgs& A, const Lane<1>& L, in
   if (L.head_leader(A.s, 0)) A.stats[i * A.s.H + L.k[0]] = make_float2(lse2, sm.delta);
 }
 
-template <typename T>
+// kSub: light nodes take one sub-group each (rows narrower than a warp).
+template <typename T, bool kSub>
 __global__ void __launch_bounds__(kThreads, 3) gt_dst_main(const GtArgs A) {
   constexpr int V = VecOf<T>::n;
   const GtDir& D = A.csr;
@@ -471,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_dst_main(const GtArgs A) {
       const float lse2 = L.ok[0] ? A.lse_in[int64_t(it.x) * H + L.k[0]] * kLog2e : 0.f;
       GtDst<T> sm;
       sm.init();
-      dst_edges<T>(A, L, cols, colbase, wb, we, jn, qs, gi, lse2, sm);
+      dst_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, 0, jn, qs, gi, lse2, sm);
       sm.subgroup_total(A.s);
       float* mine = wbuf + wid * (H + 2 * row_f);
       if (L.g == 0 && L.ok[0]) {
@@ -511,6 +519,47 @@ __global__ void __launch_bounds__(kThreads, 3) gt_dst_main(const GtArgs A) {
     }
   }
 
+  // ---- light nodes, rows narrower than a warp: one sub-group each --------
+  if (kSub) {
+    const int R = L.G >= 32 ? 1 : 2;  // nodes per sub-group per pull
+    const int npull = R * L.G;
+    for (;;) {
+      int t0 = 0;
+      if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, npull);
+      t0 = __shfl_sync(kFull, t0, 0);
+      if (t0 >= D.n_light) break;
+      int my_n = -1, my_b = 0, my_e = 0;
+      if (L.lane < npull && t0 + L.lane < D.n_light) {
+        my_n = D.light[t0 + L.lane];
+        my_b = D.ptr[my_n];
+        my_e = D.ptr[my_n + 1];
+      }
+      for (int r = 0; r < R; ++r) {
+        const int src = r * L.G + L.g;
+        const int i = __shfl_sync(kFull, my_n, src);
+        const int beg = __shfl_sync(kFull, my_b, src);
+        const int e0 = __shfl_sync(kFull, my_e, src);  // every lane shuffles
+        const int end = i >= 0 ? e0 : beg;
+        if (!__any_sync(kFull, i >= 0)) break;
+        int trips = (end - beg + kU - 1) / kU;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
+        int jn[kU];
+        batch_ids<kU>(D.idx, 0, beg, end, 0, 1, jn);
+        const int ii = i >= 0 ? i : 0;
+        query<T>(A, L, ii, qs);
+        own_row<T>(A.dout, ii, A.s, L, gi);
+        const float lse2 = L.ok[0] ? A.lse_in[int64_t(ii) * H + L.k[0]] * kLog2e : 0.f;
+        GtDst<T> sm;
+        sm.init();
+        dst_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, trips, jn, qs, gi, lse2, sm);
+        if (i >= 0) dst_finish<T>(A, L, i, sm, lse2);
+      }
+    }
+    return;
+  }
+
+  // ---- light nodes, rows of a whole warp: one warp each -----------------
   for (;;) {
     int t0 = 0;
     if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
@@ -538,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_dst_main(const GtArgs A) {
       const float lse2 = L.ok[0] ? A.lse_in[int64_t(i) * H + L.k[0]] * kLog2e : 0.f;
       GtDst<T> sm;
       sm.init();
-      dst_edges<T>(A, L, D.idx, 0, beg, end, jn, qs, gi, lse2, sm);
+      dst_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, 0, jn, qs, gi, lse2, sm);
       sm.subgroup_total(A.s);
       if (L.g == 0) dst_finish<T>(A, L, i, sm, lse2);
       i = i2;
@@ -578,17 +627,19 @@ __global__ void __launch_bounds__(kThreads) gt_dst_merge(const GtArgs A) {
 // backward pass 2: source side
 // ---------------------------------------------------------------------------
 
-template <typename T>
+template <typename T, bool kFixed>
 __device__ __forceinline__ void src_edges(const GtArgs& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int (&in)[kU],
+                                          int colbase, int beg, int end, int sg, int SG,
+                                          int trips, int (&in)[kU],
                                           const float (&ks)[VecOf<T>::n],
                                           const float (&vj)[VecOf<T>::n],
                                           float (&dk)[VecOf<T>::n], float (&dv)[VecOf<T>::n]) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kU;
-  const int step = L.G * U;
+  const int step = SG * U;
   const int H = A.s.H;
-  for (int base = beg; base < end; base += step) {
+  int base = beg;
+  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int i[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) i[u] = in[u];
@@ -601,7 +652,8 @@ __device__ __forceinline__ void src_edges(const GtArgs& A, const Lane<1>& L, con
       st[u] = (i[u] >= 0 && L.ok[0]) ? __ldg(A.stats + int64_t(i[u]) * H + L.k[0])
                                      : make_float2(0.f, 0.f);
     }
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, in);
+    if (kFixed ? t + 1 < trips : base + step < end)
+      batch_ids<U>(cols, colbase, base + step, end, sg, SG, in);
     float red[2 * U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -635,7 +687,8 @@ __device__ __forceinline__ void src_write(const GtArgs& A, const Lane<1>& L, int
   st16(reinterpret_cast<char*>(A.dval) + off, pack<T>(dv));
 }
 
-template <typename T>
+// kSub: light nodes take one sub-group each (rows narrower than a warp).
+template <typename T, bool kSub>
 __global__ void __launch_bounds__(kThreads, 3) gt_src_main(const GtArgs A) {
   constexpr int V = VecOf<T>::n;
   const GtDir& D = A.csc;
@@ -669,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_src_main(const GtArgs A) {
       own_row<T>(A.val, it.x, A.s, L, vj);
       zero<V>(dk);
       zero<V>(dv);
-      src_edges<T>(A, L, cols, colbase, wb, we, in, ks, vj, dk, dv);
+      src_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, 0, in, ks, vj, dk, dv);
       subgroup_sums<V>(dk, A.s);
       subgroup_sums<V>(dv, A.s);
       if (L.g == 0 && L.ok[0])
@@ -705,6 +758,47 @@ __global__ void __launch_bounds__(kThreads, 3) gt_src_main(const GtArgs A) {
     }
   }
 
+  // ---- light nodes, rows narrower than a warp: one sub-group each --------
+  if (kSub) {
+    const int R = L.G >= 32 ? 1 : 2;  // nodes per sub-group per pull
+    const int npull = R * L.G;
+    for (;;) {
+      int t0 = 0;
+      if (L.lane == 0) t0 = atomicAdd(A.ctr + 3, npull);
+      t0 = __shfl_sync(kFull, t0, 0);
+      if (t0 >= D.n_light) break;
+      int my_n = -1, my_b = 0, my_e = 0;
+      if (L.lane < npull && t0 + L.lane < D.n_light) {
+        my_n = D.light[t0 + L.lane];
+        my_b = D.ptr[my_n];
+        my_e = D.ptr[my_n + 1];
+      }
+      for (int r = 0; r < R; ++r) {
+        const int src = r * L.G + L.g;
+        const int j = __shfl_sync(kFull, my_n, src);
+        const int beg = __shfl_sync(kFull, my_b, src);
+        const int e0 = __shfl_sync(kFull, my_e, src);  // every lane shuffles
+        const int end = j >= 0 ? e0 : beg;
+        if (!__any_sync(kFull, j >= 0)) break;
+        int trips = (end - beg + kU - 1) / kU;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
+        int in[kU];
+        batch_ids<kU>(D.idx, 0, beg, end, 0, 1, in);
+        const int jj = j >= 0 ? j : 0;
+        own_row<T>(A.key, jj, A.s, L, ks);
+        scale<V>(ks, A.scale2);
+        own_row<T>(A.val, jj, A.s, L, vj);
+        zero<V>(dk);
+        zero<V>(dv);
+        src_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, trips, in, ks, vj, dk, dv);
+        if (j >= 0) src_write<T>(A, L, j, dk, dv);
+      }
+    }
+    return;
+  }
+
+  // ---- light nodes, rows of a whole warp: one warp each -----------------
   for (;;) {
     int t0 = 0;
     if (L.lane == 0) t0 = atomicAdd(A.ctr + 3, kGrab);
@@ -732,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_src_main(const GtArgs A) {
       own_row<T>(A.val, j, A.s, L, vj);
       zero<V>(dk);
       zero<V>(dv);
-      src_edges<T>(A, L, D.idx, 0, beg, end, in, ks, vj, dk, dv);
+      src_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, 0, in, ks, vj, dk, dv);
       subgroup_sums<V>(dk, A.s);
       subgroup_sums<V>(dv, A.s);
       if (L.g == 0) src_write<T>(A, L, j, dk, dv);
@@ -810,14 +904,16 @@ cudaError_t bwd_t(const GtArgs& A, int sm_count, cudaStream_t st) {
   cudaError_t e;
   if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), st)) != cudaSuccess) return e;
   const size_t smem1 = size_t(A.csr.col_off) + size_t(kWarps) * (A.s.H + 2 * row_f) * 4;
-  if ((e = persistent_launch<T>(gt_dst_main<T>, A, A.csr, smem1, sm_count, st)) != cudaSuccess)
+  if ((e = persistent_launch<T>(A.s.lpr < 32 ? gt_dst_main<T, true> : gt_dst_main<T, false>, A, A.csr,
+                                    smem1, sm_count, st)) != cudaSuccess)
     return e;
   if (A.csr.n_hubs > 0) {
     gt_dst_merge<T><<<unsigned((A.csr.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const size_t smem2 = size_t(A.csc.col_off) + size_t(kWarps) * 2 * row_f * 4;
-  if ((e = persistent_launch<T>(gt_src_main<T>, A, A.csc, smem2, sm_count, st)) != cudaSuccess)
+  if ((e = persistent_launch<T>(A.s.lpr < 32 ? gt_src_main<T, true> : gt_src_main<T, false>, A, A.csc,
+                                    smem2, sm_count, st)) != cudaSuccess)
     return e;
   if (A.csc.n_hubs > 0) {
     gt_src_merge<T><<<unsigned((A.csc.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
