@@ -292,6 +292,56 @@ __device__ __forceinline__ void row_dot(const void* x, int64_t node, const Shape
   head_sums<NV>(out, s.hv_log2);
 }
 
+// The sources (or destinations) of the batch of edges starting at beg that
+// this lane's sub-group takes: edges beg + g, beg + g + G, ... (U of them)
+// below end, read from cols[edge - colbase]; -1 past the end.
+template <int U>
+__device__ __forceinline__ void batch_ids(const int32_t* cols, int colbase, int beg, int end,
+                                          int g, int G, int (&j)[U]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int e = beg + u * G + g;
+    j[u] = e < end ? cols[e - colbase] : -1;
+  }
+}
+
+// Butterfly sum over the warp's sub-groups (every lane ends with the total).
+__device__ __forceinline__ float subgroup_sum(float x, const Shape& s) {
+  for (int o = s.lpr; o < 32; o <<= 1) x += __shfl_xor_sync(kFull, x, o);
+  return x;
+}
+
+template <int V>
+__device__ __forceinline__ void subgroup_sums(float (&x)[V], const Shape& s) {
+#pragma unroll
+  for (int c = 0; c < V; ++c) x[c] = subgroup_sum(x[c], s);
+}
+
+template <int V>
+__device__ __forceinline__ void zero(float (&x)[V]) {
+#pragma unroll
+  for (int c = 0; c < V; ++c) x[c] = 0.f;
+}
+
+// s += x with the rounding error of the addition carried in c (Kahan's
+// compensated summation), for merges that add thousands of hub-chunk
+// partials, where a plain running sum loses accuracy with their number.
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
+  const float y = __fsub_rn(x, c);
+  const float t = __fadd_rn(s, y);
+  c = __fsub_rn(__fsub_rn(t, s), y);
+  s = t;
+}
+
+// This lane's slice (vector q) of row `node` when a row needs at most one
+// vector per lane, widened (zeros when !ok).
+template <typename T>
+__device__ __forceinline__ void own_row(const void* x, int64_t node, const Shape& s,
+                                        const Lane<1>& L, float (&r)[VecOf<T>::n]) {
+  unpack<T>(L.ok[0] ? ld16(row_base<T>(x, node, s.rv) + 16 * L.q[0]) : make_uint4(0, 0, 0, 0),
+            r);
+}
+
 // ---- mbarrier + bulk copy (shared::cta) --------------------------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -67,27 +67,8 @@ struct BwdArgs {
 
 constexpr int kGrab = 4;  // light nodes a warp takes per counter access
 
-// Sources (or destinations) of the batch of edges starting at beg that this
-// lane's sub-group takes (edges beg + g, beg + g + G, ... below end; -1 past
-// the end).
-template <int U>
-__device__ __forceinline__ void batch_ids(const int32_t* cols, int colbase, int beg, int end,
-                                          int g, int G, int (&j)[U]) {
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int e = beg + u * G + g;
-    j[u] = e < end ? cols[e - colbase] : -1;
-  }
-}
-
 __device__ __forceinline__ float leaky(float z, float slope) { return z > 0.f ? z : slope * z; }
 __device__ __forceinline__ float leaky_grad(float z, float slope) { return z > 0.f ? 1.f : slope; }
-
-// Butterfly sum over the warp's sub-groups (all lanes end with the total).
-__device__ __forceinline__ float subgroup_sum(float x, const Shape& s) {
-  for (int o = s.lpr; o < 32; o <<= 1) x += __shfl_xor_sync(kFull, x, o);
-  return x;
-}
 
 // ---------------------------------------------------------------------------
 // pass 1: destination side (CSR)

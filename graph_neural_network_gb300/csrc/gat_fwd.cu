@@ -98,18 +98,6 @@ struct Online {
   }
 };
 
-// Sources of the batch of edges starting at beg that this lane's sub-group
-// takes (edges beg + g, beg + g + G, ... below end; -1 past the end).
-template <int U>
-__device__ __forceinline__ void batch_sources(const int32_t* cols, int colbase, int beg, int end,
-                                              int g, int G, int (&j)[U]) {
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int e = beg + u * G + g;
-    j[u] = e < end ? cols[e - colbase] : -1;
-  }
-}
-
 // Stream the edges beg + sg, beg + sg + SG, ... < end through the online
 // softmax, kUnroll edges per lane and batch: until end (kFixed false; every
 // lane of the warp then has the same beg and end), or for exactly `trips`
@@ -142,7 +130,7 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
         sc[u * NV + v] = ok ? __ldg(A.ssrc + int64_t(j[u]) * H + L.k[v]) : 0.f;
       }
     if (kFixed ? t + 1 < trips : base + step < end)
-      batch_sources<U>(cols, colbase, base + step, end, sg, SG, jn);
+      batch_ids<U>(cols, colbase, base + step, end, sg, SG, jn);
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
@@ -231,7 +219,7 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, in
   const int wb = min(end, beg + wid * per), we = min(end, wb + per);
   const int colbase = beg & ~3;
   int jn[kUnroll];
-  batch_sources<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
+  batch_ids<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
   float sd2[NV];
   node_sdst<NV>(A, L, i, sd2);
   Online<T, NV> st;
@@ -342,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) fwd_main(c
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
         int jn[kUnroll];
-        batch_sources<kUnroll>(A.idx, 0, beg, end, 0, 1, jn);
+        batch_ids<kUnroll>(A.idx, 0, beg, end, 0, 1, jn);
         float sd2[NV];
         node_sdst<NV>(A, L, i >= 0 ? i : 0, sd2);
         Online<T, NV> st;
@@ -369,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) fwd_main(c
     int i = __shfl_sync(kFull, my_i, 0);
     int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
     int jn[kUnroll];
-    batch_sources<kUnroll>(A.idx, 0, beg, end, L.g, L.G, jn);
+    batch_ids<kUnroll>(A.idx, 0, beg, end, L.g, L.G, jn);
     for (int q = 0; q < kGrab && i >= 0; ++q) {
       // the next node's range and first sources, loaded while this one runs
       const int nq = (q + 1) & (kGrab - 1);
@@ -377,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) fwd_main(c
       const int b2 = __shfl_sync(kFull, my_b, nq);
       const int e2 = __shfl_sync(kFull, my_e, nq);
       int jn2[kUnroll];
-      batch_sources<kUnroll>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
+      batch_ids<kUnroll>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
       float sd2[NV];
       node_sdst<NV>(A, L, i, sd2);
       Online<T, NV> st;

@@ -66,16 +66,6 @@ __device__ __forceinline__ float unordered(uint32_t u) {
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
 
-template <int U>
-__device__ __forceinline__ void batch_ids(const int32_t* cols, int colbase, int beg, int end,
-                                          int g, int G, int (&j)[U]) {
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int e = beg + u * G + g;
-    j[u] = e < end ? cols[e - colbase] : -1;
-  }
-}
-
 template <typename T, int NV>
 struct Best {
   static constexpr int V = VecOf<T>::n;

@@ -53,16 +53,6 @@ __global__ void spmm_coef(const int32_t* ptr, int64_t n, int mode, float* c) {
   }
 }
 
-template <int U>
-__device__ __forceinline__ void batch_ids(const int32_t* cols, int colbase, int beg, int end,
-                                          int g, int G, int (&j)[U]) {
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int e = beg + u * G + g;
-    j[u] = e < end ? cols[e - colbase] : -1;
-  }
-}
-
 // acc += c_in(j) x_j over the edges beg + g, beg + g + G, ... < end.
 template <typename T, int NV>
 __device__ __forceinline__ void spmm_edges(const SpmmArgs& A, const Lane<NV>& L,
@@ -235,16 +225,6 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(
       for (int u = 0; u < kUnroll; ++u) jn[u] = jn2[u];
     }
   }
-}
-
-// s += x with the rounding error of the addition carried in c (Kahan's
-// compensated summation): a hub may have thousands of chunk partials, and
-// a plain running sum would lose accuracy with their number.
-__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
-  const float y = __fsub_rn(x, c);
-  const float t = __fadd_rn(s, y);
-  c = __fsub_rn(__fsub_rn(t, s), y);
-  s = t;
 }
 
 // One warp per hub: add its chunk partials in chunk order.

@@ -69,52 +69,11 @@ struct GtArgs {
   int32_t* err;
 };
 
-template <int U>
-__device__ __forceinline__ void batch_ids(const int32_t* cols, int colbase, int beg, int end,
-                                          int g, int G, int (&j)[U]) {
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int e = beg + u * G + g;
-    j[u] = e < end ? cols[e - colbase] : -1;
-  }
-}
-
-template <typename T>
-__device__ __forceinline__ void own_row(const void* x, int64_t node, const Shape& s,
-                                        const Lane<1>& L, float (&r)[VecOf<T>::n]) {
-  unpack<T>(L.ok[0] ? ld16(row_base<T>(x, node, s.rv) + 16 * L.q[0]) : make_uint4(0, 0, 0, 0),
-            r);
-}
-
 template <typename T>
 __device__ __forceinline__ uint4 gather(const void* x, int node, const Shape& s,
                                         const Lane<1>& L) {
   return (node >= 0 && L.ok[0]) ? ld16(row_base<T>(x, node, s.rv) + 16 * L.q[0])
                                 : make_uint4(0, 0, 0, 0);
-}
-
-template <int V>
-__device__ __forceinline__ void zero(float (&x)[V]) {
-#pragma unroll
-  for (int c = 0; c < V; ++c) x[c] = 0.f;
-}
-
-__device__ __forceinline__ float subgroup_sum(float x, const Shape& s) {
-  for (int o = s.lpr; o < 32; o <<= 1) x += __shfl_xor_sync(kFull, x, o);
-  return x;
-}
-
-template <int V>
-__device__ __forceinline__ void subgroup_sums(float (&x)[V], const Shape& s) {
-#pragma unroll
-  for (int c = 0; c < V; ++c) x[c] = subgroup_sum(x[c], s);
-}
-
-__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
-  const float y = __fsub_rn(x, c);
-  const float t = __fadd_rn(s, y);
-  c = __fsub_rn(__fsub_rn(t, s), y);
-  s = t;
 }
 
 // ---------------------------------------------------------------------------
