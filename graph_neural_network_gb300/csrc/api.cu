@@ -484,6 +484,11 @@ gnn_status reduce_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, const
                                                static_cast<cudaStream_t>(stream)));
 }
 
+gnn_status gnn_wait_selftest(const gnn_graph* g, int polls, void* stream) {
+  if (!g || !g->err || polls < 1 || polls > 1000000) return GNN_ERR_INVALID_ARG;
+  return from_cuda(gnn::launch_wait_selftest(g, polls, static_cast<cudaStream_t>(stream)));
+}
+
 gnn_status gnn_check_device_error(const gnn_graph* g, void* stream, int32_t* info) {
   if (!g || !g->err) return GNN_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -128,6 +128,9 @@ cudaError_t launch_transformer_backward(const gnn_graph* g, const Shape& s, gnn_
                                         void* dq, void* dkey, void* dval, char* ws,
                                         cudaStream_t st);
 
+// Bounded-wait self-test (diag.cu).
+cudaError_t launch_wait_selftest(const gnn_graph* g, int polls, cudaStream_t st);
+
 // Graph preparation (prepare.cu).
 gnn_status prepare_graph(gnn_graph* g, const int32_t* row_ptr, const int32_t* col,
                          char* buffer, size_t buffer_bytes, char* scratch, size_t scratch_bytes,

@@ -353,6 +353,15 @@ gnn_status reduce_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, const
  * out) or GNN_ERR_DEVICE_ASSERT; *info (may be NULL) receives the raw word. */
 gnn_status gnn_check_device_error(const gnn_graph* g, void* stream, int32_t* info);
 
+/* Diagnostic with no counterpart on the page: makes one bounded device wait
+ * run out, to exercise the error path that replaces a hang.  A single thread
+ * waits on a shared-memory mbarrier that nothing will complete, gives up
+ * after `polls` polls (1 .. 1,000,000), sets the timeout bit of g's status
+ * word and returns; nothing stays in flight and the context remains usable.
+ * A following gnn_check_device_error returns GNN_ERR_TIMEOUT (and clears the
+ * word).  Asynchronous on `stream`. */
+gnn_status gnn_wait_selftest(const gnn_graph* g, int polls, void* stream);
+
 /* Static description of a status code. */
 const char* gnn_status_string(gnn_status s);
 

@@ -87,6 +87,7 @@ def test_bad_arguments_rejected_without_gpu(lib):
     assert lib.gat_agg_workspace_bytes(None, 1, 16, 0) == 0
     assert lib.gnn_graph_stats(None, None, 16) == _native.ERR_INVALID_ARG
     assert lib.gnn_check_device_error(None, None, None) == _native.ERR_INVALID_ARG
+    assert lib.gnn_wait_selftest(None, 100, None) == _native.ERR_INVALID_ARG
 
 
 def test_product_package_does_not_use_the_oracle():

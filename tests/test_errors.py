@@ -1,5 +1,6 @@
-"""Error paths of the compute entry points (no fault is provoked: every case
-is rejected by the host-side checks before a kernel launches)."""
+"""Error paths of the compute entry points.  No fault is provoked: the bad
+arguments are rejected by host-side checks before a kernel launches, and the
+timeout case is a bounded device wait that runs out and reports a status."""
 import pytest
 import torch
 
@@ -65,3 +66,22 @@ def test_workspace_has_no_edge_by_head_term():
              + 4 * st["csc"]["hub_chunks"] * H * (D + 1) + 16 * blocks * H * D + 9 * 256)
     assert ws <= bound
     assert ws < 4 * e * H / 2
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(setup):
+    """A device wait that nothing completes gives up after its poll limit and
+    the host reads GNN_ERR_TIMEOUT; the context stays usable (no fault, no
+    hang)."""
+    import graph_neural_network_gb300 as gnn
+    from graph_neural_network_gb300 import _native
+    from gpu_util import compare, run_gpu, run_oracle
+    rp, ci = testgraphs.with_in_degrees([0, 3, 70, 300, 3000], n_nodes=600, seed=5)
+    case = make_case(rp, ci, 2, 16, "f32", 5)
+    g = device_graph(case)
+    lib = _native.load()
+    assert lib.gnn_wait_selftest(g.handle, 1000, None) == _native.OK
+    with pytest.raises(gnn.GnnError) as ex:
+        gnn.check_device_error(g)
+    assert ex.value.status == _native.ERR_TIMEOUT
+    assert gnn.check_device_error(g) == 0          # the status word was cleared
+    compare(run_gpu(case, graph=g), run_oracle(case), "f32", what="after a timeout")
