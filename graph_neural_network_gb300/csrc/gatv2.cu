@@ -15,15 +15,18 @@
 // Backward, with da_ij = dout_i . xl_j, Delta_i = sum_j alpha_ij da_ij,
 // de_ij = alpha_ij (da_ij - Delta_i), g = LeakyReLU'(z) and l = LeakyReLU(z):
 //   pass 1, destination side (CSR), one streaming pass per node that sums
-//     Delta, P = sum alpha da g, Q = sum alpha g, R = sum alpha da l,
-//     S = sum alpha l  (D-vectors), so that
-//     dxr_i = att (P - Delta Q) and node i's share of datt is R - Delta S;
-//     the per-node record {lse, Delta} goes to the workspace.
-//   pass 2, source side (cached CSC): dxl_j = sum_i alpha_ij dout_i +
-//     de_ij att g(z_ij), gathering xr_i, dout_i and i's record per edge.
-// datt is summed deterministically: pass 1 assigns work to blocks and warps
-// statically, each block folds its warps' sums in a fixed order, and a last
-// kernel adds the block sums in a fixed order in float64.
+//     Delta, P = sum alpha da g and Q = sum alpha g (D-vectors), so that
+//     u_i = sum_j de_ij g_ij = P - Delta Q and dxr_i = att u_i; the per-node
+//     record {lse, Delta} goes to the workspace.
+//   pass 2, source side (cached CSC): w_j = sum_i de_ij g_ij and
+//     dxl_j = sum_i alpha_ij dout_i + att w_j, gathering xr_i, dout_i and
+//     i's record per edge.
+// datt = sum over edges of de l.  Since l_ij = g_ij (xr_i + xl_j), it splits
+// into per-node terms, datt = sum_i xr_i u_i + sum_j xl_j w_j, so each pass
+// adds one product per node instead of one per edge.  Both passes assign
+// work to blocks and warps statically, each block folds its warps' sums in a
+// fixed order, and a last kernel adds the block sums in a fixed order in
+// float64: datt is deterministic.
 //
 // Rows up to 512 bytes (one 16-byte vector per lane).  Degree-aware tiling
 // and hub merges as in the GAT kernels.
@@ -70,10 +73,11 @@ struct V2Args {
   float* datt;
   float2* stats;     // [N][H] {lse (base 2), Delta}
   float* d_delta;    // [CSR hub chunks][H]
-  float* d_vec;      // [CSR hub chunks][4][row_f]  (P, Q, R, S)
+  float* d_vec;      // [CSR hub chunks][2][row_f]  (P, Q)
   float* s_acc;      // [CSC hub chunks][row_f]
   double* da_part;   // [da rows][row_f]
   int da_main_rows;  // rows of da_part written by pass 1 (one per block)
+  int da_src_row0;   // first da_part row of pass 2 (one per block)
   int* ctr;
   int32_t* err;
 };
@@ -391,23 +395,21 @@ __global__ void __launch_bounds__(kThreads) v2_fwd_merge(const V2Args A) {
 template <typename T>
 struct DstSums {
   static constexpr int V = VecOf<T>::n;
-  float delta, P[V], Q[V], R[V], S[V];
+  float delta, P[V], Q[V];
   __device__ __forceinline__ void init() {
     delta = 0.f;
     zero<V>(P);
     zero<V>(Q);
-    zero<V>(R);
-    zero<V>(S);
   }
   __device__ __forceinline__ void subgroup_total(const Shape& s) {
     delta = subgroup_sum(delta, s);
     subgroup_sums<V>(P, s);
     subgroup_sums<V>(Q, s);
-    subgroup_sums<V>(R, s);
-    subgroup_sums<V>(S, s);
   }
 };
 
+// The LeakyReLU slopes g of a batch stay in registers between the score
+// (which needs l = g z) and the sums (which need g alone).
 template <typename T>
 __device__ __forceinline__ void dst_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
                                           int colbase, int beg, int end, int (&jn)[kUB],
@@ -429,11 +431,12 @@ __device__ __forceinline__ void dst_edges(const V2Args& A, const Lane<1>& L, con
                                       : make_uint4(0, 0, 0, 0);
     if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
     float red[2 * U];  // scores (base 2), then dout_i . xl_j
+    float g[U][V];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float x[V], g[V], lz[V];
+      float x[V], lz[V];
       unpack<T>(raw[u], x);
-      leaky_terms<V>(xr, x, A.slope, g, lz);
+      leaky_terms<V>(xr, x, A.slope, g[u], lz);
       red[u] = dot<V>(lz, a2);
       red[U + u] = dot<V>(x, gi);
     }
@@ -443,23 +446,19 @@ __device__ __forceinline__ void dst_edges(const V2Args& A, const Lane<1>& L, con
       const float al = j[u] >= 0 ? ex2(red[u] - lse2) : 0.f;
       const float ad = al * red[U + u];
       sm.delta += ad;
-      float x[V], g[V], lz[V];
-      unpack_alt<T>(raw[u], x);
-      leaky_terms<V>(xr, x, A.slope, g, lz);
-      axpy<V>(sm.P, ad, g);
-      axpy<V>(sm.Q, al, g);
-      axpy<V>(sm.R, ad, lz);
-      axpy<V>(sm.S, al, lz);
+      axpy<V>(sm.P, ad, g[u]);
+      axpy<V>(sm.Q, al, g[u]);
     }
   }
 }
 
-// From the totals of node i: write dxr_i and i's record, add i's share of datt
-// into this warp's datt sums dslot[row_f] (shared memory; the lane's own
-// elements, so no other lane touches them).
+// From the totals of node i: u = P - Delta Q; write dxr_i = att u and i's
+// record, add i's datt term xr_i u into this warp's datt sums dslot[row_f]
+// (shared memory; the lane's own elements, so no other lane touches them).
 template <typename T>
 __device__ __forceinline__ void dst_finish(const V2Args& A, const Lane<1>& L, int64_t i,
-                                           const DstSums<T>& sm, float lse2, float* dslot) {
+                                           const DstSums<T>& sm, float lse2,
+                                           const float (&xr)[VecOf<T>::n], float* dslot) {
   constexpr int V = VecOf<T>::n;
   if (!L.ok[0]) return;
   float a[V], y[V];
@@ -467,8 +466,9 @@ __device__ __forceinline__ void dst_finish(const V2Args& A, const Lane<1>& L, in
   float* d = dslot + L.q[0] * V;
 #pragma unroll
   for (int c = 0; c < V; ++c) {
-    y[c] = a[c] * fmaf(-sm.delta, sm.Q[c], sm.P[c]);
-    d[c] += fmaf(-sm.delta, sm.S[c], sm.R[c]);
+    const float u = fmaf(-sm.delta, sm.Q[c], sm.P[c]);
+    y[c] = a[c] * u;
+    d[c] = fmaf(xr[c], u, d[c]);
   }
   st16(reinterpret_cast<char*>(A.dxr) + i * int64_t(A.s.rv) * 16 + 16 * L.q[0], pack<T>(y));
   if (L.head_leader(A.s, 0)) A.stats[i * A.s.H + L.k[0]] = make_float2(lse2, sm.delta);
@@ -505,8 +505,8 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
   extern __shared__ __align__(16) unsigned char smem[];
   float a2[V], xr[V], gi[V];
   att_slice<T>(A.att, L, kLog2e, a2);
-  float* wbuf = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H + 4 row_f]
-  float* dsum = wbuf + kWarps * (H + 4 * row_f);              // [kWarps][row_f] datt sums
+  float* wbuf = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H + 2 row_f]
+  float* dsum = wbuf + kWarps * (H + 2 * row_f);              // [kWarps][row_f] datt sums
   float* dslot = dsum + wid * row_f;
   zero_da<V>(L, dslot);
 
@@ -532,15 +532,13 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
       sm.init();
       dst_edges<T>(A, L, cols, colbase, wb, we, jn, xr, gi, a2, lse2, sm);
       sm.subgroup_total(A.s);
-      float* mine = wbuf + wid * (H + 4 * row_f);
+      float* mine = wbuf + wid * (H + 2 * row_f);
       if (L.g == 0 && L.ok[0]) {
         if (L.head_leader(A.s, 0)) mine[L.k[0]] = sm.delta;
 #pragma unroll
         for (int c = 0; c < V; ++c) {
-          mine[H + 0 * row_f + L.q[0] * V + c] = sm.P[c];
-          mine[H + 1 * row_f + L.q[0] * V + c] = sm.Q[c];
-          mine[H + 2 * row_f + L.q[0] * V + c] = sm.R[c];
-          mine[H + 3 * row_f + L.q[0] * V + c] = sm.S[c];
+          mine[H + L.q[0] * V + c] = sm.P[c];
+          mine[H + row_f + L.q[0] * V + c] = sm.Q[c];
         }
       }
       __syncthreads();
@@ -548,27 +546,23 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
         DstSums<T> tot;
         tot.init();
         for (int w = 0; w < kWarps; ++w) {
-          const float* o = wbuf + w * (H + 4 * row_f);
+          const float* o = wbuf + w * (H + 2 * row_f);
           tot.delta += o[L.k[0]];
 #pragma unroll
           for (int c = 0; c < V; ++c) {
-            tot.P[c] += o[H + 0 * row_f + L.q[0] * V + c];
-            tot.Q[c] += o[H + 1 * row_f + L.q[0] * V + c];
-            tot.R[c] += o[H + 2 * row_f + L.q[0] * V + c];
-            tot.S[c] += o[H + 3 * row_f + L.q[0] * V + c];
+            tot.P[c] += o[H + L.q[0] * V + c];
+            tot.Q[c] += o[H + row_f + L.q[0] * V + c];
           }
         }
         if (it.w < 0) {
-          dst_finish<T>(A, L, it.x, tot, lse2, dslot);
+          dst_finish<T>(A, L, it.x, tot, lse2, xr, dslot);
         } else {
           if (L.head_leader(A.s, 0)) A.d_delta[int64_t(it.w) * H + L.k[0]] = tot.delta;
-          float* pv = A.d_vec + int64_t(it.w) * 4 * row_f + L.q[0] * V;
+          float* pv = A.d_vec + int64_t(it.w) * 2 * row_f + L.q[0] * V;
 #pragma unroll
           for (int c = 0; c < V; ++c) {
-            pv[0 * row_f + c] = tot.P[c];
-            pv[1 * row_f + c] = tot.Q[c];
-            pv[2 * row_f + c] = tot.R[c];
-            pv[3 * row_f + c] = tot.S[c];
+            pv[c] = tot.P[c];
+            pv[row_f + c] = tot.Q[c];
           }
         }
       }
@@ -604,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
       sm.init();
       dst_edges<T>(A, L, D.idx, 0, beg, end, jn, xr, gi, a2, lse2, sm);
       sm.subgroup_total(A.s);
-      if (L.g == 0) dst_finish<T>(A, L, i, sm, lse2, dslot);
+      if (L.g == 0) dst_finish<T>(A, L, i, sm, lse2, xr, dslot);
       i = i2;
       beg = b2;
       end = e2;
@@ -616,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
 }
 
 // One warp per CSR hub (static): add its chunk sums in chunk order, finish the
-// node; each block's datt shares go to da_part[da_main_rows + block].
+// node; each block's datt terms go to da_part[da_main_rows + block].
 template <typename T>
 __global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
   constexpr int V = VecOf<T>::n;
@@ -635,17 +629,17 @@ __global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
     for (int c = 0; c < hb.z; ++c) {
       const int64_t slot = int64_t(hb.y) + c;
       tot.delta += A.d_delta[slot * H + L.k[0]];
-      const float* pv = A.d_vec + slot * 4 * row_f + L.q[0] * V;
+      const float* pv = A.d_vec + slot * 2 * row_f + L.q[0] * V;
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        tot.P[e] += pv[0 * row_f + e];
-        tot.Q[e] += pv[1 * row_f + e];
-        tot.R[e] += pv[2 * row_f + e];
-        tot.S[e] += pv[3 * row_f + e];
+        tot.P[e] += pv[e];
+        tot.Q[e] += pv[row_f + e];
       }
     }
+    float xr[V];
+    own_row<T>(A.xr, hb.x, A.s, L, xr);
     const float lse2 = A.lse_in[int64_t(hb.x) * H + L.k[0]] * kLog2e;
-    dst_finish<T>(A, L, hb.x, tot, lse2, dslot);
+    dst_finish<T>(A, L, hb.x, tot, lse2, xr, dslot);
   }
   fold_da(A, row_f, buf, A.da_main_rows + blockIdx.x);
 }
@@ -654,20 +648,19 @@ __global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
 // backward pass 2: source side
 // ---------------------------------------------------------------------------
 
-template <typename T, bool kFixed>
+// acc += alpha_ij dout_i and w += de_ij g_ij over the batch; the slopes g of
+// a batch stay in registers between the score and the sums.
+template <typename T>
 __device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int sg, int SG,
-                                          int trips, int (&in)[kUB],
+                                          int colbase, int beg, int end, int (&in)[kUB],
                                           const float (&xl)[VecOf<T>::n],
                                           const float (&a2)[VecOf<T>::n],
-                                          const float (&a)[VecOf<T>::n],
-                                          float (&acc)[VecOf<T>::n]) {
+                                          float (&acc)[VecOf<T>::n], float (&w)[VecOf<T>::n]) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUB;
-  const int step = SG * U;
+  const int step = L.G * U;
   const int H = A.s.H;
-  int base = beg;
-  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
+  for (int base = beg; base < end; base += step) {
     int i[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) i[u] = in[u];
@@ -680,15 +673,15 @@ __device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, con
       rg[u] = ok ? ld16(row_base<T>(A.dout, i[u], A.s.rv) + 16 * L.q[0]) : make_uint4(0, 0, 0, 0);
       st[u] = ok ? __ldg(A.stats + int64_t(i[u]) * H + L.k[0]) : make_float2(0.f, 0.f);
     }
-    if (kFixed ? t + 1 < trips : base + step < end)
-      batch_ids<U>(cols, colbase, base + step, end, sg, SG, in);
+    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, in);
     float red[2 * U];
+    float g[U][V];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float r[V], gd[V], g[V], lz[V];
+      float r[V], gd[V], lz[V];
       unpack<T>(rr[u], r);
       unpack<T>(rg[u], gd);
-      leaky_terms<V>(r, xl, A.slope, g, lz);
+      leaky_terms<V>(r, xl, A.slope, g[u], lz);
       red[u] = dot<V>(lz, a2);
       red[U + u] = dot<V>(gd, xl);
     }
@@ -697,15 +690,32 @@ __device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, con
     for (int u = 0; u < U; ++u) {
       const float al = i[u] >= 0 ? ex2(red[u] - st[u].x) : 0.f;
       const float de = al * (red[U + u] - st[u].y);
-      float r[V], gd[V], g[V], lz[V], dg[V];
-      unpack_alt<T>(rr[u], r);
+      float gd[V];
       unpack_alt<T>(rg[u], gd);
-      leaky_terms<V>(r, xl, A.slope, g, lz);
-#pragma unroll
-      for (int c = 0; c < V; c += 2) mul2v(dg[c], dg[c + 1], a[c], a[c + 1], g[c], g[c + 1]);
-      axpy<V>(acc, de, dg);
       axpy<V>(acc, al, gd);
+      axpy<V>(w, de, g[u]);
     }
+  }
+}
+
+// Warp totals of node j's (partial) sums: add the datt term xl_j w into this
+// warp's datt sums and turn acc into acc + att w (the lanes with g == 0).
+template <typename T>
+__device__ __forceinline__ void src_combine(const V2Args& A, const Lane<1>& L,
+                                            const float (&xl)[VecOf<T>::n],
+                                            float (&acc)[VecOf<T>::n],
+                                            float (&w)[VecOf<T>::n], float* dslot) {
+  constexpr int V = VecOf<T>::n;
+  subgroup_sums<V>(acc, A.s);
+  subgroup_sums<V>(w, A.s);
+  if (L.g != 0 || !L.ok[0]) return;
+  float a[V];
+  att_slice<T>(A.att, L, 1.f, a);
+  float* d = dslot + L.q[0] * V;
+#pragma unroll
+  for (int c = 0; c < V; ++c) {
+    d[c] = fmaf(xl[c], w[c], d[c]);
+    acc[c] = fmaf(a[c], w[c], acc[c]);
   }
 }
 
@@ -716,6 +726,9 @@ __device__ __forceinline__ void src_write(const V2Args& A, const Lane<1>& L, int
   st16(reinterpret_cast<char*>(A.dxl) + j * int64_t(A.s.rv) * 16 + 16 * L.q[0], pack<T>(acc));
 }
 
+// Work is assigned statically (block items b, b + B, ...; light groups by
+// warp), so that the per-block datt sums, folded into da_part[da_src_row0 +
+// block], do not depend on timing.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
   constexpr int V = VecOf<T>::n;
@@ -724,22 +737,20 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
   const int wid = threadIdx.x >> 5;
   const int row_f = A.s.rv * V;
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int s_item;
-  float a2[V], a[V], xl[V], acc[V];
+  float a2[V], xl[V], acc[V], w[V];
   att_slice<T>(A.att, L, kLog2e, a2);
-  att_slice<T>(A.att, L, 1.f, a);
+  float* wacc = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][row_f]
+  float* dsum = wacc + kWarps * row_f;                        // [kWarps][row_f] datt sums
+  float* dslot = dsum + wid * row_f;
+  zero_da<V>(L, dslot);
 
   if (D.n_items > 0) {
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     int32_t* cols = reinterpret_cast<int32_t*>(smem + 16);
-    float* wacc = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][row_f]
     uint32_t parity = 0;
     if (threadIdx.x == 0) mbar_init(bar, 1);
-    for (;;) {
-      if (threadIdx.x == 0) s_item = atomicAdd(A.ctr + 2, 1);
-      __syncthreads();
-      const int it_i = s_item;
-      if (it_i >= D.n_items) break;
+    __syncthreads();
+    for (int64_t it_i = blockIdx.x; it_i < D.n_items; it_i += gridDim.x) {
       const int4 it = D.items[it_i];
       if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
       const int per = (it.z - it.y + kWarps - 1) / kWarps;
@@ -749,8 +760,9 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
       batch_ids<kUB>(cols, colbase, wb, we, L.g, L.G, in);
       own_row<T>(A.xl, it.x, A.s, L, xl);
       zero<V>(acc);
-      src_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, 0, in, xl, a2, a, acc);
-      subgroup_sums<V>(acc, A.s);
+      zero<V>(w);
+      src_edges<T>(A, L, cols, colbase, wb, we, in, xl, a2, acc, w);
+      src_combine<T>(A, L, xl, acc, w, dslot);
       if (L.g == 0 && L.ok[0])
 #pragma unroll
         for (int c = 0; c < V; ++c) wacc[wid * row_f + L.q[0] * V + c] = acc[c];
@@ -759,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
 #pragma unroll
         for (int c = 0; c < V; ++c) {
           float s = 0.f;
-          for (int w = 0; w < kWarps; ++w) s += wacc[w * row_f + L.q[0] * V + c];
+          for (int k = 0; k < kWarps; ++k) s += wacc[k * row_f + L.q[0] * V + c];
           acc[c] = s;
         }
         if (it.w < 0) {
@@ -776,12 +788,10 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
     }
   }
 
-  // ---- light nodes, rows of a whole warp: one warp each -----------------
-  for (;;) {
-    int t0 = 0;
-    if (L.lane == 0) t0 = atomicAdd(A.ctr + 3, kGrab);
-    t0 = __shfl_sync(kFull, t0, 0);
-    if (t0 >= D.n_light) break;
+  // ---- light nodes, assigned statically: groups of kGrab per warp ---------
+  const int64_t gw = int64_t(blockIdx.x) * kWarps + wid;
+  const int64_t W = int64_t(gridDim.x) * kWarps;
+  for (int64_t t0 = gw * kGrab; t0 < D.n_light; t0 += W * kGrab) {
     int my_j = -1, my_b = 0, my_e = 0;
     if (L.lane < kGrab && t0 + L.lane < D.n_light) {
       my_j = D.light[t0 + L.lane];
@@ -801,8 +811,9 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
       batch_ids<kUB>(D.idx, 0, b2, j2 >= 0 ? e2 : b2, L.g, L.G, in2);
       own_row<T>(A.xl, j, A.s, L, xl);
       zero<V>(acc);
-      src_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, 0, in, xl, a2, a, acc);
-      subgroup_sums<V>(acc, A.s);
+      zero<V>(w);
+      src_edges<T>(A, L, D.idx, 0, beg, end, in, xl, a2, acc, w);
+      src_combine<T>(A, L, xl, acc, w, dslot);
       if (L.g == 0) src_write<T>(A, L, j, acc);
       j = j2;
       beg = b2;
@@ -811,6 +822,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
       for (int u = 0; u < kUB; ++u) in[u] = in2[u];
     }
   }
+  fold_da(A, row_f, dsum, A.da_src_row0 + blockIdx.x);
 }
 
 template <typename T>
@@ -879,15 +891,14 @@ template <typename T>
 cudaError_t bwd_t(V2Args A, int sm_count, cudaStream_t st) {
   constexpr int V = VecOf<T>::n;
   const int row_f = A.s.rv * V;
+  const int64_t cap = int64_t(sm_count > 0 ? sm_count : 1) * 8;
   cudaError_t e;
-  if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), st)) != cudaSuccess) return e;
   // pass 1: a fixed grid (static work assignment), one da_part row per block
   {
     const V2Dir& D = A.csr;
-    const size_t smem = size_t(D.col_off) + size_t(kWarps) * (A.s.H + 5 * row_f) * 4;
+    const size_t smem = size_t(D.col_off) + size_t(kWarps) * (A.s.H + 3 * row_f) * 4;
     if ((e = set_smem(v2_dst_main<T>, smem)) != cudaSuccess) return e;
     int64_t blocks = persistent_blocks(v2_dst_main<T>, smem, sm_count);
-    const int64_t cap = int64_t(sm_count > 0 ? sm_count : 1) * 8;
     if (blocks > cap) blocks = cap;
     A.da_main_rows = int(blocks);
     v2_dst_main<T><<<unsigned(blocks), kThreads, smem, st>>>(A);
@@ -897,26 +908,24 @@ cudaError_t bwd_t(V2Args A, int sm_count, cudaStream_t st) {
       v2_dst_merge<T><<<unsigned(mblocks), kThreads, 0, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    v2_datt_final<<<unsigned((row_f + kWarps - 1) / kWarps), kThreads, 0, st>>>(
-        A.da_part, int(blocks + mblocks), row_f, A.datt);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    A.da_src_row0 = int(blocks + mblocks);
   }
-  // pass 2
+  // pass 2: likewise a fixed grid, one da_part row per block
   {
     const V2Dir& D = A.csc;
-    if (D.n_items + D.n_light > 0) {
-      const size_t smem = size_t(D.col_off) + size_t(kWarps) * row_f * 4;
-      auto kernel = v2_src_main<T>;
-      if ((e = set_smem(kernel, smem)) != cudaSuccess) return e;
-      const int64_t work = D.n_items + (D.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
-      const int64_t cap = persistent_blocks(kernel, smem, sm_count);
-      kernel<<<unsigned(work < cap ? work : cap), kThreads, smem, st>>>(A);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    const size_t smem = size_t(D.col_off) + size_t(kWarps) * 2 * row_f * 4;
+    if ((e = set_smem(v2_src_main<T>, smem)) != cudaSuccess) return e;
+    int64_t blocks = persistent_blocks(v2_src_main<T>, smem, sm_count);
+    if (blocks > cap) blocks = cap;
+    v2_src_main<T><<<unsigned(blocks), kThreads, smem, st>>>(A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (D.n_hubs > 0) {
       v2_src_merge<T><<<unsigned((D.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    v2_datt_final<<<unsigned((row_f + kWarps - 1) / kWarps), kThreads, 0, st>>>(
+        A.da_part, int(A.da_src_row0 + blocks), row_f, A.datt);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -942,7 +951,8 @@ struct V2Layout {
 V2Layout v2_layout(const gnn_graph* g, const Shape& s) {
   const size_t row_f = size_t(s.rv) * 16 / s.esize;
   const size_t cc = size_t(g->csr.n_hub_chunks), sc = size_t(g->csc.n_hub_chunks);
-  const size_t da_rows = size_t(g->sm_count > 0 ? g->sm_count : 1) * 8 +
+  // one row per block of each pass (at most 8 per SM) and per hub-merge block
+  const size_t da_rows = size_t(g->sm_count > 0 ? g->sm_count : 1) * 16 +
                          size_t((g->csr.n_hubs + kWarps - 1) / kWarps);
   V2Layout L{};
   size_t off = 0;
@@ -956,7 +966,7 @@ V2Layout v2_layout(const gnn_graph* g, const Shape& s) {
   L.f_ml = take(cc * s.H * 8);
   L.stats = take(size_t(g->n) * s.H * 8);
   L.d_delta = take(cc * s.H * 4);
-  L.d_vec = take(cc * 4 * row_f * 4);
+  L.d_vec = take(cc * 2 * row_f * 4);
   L.s_acc = take(sc * row_f * 4);
   L.da_part = take(da_rows * row_f * 8);
   L.total = off;
