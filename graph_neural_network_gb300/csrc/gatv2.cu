@@ -99,6 +99,22 @@ __device__ __forceinline__ void leaky_terms(const float (&r)[V], const float (&x
   }
 }
 
+// l = LeakyReLU(r + x) elementwise, for the score alone: max(z, s z) when the
+// slope s is at most 1, min(z, s z) above 1.  Both give exactly z or the
+// rounded s z, the same values as g z above.
+template <int V>
+__device__ __forceinline__ void leaky_vals(const float (&r)[V], const float (&x)[V],
+                                           float slope, bool le1, float (&lz)[V]) {
+#pragma unroll
+  for (int c = 0; c < V; c += 2) {
+    float z0, z1, s0, s1;
+    add2(z0, z1, r[c], r[c + 1], x[c], x[c + 1]);
+    mul2v(s0, s1, z0, z1, slope, slope);
+    lz[c] = le1 ? fmaxf(z0, s0) : fminf(z0, s0);
+    lz[c + 1] = le1 ? fmaxf(z1, s1) : fminf(z1, s1);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void att_slice(const float* att, const Lane<1>& L, float scale,
                                           float (&w)[VecOf<T>::n]) {
@@ -164,11 +180,12 @@ __device__ __forceinline__ void fwd_edges(const V2Args& A, const Lane<1>& L, con
     if (kFixed ? t + 1 < trips : base + step < end)
       batch_ids<U>(cols, colbase, base + step, end, sg, SG, jn);
     float sc[U];
+    const bool le1 = A.slope <= 1.f;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float x[V], g[V], lz[V];
+      float x[V], lz[V];
       unpack<T>(raw[u], x);
-      leaky_terms<V>(xr, x, A.slope, g, lz);
+      leaky_vals<V>(xr, x, A.slope, le1, lz);
       sc[u] = dot<V>(lz, a2);
     }
     head_sums<U>(sc, A.s.hv_log2);
