@@ -534,11 +534,51 @@ def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev,
     e1.record(s_g)
     torch.cuda.synchronize()
     (ms,) = max_over_ranks([e0.elapsed_time(e1) / K], world, dev)
+    link = link_rates(bufs[0], ((h_host, "h"), (d_host, "dout")),
+                      ((o_host, "out"), (dh_host, "dh")), s_h, s_o)
+    # the step's copies cannot finish faster than the link moves them
+    link["copy_bound_ms"] = (h2d + d2h) / (link["both_gbs"] * 1e6)
     return {"value": job_rate(units, world, ms), "unit": UNIT, "ms_per_step": ms,
             "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "host_link": link,
             "pipeline": "two upload, one compute and two download streams, two device buffer "
                         "sets; dout uploads during the forward, out and lse download during "
                         "the backward"}
+
+
+def link_rates(b, ups, downs, s_up, s_down, reps=5):
+    """Host link bandwidth in GB/s measured with the e2e buffers (pinned host
+    memory, copy engines): uploads alone, downloads alone, and both directions
+    at once on their own streams, each timed with events after a warm-up."""
+    import torch
+
+    def rate(do_up, do_down):
+        nbytes = 0
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for r in range(reps + 1):
+            if r == 1:
+                torch.cuda.synchronize()
+                t0.record(s_up)
+                s_down.wait_event(t0)
+            if do_up:
+                with torch.cuda.stream(s_up):
+                    for src, name in ups:
+                        b[name].copy_(src, non_blocking=True)
+                        nbytes += src.numel() * src.element_size() if r else 0
+            if do_down:
+                with torch.cuda.stream(s_down):
+                    for dst, name in downs:
+                        dst.copy_(b[name], non_blocking=True)
+                        nbytes += dst.numel() * dst.element_size() if r else 0
+        done = torch.cuda.Event()
+        done.record(s_down)
+        s_up.wait_event(done)
+        t1.record(s_up)
+        torch.cuda.synchronize()
+        return nbytes / (t0.elapsed_time(t1) * 1e6)
+
+    return {"h2d_gbs": rate(True, False), "d2h_gbs": rate(False, True),
+            "both_gbs": rate(True, True)}
 
 
 def run_layer(args, rank, world):

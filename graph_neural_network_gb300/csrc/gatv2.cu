@@ -99,20 +99,23 @@ __device__ __forceinline__ void leaky_terms(const float (&r)[V], const float (&x
   }
 }
 
-// l = LeakyReLU(r + x) elementwise, for the score alone: max(z, s z) when the
-// slope s is at most 1, min(z, s z) above 1.  Both give exactly z or the
-// rounded s z, the same values as g z above.
+// The score att . LeakyReLU(r + x) (att given as w) for the forward, with
+// LeakyReLU(z) = c1 z + c2 |z|, c1 = (1 + s) / 2, c2 = (1 - s) / 2: the sums
+// of w z and of w |z| take multiply-adds only (|z| is an operand modifier),
+// where max(z, s z) or a select would take the integer/logic pipe.
 template <int V>
-__device__ __forceinline__ void leaky_vals(const float (&r)[V], const float (&x)[V],
-                                           float slope, bool le1, float (&lz)[V]) {
+__device__ __forceinline__ float score_abs(const float (&r)[V], const float (&x)[V],
+                                           const float (&w)[V], float c1, float c2) {
+  float d0 = 0.f, d1 = 0.f, e0 = 0.f, e1 = 0.f;
 #pragma unroll
   for (int c = 0; c < V; c += 2) {
-    float z0, z1, s0, s1;
+    float z0, z1;
     add2(z0, z1, r[c], r[c + 1], x[c], x[c + 1]);
-    mul2v(s0, s1, z0, z1, slope, slope);
-    lz[c] = le1 ? fmaxf(z0, s0) : fminf(z0, s0);
-    lz[c + 1] = le1 ? fmaxf(z1, s1) : fminf(z1, s1);
+    fma2(d0, d1, z0, z1, w[c], w[c + 1]);
+    e0 = fmaf(w[c], fabsf(z0), e0);
+    e1 = fmaf(w[c + 1], fabsf(z1), e1);
   }
+  return fmaf(c1, d0 + d1, c2 * (e0 + e1));
 }
 
 template <typename T>
@@ -180,13 +183,12 @@ __device__ __forceinline__ void fwd_edges(const V2Args& A, const Lane<1>& L, con
     if (kFixed ? t + 1 < trips : base + step < end)
       batch_ids<U>(cols, colbase, base + step, end, sg, SG, jn);
     float sc[U];
-    const bool le1 = A.slope <= 1.f;
+    const float c1 = 0.5f * (1.f + A.slope), c2 = 0.5f * (1.f - A.slope);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float x[V], lz[V];
+      float x[V];
       unpack<T>(raw[u], x);
-      leaky_vals<V>(xr, x, A.slope, le1, lz);
-      sc[u] = dot<V>(lz, a2);
+      sc[u] = score_abs<V>(xr, x, a2, c1, c2);
     }
     head_sums<U>(sc, A.s.hv_log2);
     float bm = -INFINITY;

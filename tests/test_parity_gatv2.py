@@ -82,7 +82,7 @@ def test_gatv2_power_law_default_tiling(dtype):
 def test_gatv2_slope_and_reproducibility():
     rp, ci = workload.chung_lu(20_000, 2.1, 15.0, 4_000.0, 29)
     check(rp, ci, 2, 16, "f32", slope=1.0, what="slope 1")
-    # the score's LeakyReLU takes max(z, s z) up to slope 1 and min(z, s z) above it
+    # the forward's score writes LeakyReLU(z) as (1 + s)/2 z + (1 - s)/2 |z|, for any slope
     check(rp, ci, 2, 16, "f32", slope=1.5, what="slope 1.5")
     check(rp, ci, 2, 16, "bf16", slope=-0.3, what="slope -0.3")
     check(rp, ci, 2, 16, "f32", slope=0.0, what="slope 0")
