@@ -260,8 +260,8 @@ gnn_status gcn_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, gnn_norm
  * layers).  Same streaming design as the GAT calls: one pass over each
  * node's in-neighbours with an online softmax, no per-edge tensor in device
  * memory, lse kept for the backward, which walks the CSR (destination side:
- * dxr and datt) and the cached CSC (source side: dxl).  Results, datt
- * included, are bitwise reproducible.
+ * dxr) and the cached CSC (source side: dxl); each pass adds its per-node
+ * share of datt.  Results, datt included, are bitwise reproducible.
  * Layout: xl, xr, out, dout, dxl, dxr [N][H][D] dtype; att, datt [H][D]
  * float; lse [N][H] float.  Shapes as for the GAT calls, with the further
  * limit H * D * sizeof(dtype) <= 512 bytes.  Pointers 16-byte aligned (lse
