@@ -175,21 +175,36 @@ def time_oracle(rp, ci, h, a_s, a_d, dout, slope):
     return time.perf_counter() - t0
 
 
-def oracle_baseline(w, rp, ci, h, a_s, a_d, dout, budget_s):
+def oracle_sample_rate(w, rp, ci, h, a_s, a_d, dout, budget_s):
     """Oracle throughput on a bounded sample: a probe on 2% of the edges sizes
     a prefix subgraph that takes about budget_s seconds."""
-    import oracle
     probe_rp, probe_ci, _ = cpu_sample(rp, ci, 0.02)
     t_probe = time_oracle(probe_rp, probe_ci, h, a_s, a_d, dout, w.slope)
     frac = min(1.0, 0.02 * budget_s / max(t_probe, 1e-3))
     srp, sci, m = cpu_sample(rp, ci, frac)
     t = time_oracle(srp, sci, h, a_s, a_d, dout, w.slope)
-    units = len(sci) * w.H
-    return {"value": units / t / 1e9, "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"destinations 0..{m - 1} of {len(rp) - 1} with their {len(sci)} in-edges "
-                      f"({100.0 * len(sci) / len(ci):.1f}% of E), all N nodes; fp64 forward + "
-                      f"backward, {t:.2f} s"}
+    sample = (f"destinations 0..{m - 1} of {len(rp) - 1} with their {len(sci)} in-edges "
+              f"({100.0 * len(sci) / len(ci):.1f}% of E), all N nodes; fp64 forward + "
+              f"backward, {t:.2f} s")
+    return len(sci) * w.H / t / 1e9, sample
+
+
+def oracle_baseline(w, rp, ci, h, a_s, a_d, dout, budget_s, one_core=False):
+    """The oracle on all host cores; with one_core also on one core (a
+    smaller sample, half the budget)."""
+    import oracle
+    value, sample = oracle_sample_rate(w, rp, ci, h, a_s, a_d, dout, budget_s)
+    res = {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": sample}
+    if one_core:
+        n_all = oracle.num_threads()
+        oracle.set_threads(1)
+        try:
+            v1, s1 = oracle_sample_rate(w, rp, ci, h, a_s, a_d, dout, budget_s / 2)
+        finally:
+            oracle.set_threads(n_all)
+        res["one_core"] = {"value": v1, "unit": UNIT, "cores": 1, "sample": s1}
+    return res
 
 
 # ---- reference arm: the oracle on the host ------------------------------------------
@@ -241,6 +256,13 @@ def source_hash(paths):
 def measured_traffic(workload_name, kernel):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if its
     kernel source is unchanged since the capture; else None."""
+    entry = measured_entry(workload_name, kernel)
+    return entry["bytes_per_launch"] if entry else None
+
+
+def measured_entry(workload_name, kernel):
+    """The committed ncu record of `kernel` (bytes_per_launch, l2_hit_pct),
+    if its kernel source is unchanged since the capture; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -253,7 +275,7 @@ def measured_traffic(workload_name, kernel):
         srcs = [os.path.join(ROOT, p) for p in entry["sources"]]
         if source_hash(srcs) != entry["source_hash"]:
             return None
-        return entry["bytes_per_launch"]
+        return entry
     except (OSError, ValueError, KeyError):
         return None
 
@@ -401,16 +423,31 @@ def run_gnnagg(args, rank, world):
 
     kern = {name: 0.0 for name in FWD_KERNELS + BWD_KERNELS}
     t_fwd = t_bwd = 0.0
+    per_step = []
     for k in range(K):
         fe, be = fev[k][0], bev[k][0]
         for i, name in enumerate(FWD_KERNELS):
             kern[name] += fe[i].elapsed_time(fe[i + 1])
         for i, name in enumerate(BWD_KERNELS):
             kern[name] += be[i].elapsed_time(be[i + 1])
-        t_fwd += fe[0].elapsed_time(fe[-1])
-        t_bwd += be[0].elapsed_time(be[-1])
+        tf, tb = fe[0].elapsed_time(fe[-1]), be[0].elapsed_time(be[-1])
+        t_fwd += tf
+        t_bwd += tb
+        per_step.append(tf + tb)
     t_fwd /= K
     t_bwd /= K
+
+    # secondary figure: the same steps back to back with no flush (warm L2)
+    Kw = min(K, 50)
+    wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(Kw)]
+    for a, b in wev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    gnn.check_device_error(g)
+    (warm_ms,) = max_over_ranks([sum(a.elapsed_time(b) for a, b in wev) / Kw], world, dev)
     kern = {k: v / K for k, v in kern.items()}
     ms_step, t_fwd = max_over_ranks([t_fwd + t_bwd, t_fwd], world, dev)
     units = e * H
@@ -423,11 +460,20 @@ def run_gnnagg(args, rank, world):
     dom = max(main, key=main.get)
     peak, peak_kind = peaks()
     achieved = ab[dom] / (kern[dom] * 1e-3) / 1e9
-    traffic = measured_traffic(w.name, dom)
+    rec = measured_entry(w.name, dom)
+    traffic = rec["bytes_per_launch"] if rec else None
     step_bytes = ab["fwd_main"] + ab["bwd_dst_main"] + ab["bwd_src_main"] + 2 * ab["scores"]
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_bytes": ab[dom], "peak_source": peak_kind}
+    if rec:
+        # real DRAM rate of the same kernel: ncu bytes per launch over its event time
+        roofline["dram_gbs"] = traffic / (kern[dom] * 1e-3) / 1e9
+        roofline["dram_frac"] = roofline["dram_gbs"] / peak
+        if "l2_hit_pct" in rec:
+            roofline["l2_hit_pct"] = rec["l2_hit_pct"]
+    io_bytes = sum(t.numel() * t.element_size()
+                   for t in (rp_d, ci_d, h, dout, a_s, a_d, out, lse, dh, da_s, da_d))
     kernel_frac = {k: ab[k] / (kern[k] * 1e-3) / 1e9 / peak for k in main if kern[k] > 0}
     for k in ("fwd_scores", "bwd_scores"):
         if kern[k] > 0:
@@ -448,12 +494,18 @@ def run_gnnagg(args, rank, world):
                        "l2": flush.describe(),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "fwd_value": fwd_value, "fwd_ms": t_fwd, "bwd_ms": t_bwd,
+            "ms_per_step_median": float(np.median(per_step)),
+            "warm": {"ms_per_step": warm_ms, "value": job_rate(units, world, warm_ms),
+                     "steps": Kw, "l2": "not flushed between steps"},
             "kernels_ms": kern, "kernel_hbm_frac": kernel_frac,
             "roofline": roofline,
             "step_roofline": {"achieved": step_bytes / (ms_step * 1e-3) / 1e9, "peak": peak,
                               "unit": "GB/s", "frac": step_bytes / (ms_step * 1e-3) / 1e9 / peak},
             "gpu_launches": launches_per_step * K,
             "prepare_ms": prepare_ms, "peak_mem_gb": peak_mem / 1e9,
+            "memory_gb": {"graph_buffer": g.buffer.numel() / 1e9, "workspace": ws.numel() / 1e9,
+                          "inputs_outputs": io_bytes / 1e9,
+                          "peak_above_inputs": peak_mem / 1e9},
             "clocks": clocks, "wall_s": wall}
 
     if not args.no_e2e:
@@ -461,7 +513,7 @@ def run_gnnagg(args, rank, world):
                           dev, units)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(w, rp, ci, h_np, a_s_np, a_d_np, dout_np,
-                                               args.cpu_budget_s)
+                                               args.cpu_budget_s, one_core=args.config <= 2)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

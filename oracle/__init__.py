@@ -86,6 +86,8 @@ def _bind(path: str):
     lib.oracle_gt_backward.restype = i32
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
+    lib.oracle_set_threads.argtypes = [i32]
+    lib.oracle_set_threads.restype = None
     return lib
 
 
@@ -137,6 +139,10 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
+
+    def set_threads(self, n: int) -> None:
+        """Threads of the oracle's later calls (no effect on the results)."""
+        self.lib.oracle_set_threads(int(n))
 
     def forward(self, row_ptr, col, h, a_src, a_dst, slope, sel=None, with_mag=False, with_alpha_sum=False):
         row_ptr, col, h, a_src, a_dst, n, H, D, dt = _prep(row_ptr, col, h, a_src, a_dst)
@@ -444,6 +450,7 @@ def _sel(sel):
 _default = Oracle()
 att_grads = _default.att_grads
 num_threads = _default.num_threads
+set_threads = _default.set_threads
 forward = _default.forward
 node_stats = _default.node_stats
 backward = _default.backward

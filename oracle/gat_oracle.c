@@ -160,6 +160,15 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads for the oracle's later parallel regions (timing on fewer cores). */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /*
  * Forward.  sel = NULL computes every node (n_out = n); otherwise the n_sel
  * listed nodes, output row t belonging to node sel[t].
