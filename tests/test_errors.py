@@ -68,6 +68,32 @@ def test_workspace_has_no_edge_by_head_term():
     assert ws < 4 * e * H / 2
 
 
+def test_peak_memory_has_no_edge_by_head_term():
+    """Device memory the forward + backward calls take beyond their inputs
+    and outputs (workspace and any temporary of the binding), as torch's
+    allocator records it, stays far below one float per edge and head."""
+    import graph_neural_network_gb300 as gnn
+    import workload
+    rp, ci = workload.chung_lu(200_000, 2.1, 50.0, 20_000.0, 11)
+    H, D = 8, 16
+    case = make_case(rp, ci, H, D, "bf16", 5)
+    h = to_device(case["h"], "bf16")
+    dout = to_device(case["dout"], "bf16")
+    a_s = torch.from_numpy(case["a_src"]).cuda()
+    a_d = torch.from_numpy(case["a_dst"]).cuda()
+    g = device_graph(case)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    out, lse = gnn.gat_forward(g, h, a_s, a_d, 0.2)
+    dh, da_s, da_d = gnn.gat_backward(g, h, a_s, a_d, 0.2, lse, dout)
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated() - base
+    outputs = sum(t.numel() * t.element_size() for t in (out, lse, dh, da_s, da_d))
+    e = len(case["col"])
+    assert peak - outputs < 4 * e * H / 4, (peak - outputs, 4 * e * H)
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(setup):
     """A device wait that nothing completes gives up after its poll limit and
     the host reads GNN_ERR_TIMEOUT; the context stays usable (no fault, no
