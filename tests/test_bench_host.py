@@ -1,0 +1,48 @@
+"""Host-side helpers of bench.py (CPU only): the bounded oracle sample, the
+bytes model and the committed traffic records."""
+import json
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_cpu_sample_is_a_csr_prefix():
+    rp = np.array([0, 2, 5, 5, 9, 12], np.int32)
+    ci = np.arange(12, dtype=np.int32) % 5
+    srp, sci, m = bench.cpu_sample(rp, ci, 0.4)   # about 5 of 12 edges
+    assert m == 2 and len(srp) == len(rp)
+    assert list(srp) == [0, 2, 5, 5, 5, 5]       # rows past m keep no edges
+    assert list(sci) == list(ci[:5])
+    _, sci_all, m_all = bench.cpu_sample(rp, ci, 1.0)
+    assert m_all == 5 and len(sci_all) == 12
+
+
+def test_bytes_model_matches_its_definition():
+    n, e, H, D, s = 1000, 17000, 4, 32, 4
+    ab = bench.algorithmic_bytes(n, e, H, D, s)
+    idx = 4 * (n + 1) + 4 * e
+    assert ab["fwd_main"] == idx + s * e * H * D + s * n * H * D + 4 * n * H
+    assert ab["bwd_dst_main"] == idx + s * e * H * D + 2 * s * n * H * D
+    assert ab["bwd_src_main"] == idx + s * e * H * D + 2 * s * n * H * D
+
+
+def test_traffic_records_name_existing_sources():
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    for wl, kernels in rec.items():
+        if wl.startswith("_"):
+            continue
+        for k, entry in kernels.items():
+            assert entry["bytes_per_launch"] > 0, (wl, k)
+            for src in entry["sources"]:
+                assert os.path.exists(os.path.join(ROOT, src)), src
+            # a record is reported only while its sources hash to the recorded value
+            got = bench.measured_traffic(wl, k)
+            current = bench.source_hash([os.path.join(ROOT, p) for p in entry["sources"]])
+            assert got == (entry["bytes_per_launch"] if current == entry["source_hash"] else None)
