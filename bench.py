@@ -77,7 +77,8 @@ def algorithmic_bytes(n, e, H, D, s):
     dout_i, h_j read, dh_j written.  The per-edge gather of the 16-byte
     destination statistics in the source-side pass is extra traffic, not
     counted here (reported separately as stats_bytes).  The per-node score
-    pre-pass of each call reads h once and writes two float [N][H] arrays."""
+    pre-pass of the forward call reads h once and writes two float [N][H]
+    arrays; the backward of a step reuses them."""
     idx = 4 * (n + 1) + 4 * e
     gath = s * e * H * D
     row = s * n * H * D
@@ -388,8 +389,10 @@ def run_gnnagg(args, rank, world):
                                        fe, FWD_EVENTS if fe is not None else 0)
         _native.check(rc, "forward")
 
+    # a step passes one workspace to both calls, so the backward takes the
+    # per-node scores the forward left there
     def bwd(be=None):
-        rc = lib.gat_agg_backward_timed(g.handle, H, D, dt_code, ptr(h), ptr(a_s), ptr(a_d),
+        rc = lib.gat_agg_backward_reuse(g.handle, H, D, dt_code, ptr(h), ptr(a_s), ptr(a_d),
                                         w.slope, ptr(lse), ptr(dout), ptr(dh), ptr(da_s),
                                         ptr(da_d), ptr(ws), ws.numel(), sp,
                                         be, BWD_EVENTS if be is not None else 0)
@@ -483,7 +486,7 @@ def run_gnnagg(args, rank, world):
                                        w.slope, ptr(out), ptr(lse), ptr(ws), ws.numel(), spx,
                                        None, 0)
         _native.check(rc, "forward")
-        rc = lib.gat_agg_backward_timed(g.handle, H, D, dt_code, ptr(h), ptr(a_s), ptr(a_d),
+        rc = lib.gat_agg_backward_reuse(g.handle, H, D, dt_code, ptr(h), ptr(a_s), ptr(a_d),
                                         w.slope, ptr(lse), ptr(dout), ptr(dh), ptr(da_s),
                                         ptr(da_d), ptr(ws), ws.numel(), spx, None, 0)
         _native.check(rc, "backward")
@@ -521,7 +524,7 @@ def run_gnnagg(args, rank, world):
     achieved = ab[dom] / (kern[dom] * 1e-3) / 1e9
     rec = measured_entry(w.name, dom)
     traffic = rec["bytes_per_launch"] if rec else None
-    step_bytes = ab["fwd_main"] + ab["bwd_dst_main"] + ab["bwd_src_main"] + 2 * ab["scores"]
+    step_bytes = ab["fwd_main"] + ab["bwd_dst_main"] + ab["bwd_src_main"] + ab["scores"]
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_bytes": ab[dom], "peak_source": peak_kind}
@@ -534,13 +537,12 @@ def run_gnnagg(args, rank, world):
     io_bytes = sum(t.numel() * t.element_size()
                    for t in (rp_d, ci_d, h, dout, a_s, a_d, out, lse, dh, da_s, da_d))
     kernel_frac = {k: ab[k] / (kern[k] * 1e-3) / 1e9 / peak for k in main if kern[k] > 0}
-    for k in ("fwd_scores", "bwd_scores"):
-        if kern[k] > 0:
-            kernel_frac[k] = ab["scores"] / (kern[k] * 1e-3) / 1e9 / peak
+    if kern["fwd_scores"] > 0:  # the backward reuses these scores: no bwd_scores kernel
+        kernel_frac["fwd_scores"] = ab["scores"] / (kern["fwd_scores"] * 1e-3) / 1e9 / peak
 
-    # forward: scores, main, hub merge; backward: scores, two main kernels and
-    # their hub merges, two attention-gradient kernels
-    launches_per_step = (2 + (st["csr"]["hubs"] > 0)) + (2 + (st["csr"]["hubs"] > 0)) + \
+    # forward: scores, main, hub merge; backward (scores reused): two main
+    # kernels and their hub merges, two attention-gradient kernels
+    launches_per_step = (2 + (st["csr"]["hubs"] > 0)) + (1 + (st["csr"]["hubs"] > 0)) + \
         (1 + (st["csc"]["hubs"] > 0)) + 2
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -635,7 +637,8 @@ def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev,
         fwd_done[i].record(comp)
         comp.wait_event(d_ready[i])            # dout arrived while the forward ran
         gnn.gat_backward(g, b["h"], b["a_s"], b["a_d"], w.slope, b["lse"], b["dout"],
-                         dh=b["dh"], da_src=b["da_s"], da_dst=b["da_d"], ws=ws, stream=comp)
+                         dh=b["dh"], da_src=b["da_s"], da_dst=b["da_d"], ws=ws, stream=comp,
+                         reuse_scores=True)
         comp_done[i].record(comp)
         for st, after, done, copies in ((s_o, fwd_done, o_done, ((o_host, "out"),
                                                                    (l_host, "lse"))),

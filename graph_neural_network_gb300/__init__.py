@@ -184,8 +184,12 @@ def gat_forward(g: Graph, h: torch.Tensor, a_src: torch.Tensor, a_dst: torch.Ten
 
 def gat_backward(g: Graph, h: torch.Tensor, a_src: torch.Tensor, a_dst: torch.Tensor,
                  slope: float, lse: torch.Tensor, dout: torch.Tensor, dh=None, da_src=None,
-                 da_dst=None, ws=None, stream=None):
-    """dh [N,H,D] (h's dtype), da_src and da_dst [H,D] float32."""
+                 da_dst=None, ws=None, stream=None, reuse_scores=False):
+    """dh [N,H,D] (h's dtype), da_src and da_dst [H,D] float32.
+
+    reuse_scores: ws is the workspace the gat_forward call on the same h,
+    a_src, a_dst used, untouched since; the backward then takes the per-node
+    scores that call left there instead of computing them again."""
     _check_features(g, h, "h")
     _check_features(g, dout, "dout")
     if dout.dtype != h.dtype:
@@ -202,10 +206,18 @@ def gat_backward(g: Graph, h: torch.Tensor, a_src: torch.Tensor, a_dst: torch.Te
     if da_dst is None:
         da_dst = torch.empty((H, D), dtype=torch.float32, device=h.device)
     if ws is None:
+        if reuse_scores:
+            raise ValueError("reuse_scores needs the forward call's workspace")
         ws = g.workspace(H, D, h.dtype)
-    rc = g._lib.gat_agg_backward(g.handle, H, D, dt, _ptr(h), _ptr(a_src), _ptr(a_dst),
-                                 float(slope), _ptr(lse), _ptr(dout), _ptr(dh), _ptr(da_src),
-                                 _ptr(da_dst), _ptr(ws), ws.numel(), _stream(stream, h.device))
+    if reuse_scores:
+        rc = g._lib.gat_agg_backward_reuse(g.handle, H, D, dt, _ptr(h), _ptr(a_src), _ptr(a_dst),
+                                           float(slope), _ptr(lse), _ptr(dout), _ptr(dh),
+                                           _ptr(da_src), _ptr(da_dst), _ptr(ws), ws.numel(),
+                                           _stream(stream, h.device), None, 0)
+    else:
+        rc = g._lib.gat_agg_backward(g.handle, H, D, dt, _ptr(h), _ptr(a_src), _ptr(a_dst),
+                                     float(slope), _ptr(lse), _ptr(dout), _ptr(dh), _ptr(da_src),
+                                     _ptr(da_dst), _ptr(ws), ws.numel(), _stream(stream, h.device))
     _native.check(rc, "gat_agg_backward")
     return dh, da_src, da_dst
 
@@ -473,14 +485,17 @@ class GATAggregate(torch.autograd.Function):
     @staticmethod
     def forward(ctx, g, h, a_src, a_dst, slope):
         h = h.contiguous()
-        out, lse = gat_forward(g, h, a_src, a_dst, slope)
+        ws = g.workspace(h.shape[1], h.shape[2], h.dtype)
+        out, lse = gat_forward(g, h, a_src, a_dst, slope, ws=ws)
         ctx.g = g
         ctx.slope = slope
+        ctx.ws = ws  # its per-node scores serve the backward; nothing else writes it
         ctx.save_for_backward(h, a_src, a_dst, lse)
         return out
 
     @staticmethod
     def backward(ctx, dout):
         h, a_src, a_dst, lse = ctx.saved_tensors
-        dh, da_s, da_d = gat_backward(ctx.g, h, a_src, a_dst, ctx.slope, lse, dout.contiguous())
+        dh, da_s, da_d = gat_backward(ctx.g, h, a_src, a_dst, ctx.slope, lse, dout.contiguous(),
+                                      ws=ctx.ws, reuse_scores=True)
         return None, dh, da_s.to(a_src.dtype), da_d.to(a_dst.dtype), None

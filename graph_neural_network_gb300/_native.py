@@ -40,6 +40,8 @@ SIGNATURES = [
                                      _P, _I32]),
     ("gat_agg_backward_timed", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _F, _P, _P, _P, _P, _P,
                                       _P, _SZ, _P, _P, _I32]),
+    ("gat_agg_backward_reuse", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _F, _P, _P, _P, _P, _P,
+                                      _P, _SZ, _P, _P, _I32]),
     ("gat_agg_forward_noalloc", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _F, _P, _P, _P]),
     ("gat_agg_forward_noalloc_capacity", _SZ, []),
     ("gcn_agg_workspace_bytes", _SZ, [_P, _I32, _I32]),

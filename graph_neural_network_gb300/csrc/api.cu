@@ -257,11 +257,15 @@ gnn_status gat_agg_forward(const gnn_graph* g, int H, int D, gnn_dtype dtype, co
                                stream, nullptr, 0);
 }
 
-gnn_status gat_agg_backward_timed(const gnn_graph* g, int H, int D, gnn_dtype dtype,
-                                  const void* h, const float* a_src, const float* a_dst,
-                                  float slope, const float* lse, const void* dout, void* dh,
-                                  float* da_src, float* da_dst, void* ws, size_t ws_bytes,
-                                  void* stream, void* const* events, int n_events) {
+}  // extern "C"
+
+namespace {
+
+gnn_status backward_call(const gnn_graph* g, int H, int D, gnn_dtype dtype, const void* h,
+                         const float* a_src, const float* a_dst, float slope, const float* lse,
+                         const void* dout, void* dh, float* da_src, float* da_dst, void* ws,
+                         size_t ws_bytes, void* stream, void* const* events, int n_events,
+                         bool reuse_scores) {
   if (events && n_events < 8) return GNN_ERR_INVALID_ARG;
   Shape s;
   gnn_status r = check_call(g, H, D, dtype, &s);
@@ -277,10 +281,35 @@ gnn_status gat_agg_backward_timed(const gnn_graph* g, int H, int D, gnn_dtype dt
   const WsLayout L = gnn::ws_layout(g, s);
   if (ws_bytes < L.bwd_total) return GNN_ERR_WORKSPACE_TOO_SMALL;
   if (!ws || !aligned(ws, 256)) return GNN_ERR_INVALID_ARG;
+  // both calls keep the per-node scores at the same offset of ws
+  if (reuse_scores && L.fwd_scores != L.bwd_scores) return GNN_ERR_INVALID_ARG;
   return from_cuda(gnn::launch_backward(g, s, dtype, h, a_src, a_dst, slope, lse, dout, dh,
                                         da_src, da_dst, static_cast<char*>(ws), L,
                                         static_cast<cudaStream_t>(stream),
-                                        reinterpret_cast<const cudaEvent_t*>(events)));
+                                        reinterpret_cast<const cudaEvent_t*>(events),
+                                        reuse_scores));
+}
+
+}  // namespace
+
+extern "C" {
+
+gnn_status gat_agg_backward_timed(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                                  const void* h, const float* a_src, const float* a_dst,
+                                  float slope, const float* lse, const void* dout, void* dh,
+                                  float* da_src, float* da_dst, void* ws, size_t ws_bytes,
+                                  void* stream, void* const* events, int n_events) {
+  return backward_call(g, H, D, dtype, h, a_src, a_dst, slope, lse, dout, dh, da_src, da_dst,
+                       ws, ws_bytes, stream, events, n_events, false);
+}
+
+gnn_status gat_agg_backward_reuse(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                                  const void* h, const float* a_src, const float* a_dst,
+                                  float slope, const float* lse, const void* dout, void* dh,
+                                  float* da_src, float* da_dst, void* ws, size_t ws_bytes,
+                                  void* stream, void* const* events, int n_events) {
+  return backward_call(g, H, D, dtype, h, a_src, a_dst, slope, lse, dout, dh, da_src, da_dst,
+                       ws, ws_bytes, stream, events, n_events, true);
 }
 
 gnn_status gat_agg_backward(const gnn_graph* g, int H, int D, gnn_dtype dtype, const void* h,

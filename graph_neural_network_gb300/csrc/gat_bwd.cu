@@ -717,7 +717,7 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 template <typename T, int NV>
 cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t st,
-                     const cudaEvent_t* ev) {
+                     const cudaEvent_t* ev, bool reuse_scores) {
   constexpr int V = VecOf<T>::n;
   const int H = A.s.H, row_f = A.s.rv * V;
   cudaError_t e;
@@ -729,7 +729,9 @@ cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t 
   // rows of more than 512 bytes always fill the warp)
   const bool sub = NV == 1 && A.s.lpr < 32;
   mark(0);
-  if ((e = launch_node_scores(A.s, dt, A.h, A.a_src, A.a_dst, A.n, const_cast<float*>(A.ssrc),
+  // the forward call left the same scores at the same place in ws
+  if (!reuse_scores &&
+      (e = launch_node_scores(A.s, dt, A.h, A.a_src, A.a_dst, A.n, const_cast<float*>(A.ssrc),
                               const_cast<float*>(A.sdst), sm_count, st)) != cudaSuccess)
     return e;
   mark(1);
@@ -806,7 +808,7 @@ cudaError_t launch_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt, co
                             const float* a_src, const float* a_dst, float slope,
                             const float* lse, const void* dout, void* dh, float* da_src,
                             float* da_dst, char* ws, const WsLayout& L, cudaStream_t st,
-                            const cudaEvent_t* ev) {
+                            const cudaEvent_t* ev, bool reuse_scores) {
   BwdArgs A{};
   A.s = s;
   A.csr = dir_args(g->csr);
@@ -834,15 +836,15 @@ cudaError_t launch_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt, co
   A.err = g->err;
   if (dt == GNN_F32) {
     switch (s.nv) {
-      case 1: return launch_t<float, 1>(A, dt, g->sm_count, st, ev);
-      case 2: return launch_t<float, 2>(A, dt, g->sm_count, st, ev);
-      case 4: return launch_t<float, 4>(A, dt, g->sm_count, st, ev);
+      case 1: return launch_t<float, 1>(A, dt, g->sm_count, st, ev, reuse_scores);
+      case 2: return launch_t<float, 2>(A, dt, g->sm_count, st, ev, reuse_scores);
+      case 4: return launch_t<float, 4>(A, dt, g->sm_count, st, ev, reuse_scores);
     }
   } else {
     switch (s.nv) {
-      case 1: return launch_t<__nv_bfloat16, 1>(A, dt, g->sm_count, st, ev);
-      case 2: return launch_t<__nv_bfloat16, 2>(A, dt, g->sm_count, st, ev);
-      case 4: return launch_t<__nv_bfloat16, 4>(A, dt, g->sm_count, st, ev);
+      case 1: return launch_t<__nv_bfloat16, 1>(A, dt, g->sm_count, st, ev, reuse_scores);
+      case 2: return launch_t<__nv_bfloat16, 2>(A, dt, g->sm_count, st, ev, reuse_scores);
+      case 4: return launch_t<__nv_bfloat16, 4>(A, dt, g->sm_count, st, ev, reuse_scores);
     }
   }
   return cudaErrorInvalidValue;

@@ -81,7 +81,7 @@ cudaError_t launch_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt, co
                             const float* a_src, const float* a_dst, float slope,
                             const float* lse, const void* dout, void* dh, float* da_src,
                             float* da_dst, char* ws, const WsLayout& L, cudaStream_t st,
-                            const cudaEvent_t* ev);
+                            const cudaEvent_t* ev, bool reuse_scores);
 
 // Per-node base-2 score halves s_src, s_dst [N][H] (scores.cu).
 cudaError_t launch_node_scores(const Shape& s, gnn_dtype dt, const void* h, const float* a_src,

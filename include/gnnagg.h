@@ -180,6 +180,21 @@ gnn_status gat_agg_backward_timed(const gnn_graph* g, int H, int D, gnn_dtype dt
                                   float* da_src, float* da_dst, void* ws, size_t ws_bytes,
                                   void* stream, void* const* events, int n_events);
 
+/* gat_agg_backward_timed (events may be NULL) that reuses the per-node score
+ * halves a_src . h_n and a_dst . h_n which gat_agg_forward computed into its
+ * workspace, instead of computing them again: ws must be the workspace of
+ * the forward call on the same h, a_src and a_dst, with nothing written to
+ * it since (a training step that passes one workspace to both calls; the
+ * caller vouches for that, the library cannot check it).  The page's
+ * backward keeps compact per-node statistics from the forward pass; these
+ * are two more of them.  Results are bitwise those of gat_agg_backward; the
+ * score pre-pass interval of the events is empty. */
+gnn_status gat_agg_backward_reuse(const gnn_graph* g, int H, int D, gnn_dtype dtype,
+                                  const void* h, const float* a_src, const float* a_dst,
+                                  float slope, const float* lse, const void* dout, void* dh,
+                                  float* da_src, float* da_dst, void* ws, size_t ws_bytes,
+                                  void* stream, void* const* events, int n_events);
+
 /* Forward pass that allocates nothing and takes no workspace.  The page has
  * no counterpart to this call; it exists for callers that must not allocate
  * device memory -- for example code that runs under another framework's

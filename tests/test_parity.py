@@ -6,7 +6,7 @@ import torch
 
 import workload
 from workload import testgraphs
-from gpu_util import compare, make_case, run_gpu, run_oracle, to_device, assert_close
+from gpu_util import assert_close, compare, device_graph, make_case, run_gpu, run_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -111,6 +111,24 @@ def test_side_stream_matches_default_stream():
         b = run_gpu(case, (8, 64, 16), stream=s)
     for k in ("out", "lse", "dh", "da_src", "da_dst"):
         assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_backward_reusing_the_forward_scores_is_bitwise_the_same(dtype):
+    import graph_neural_network_gb300 as gnn
+    rp, ci = testgraphs.with_in_degrees(THRESHOLD_DEGREES, n_nodes=2000, seed=47)
+    D = 32 if dtype == "f32" else 64
+    case = make_case(rp, ci, 2, D, dtype, 47)
+    g = device_graph(case, (8, 64, 16))
+    h, dout = to_device(case["h"], dtype), to_device(case["dout"], dtype)
+    a_s = torch.from_numpy(case["a_src"]).cuda()
+    a_d = torch.from_numpy(case["a_dst"]).cuda()
+    ws = g.workspace(2, D, h.dtype)
+    out, lse = gnn.gat_forward(g, h, a_s, a_d, 0.2, ws=ws)
+    ref = gnn.gat_backward(g, h, a_s, a_d, 0.2, lse, dout)  # its own workspace
+    got = gnn.gat_backward(g, h, a_s, a_d, 0.2, lse, dout, ws=ws, reuse_scores=True)
+    for name, a, b in zip(("dh", "da_src", "da_dst"), ref, got):
+        assert torch.equal(a, b), name
 
 
 def test_autograd_function():
