@@ -46,3 +46,13 @@ def test_traffic_records_name_existing_sources():
             got = bench.measured_traffic(wl, k)
             current = bench.source_hash([os.path.join(ROOT, p) for p in entry["sources"]])
             assert got == (entry["bytes_per_launch"] if current == entry["source_hash"] else None)
+
+
+def test_oracle_sample_rate_stays_within_its_budget():
+    import time
+    w, rp, ci, h, a_s, a_d, dout = bench.load_workload(1)   # the 512-node graph
+    t0 = time.perf_counter()
+    rate, sample = bench.oracle_sample_rate(w, rp, ci, h, a_s, a_d, dout, budget_s=0.5,
+                                            max_reps=5)
+    assert time.perf_counter() - t0 < 5.0
+    assert rate > 0 and "100.0% of E" in sample and "run(s)" in sample
