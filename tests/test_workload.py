@@ -97,3 +97,20 @@ def test_features_shapes(idx):
     h, a_s, a_d, dout = workload.make_features(w, 100)
     assert h.shape == (100, w.H, w.D) and dout.shape == h.shape
     assert a_s.shape == (w.H, w.D) and a_d.shape == (w.H, w.D)
+
+
+def test_hubs_then_rcm_order():
+    rp, ci = workload.chung_lu(5_000, 2.1, 12.0, 1_500.0, 3)
+    n = len(rp) - 1
+    deg = np.diff(rp.astype(np.int64)) + np.bincount(ci, minlength=n)
+    new_id = workload.hubs_then_rcm_order(rp, ci, 200)
+    assert np.array_equal(np.sort(new_id), np.arange(n))       # a permutation
+    order = np.argsort(new_id)                                  # old id by new id
+    n_hub = int((deg > 200).sum())
+    assert n_hub > 0
+    assert np.all(deg[order[:n_hub]] > 200) and np.all(deg[order[n_hub:]] <= 200)
+    assert np.all(np.diff(deg[order[:n_hub]]) <= 0)             # descending degree
+    rcm = workload.rcm_order(rp, ci)
+    assert np.all(np.diff(rcm[order[n_hub:]]) > 0)              # the rest keep RCM order
+    rp2, ci2 = workload.relabel(rp, ci, new_id)
+    assert len(ci2) == len(ci)

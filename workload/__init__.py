@@ -138,6 +138,23 @@ def rcm_order(row_ptr, col) -> np.ndarray:
         lib.gen_graph_free(h)
 
 
+def hubs_then_rcm_order(row_ptr, col, min_degree: int) -> np.ndarray:
+    """new_id[v]: the nodes of in- plus out-degree above min_degree first, by
+    descending degree (ties by id), then every other node in reverse
+    Cuthill-McKee order.  The alternative reading of "degree-sorted + RCM"."""
+    n = len(row_ptr) - 1
+    deg = np.diff(np.asarray(row_ptr, np.int64)) + np.bincount(np.asarray(col), minlength=n)
+    rcm = rcm_order(row_ptr, col)
+    hubs = np.flatnonzero(deg > min_degree)
+    hubs = hubs[np.lexsort((hubs, -deg[hubs]))]
+    rest = np.flatnonzero(deg <= min_degree)
+    rest = rest[np.argsort(rcm[rest], kind="stable")]
+    order = np.concatenate([hubs, rest])  # order[k]: the node that gets id k
+    new_id = np.empty(n, dtype=np.int32)
+    new_id[order] = np.arange(n, dtype=np.int32)
+    return new_id
+
+
 def relabel(row_ptr, col, new_id):
     lib = _load()
     h = _wrap(row_ptr, col)

@@ -28,7 +28,7 @@ class Workload:
     D: int = 16
     dtype: str = "f32"        # f32 | bf16
     slope: float = 0.2
-    order: str = "natural"    # natural | random | rcm
+    order: str = "natural"    # natural | random | rcm | hubs_rcm
 
     @property
     def seed(self) -> int:
@@ -49,12 +49,21 @@ CONFIGS = {
     6: Workload(5, "rmat_s22_ef32_h4d64_bf16_rcm", "rmat",
                 dict(scale=22, ef=32, a=0.57, b=0.19, c=0.19), H=4, D=64, dtype="bf16",
                 order="rcm"),
+    # the alternative reading of the reordered run: hubs first, then RCM
+    7: Workload(5, "rmat_s22_ef32_h4d64_bf16_hubs_rcm", "rmat",
+                dict(scale=22, ef=32, a=0.57, b=0.19, c=0.19), H=4, D=64, dtype="bf16",
+                order="hubs_rcm"),
 }
+
+# nodes above this in- plus out-degree lead the hubs-first order (the
+# default tiling's largest in-degree handled by one thread block)
+HUB_DEGREE = 4096
 
 
 def make_graph(w: Workload):
     """CSR (row_ptr, col_idx) of a workload, deterministic in its seed."""
-    from . import erdos_renyi, uniform, chung_lu, rmat, permute_random, rcm_order, relabel
+    from . import (erdos_renyi, uniform, chung_lu, rmat, permute_random, rcm_order, relabel,
+                   hubs_then_rcm_order)
     p = w.params
     if w.kind == "er":
         g = erdos_renyi(p["n"], p["avg"], w.seed)
@@ -66,10 +75,12 @@ def make_graph(w: Workload):
         g = rmat(p["scale"], p["ef"], p["a"], p["b"], p["c"], w.seed)
     else:
         raise ValueError(w.kind)
-    if w.order in ("random", "rcm"):
+    if w.order in ("random", "rcm", "hubs_rcm"):
         g = permute_random(g[0], g[1], w.seed)
     if w.order == "rcm":
         g = relabel(g[0], g[1], rcm_order(g[0], g[1]))
+    if w.order == "hubs_rcm":
+        g = relabel(g[0], g[1], hubs_then_rcm_order(g[0], g[1], HUB_DEGREE))
     return g
 
 
