@@ -553,7 +553,9 @@ def run_gnnagg(args, rank, world):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            # arithmetic type: every kernel accumulates in float32 (bf16 rows are
+            # widened as they are loaded); the storage type is config.feature_dtype
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "n_nodes": n, "n_edges": e, "H": H, "D": D,
                        "feature_dtype": w.dtype,
                        "max_in_degree": st["csr"]["max_deg"],
@@ -876,7 +878,7 @@ def run_layer(args, rank, world):
             "bwd_ms": t_b, "ms_per_step_median": median,
             "warm": {"ms_per_step": warm_ms, "value": job_rate(units, world, warm_ms),
                      "steps": Kw, "l2": "not flushed between steps"},
-            "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
+            "higher_is_better": True, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "n_nodes": n, "n_edges": e, "F": F,
                        "feature_dtype": w.dtype,
                        "l2": flush.describe()},
