@@ -10,10 +10,14 @@ N = 100,000, every in-degree 16 plus a self-loop, H = 4, D = 32, float32.
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
 
 Prints one JSON line on rank 0.  `value` is forward+backward throughput in
-GEdge*head/s (E * H / step time, E counting self-loops); the forward-only
-figure, per-kernel times, the HBM roofline of the dominant kernel, an
-end-to-end figure through the public API with host buffers, the oracle's CPU
-throughput and the SM clocks seen during the timed region ride along.
+GEdge*head/s (E * H / step time, E counting self-loops); a step passes one
+workspace to both calls, so the backward reuses the forward's per-node
+scores.  The forward-only figure, per-kernel times (from a separate
+instrumented pass), the HBM roofline of the dominant kernel with its ncu DRAM
+traffic, an end-to-end figure through the public API with host buffers and
+the host link's measured rates, warm-L2 and CUDA-graph figures, the memory
+split, the oracle's CPU throughput and the SM clocks seen during the timed
+region ride along.
 Under torchrun each rank runs an independent replica of the workload (the
 operation has no exchange step on one graph); the max time over ranks is
 used and `value` sums the replicas' units.
