@@ -3,8 +3,10 @@
 
 One step = one forward and one backward pass over one synthetic graph whose
 inputs are resident in device memory (the graph is prepared once, outside the
-timed region, as in training).  Default workload: uniform random graph,
-N = 100,000, every in-degree 16 plus a self-loop, H = 4, D = 32, float32.
+timed region, as in training).  Default workload: the largest one, an R-MAT
+graph of scale 22 (4,194,304 nodes, edge factor 32, about 132.5M edges after
+duplicates are dropped and self-loops added) with random node ids, H = 4,
+D = 64, bfloat16 features accumulated in float32.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
@@ -12,12 +14,14 @@ N = 100,000, every in-degree 16 plus a self-loop, H = 4, D = 32, float32.
 Prints one JSON line on rank 0.  `value` is forward+backward throughput in
 GEdge*head/s (E * H / step time, E counting self-loops); a step passes one
 workspace to both calls, so the backward reuses the forward's per-node
-scores.  The forward-only figure, per-kernel times (from a separate
-instrumented pass), the HBM roofline of the dominant kernel with its ncu DRAM
-traffic, an end-to-end figure through the public API with host buffers and
-the host link's measured rates, warm-L2 and CUDA-graph figures, the memory
-split, the oracle's CPU throughput and the SM clocks seen during the timed
-region ride along.
+scores.  The forward-only figure, the forward and backward call fractions of
+the HBM roofline, per-kernel times (from a separate instrumented pass), the
+HBM roofline of the dominant kernel with its ncu DRAM traffic, an end-to-end
+figure through the public API with host buffers and the host link's measured
+rates, warm-L2 and CUDA-graph figures, the memory split, the oracle's CPU
+throughput and the SM clocks seen during the timed region ride along.  On the
+default workload a `power_law` list adds a compact line for each of the two
+Chung-Lu graphs and the reordered R-MAT graph.
 Under torchrun each rank runs an independent replica of the workload (the
 operation has no exchange step on one graph); the max time over ranks is
 used and `value` sums the replicas' units.
@@ -42,7 +46,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GEdge·head/s fwd and fwd+bwd GAT aggregation; achieved HBM GB/s vs roofline"
 UNIT = "GEdge*head/s"
-DEFAULT_CONFIG = 2
+DEFAULT_CONFIG = 5
+# compact lines beside the default: both Chung-Lu graphs and R-MAT in RCM order
+SUB_CONFIGS = (3, 4, 6)
 FWD_EVENTS, BWD_EVENTS = 4, 8
 FWD_KERNELS = ["fwd_scores", "fwd_main", "fwd_merge"]
 BWD_KERNELS = ["bwd_scores", "bwd_dst_main", "bwd_dst_merge", "bwd_src_main", "bwd_src_merge",
@@ -52,7 +58,7 @@ BWD_KERNELS = ["bwd_scores", "bwd_dst_main", "bwd_dst_merge", "bwd_src_main", "b
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     p.add_argument("--impl", choices=["gnnagg", "reference"], default="gnnagg")
@@ -66,6 +72,13 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=12.0,
                    help="CPU seconds for the oracle baseline sample")
+    p.add_argument("--no-sub", action="store_true",
+                   help="skip the compact lines of the other power-law workloads")
+    p.add_argument("--sub", default=None,
+                   help="comma-separated workload indices for the compact lines "
+                        "(default: 3,4,6 with the default workload, none otherwise)")
+    p.add_argument("--sub-steps", type=int, default=10,
+                   help="timed steps of each compact line")
     return p.parse_args(argv)
 
 
@@ -93,6 +106,21 @@ def algorithmic_bytes(n, e, H, D, s):
         "bwd_src_main": idx + gath + 2 * row,
         "stats_bytes": 16 * e * H,
     }
+
+
+def workload_config(w, rp, ci, world):
+    """The `config` object of the JSON line, the same for both arms: the
+    workload's name and sizes, its degree extremes and the L2 protocol."""
+    n, e = len(rp) - 1, len(ci)
+    s = 4 if w.dtype == "f32" else 2
+    feat_mb = n * w.H * w.D * s / 1e6
+    return {"workload": w.name, "n_nodes": n, "n_edges": e, "H": w.H, "D": w.D,
+            "feature_dtype": w.dtype,
+            "max_in_degree": int(np.diff(rp).max(initial=0)),
+            "max_out_degree": int(np.bincount(ci, minlength=n).max(initial=0)) if e else 0,
+            "l2": f"flushed before every timed GPU step (a write of twice the L2 size); "
+                  f"feature matrix {feat_mb:.0f} MB",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 # ---- clocks during the timed region ------------------------------------------------
@@ -161,6 +189,13 @@ def load_workload(idx):
     return w, rp, ci, h, a_s, a_d, dout
 
 
+# what the oracle's threads run: the forward and the destination side of the
+# backward are split over nodes; the source-side scatter of the backward runs
+# on one thread in edge order (deterministic by construction)
+ORACLE_THREADS = ("forward and backward destination side on all threads (OpenMP over "
+                  "nodes); backward source-side scatter on one thread")
+
+
 def cpu_sample(rp, ci, frac_edges):
     """The subgraph of the first m destination rows (all N nodes kept), with
     about frac_edges of the edges: a prefix of the CSR."""
@@ -196,7 +231,7 @@ def oracle_sample_rate(w, rp, ci, h, a_s, a_d, dout, budget_s, max_reps=10):
         reps += 1
     sample = (f"destinations 0..{m - 1} of {len(rp) - 1} with their {len(sci)} in-edges "
               f"({100.0 * len(sci) / len(ci):.1f}% of E), all N nodes; fp64 forward + "
-              f"backward, {reps} run(s), {t:.2f} s")
+              f"backward, {reps} run(s), {t:.2f} s; {ORACLE_THREADS}")
     return len(sci) * w.H * reps / t / 1e9, sample
 
 
@@ -239,13 +274,12 @@ def run_reference(args, rank, world):
     units = len(sci) * w.H
     value = units * args.steps / t / 1e9
     sample = (f"destinations 0..{m - 1} of {len(rp) - 1} with their {len(sci)} in-edges "
-              f"({100.0 * len(sci) / len(ci):.1f}% of E) per step, all N nodes")
+              f"({100.0 * len(sci) / len(ci):.1f}% of E) per step, all N nodes; {ORACLE_THREADS}")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "n_nodes": len(rp) - 1, "n_edges": len(ci),
-                       "H": w.H, "D": w.D},
+            "config": workload_config(w, rp, ci, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
                              "cores": oracle.num_threads(), "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -337,6 +371,206 @@ def job_rate(units_per_rank, world, ms):
     return world * units_per_rank / (ms * 1e-3) / 1e9
 
 
+class GatSession:
+    """One workload on the device: inputs resident, graph prepared once, outputs
+    and one workspace shared by the forward and the backward call of a step."""
+
+    def __init__(self, idx, dev):
+        import torch
+        import graph_neural_network_gb300 as gnn
+        from graph_neural_network_gb300 import _native
+        self.torch, self.gnn, self.native = torch, gnn, _native
+        self.dev = dev
+        w, rp, ci, h_np, a_s_np, a_d_np, dout_np = load_workload(idx)
+        self.w, self.rp, self.ci = w, rp, ci
+        self.host = (h_np, a_s_np, a_d_np, dout_np)
+        self.n, self.e, self.H, self.D = len(rp) - 1, len(ci), w.H, w.D
+        self.s = 4 if w.dtype == "f32" else 2
+        self.tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+
+        def dev_feat(x):
+            x = np.ascontiguousarray(x)
+            t = torch.from_numpy(x.view(np.int16) if w.dtype == "bf16" else x).to(dev)
+            return t.view(torch.bfloat16) if w.dtype == "bf16" else t
+
+        self.rp_d = torch.from_numpy(rp).to(dev)
+        self.ci_d = torch.from_numpy(ci).to(dev)
+        self.h = dev_feat(h_np)
+        self.dout = dev_feat(dout_np)
+        self.a_s = torch.from_numpy(a_s_np).to(dev)
+        self.a_d = torch.from_numpy(a_d_np).to(dev)
+
+    def prepare(self):
+        torch, gnn = self.torch, self.gnn
+        n, H, D, dev = self.n, self.H, self.D, self.dev
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        self.g = gnn.Graph(self.rp_d, self.ci_d)
+        self.prepare_ms = 1e3 * (time.perf_counter() - t0)
+        self.st = self.g.stats()
+        self.out = torch.empty_like(self.h)
+        self.lse = torch.empty((n, H), dtype=torch.float32, device=dev)
+        self.dh = torch.empty_like(self.h)
+        self.da_s = torch.empty((H, D), dtype=torch.float32, device=dev)
+        self.da_d = torch.empty((H, D), dtype=torch.float32, device=dev)
+        self.ws = self.g.workspace(H, D, self.tdt)
+        self.lib = self.native.load()
+        self.dt_code = self.native.F32 if self.w.dtype == "f32" else self.native.BF16
+        self.stream = torch.cuda.current_stream(dev)
+        self.sp = ctypes.c_void_p(self.stream.cuda_stream)
+
+    @staticmethod
+    def ptr(t):
+        return ctypes.c_void_p(t.data_ptr())
+
+    def fwd(self, fe=None, sp=None):
+        p = self.ptr
+        rc = self.lib.gat_agg_forward_timed(
+            self.g.handle, self.H, self.D, self.dt_code, p(self.h), p(self.a_s), p(self.a_d),
+            self.w.slope, p(self.out), p(self.lse), p(self.ws), self.ws.numel(),
+            sp if sp is not None else self.sp, fe, FWD_EVENTS if fe is not None else 0)
+        self.native.check(rc, "forward")
+
+    # a step passes one workspace to both calls, so the backward takes the
+    # per-node scores the forward left there
+    def bwd(self, be=None, sp=None):
+        p = self.ptr
+        rc = self.lib.gat_agg_backward_reuse(
+            self.g.handle, self.H, self.D, self.dt_code, p(self.h), p(self.a_s), p(self.a_d),
+            self.w.slope, p(self.lse), p(self.dout), p(self.dh), p(self.da_s), p(self.da_d),
+            p(self.ws), self.ws.numel(), sp if sp is not None else self.sp, be,
+            BWD_EVENTS if be is not None else 0)
+        self.native.check(rc, "backward")
+
+    def step(self, fe=None, be=None, sp=None):
+        self.fwd(fe, sp)
+        self.bwd(be, sp)
+
+    def check(self):
+        self.torch.cuda.synchronize()
+        self.gnn.check_device_error(self.g)
+
+    def timed_steps(self, K, flush):
+        """K flushed steps with three events each (start, between the calls,
+        end): mean forward and backward ms and the per-step totals."""
+        torch = self.torch
+        tev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for k in range(K):
+            flush()  # outside the timed events
+            tev[k][0].record(self.stream)
+            self.fwd()
+            tev[k][1].record(self.stream)
+            self.bwd()
+            tev[k][2].record(self.stream)
+        torch.cuda.synchronize()
+        tf = [a.elapsed_time(b) for a, b, _ in tev]
+        tb = [b.elapsed_time(c) for _, b, c in tev]
+        return sum(tf) / K, sum(tb) / K, [x + y for x, y in zip(tf, tb)]
+
+    def kernel_times(self, K, flush):
+        """Mean per-kernel ms over K flushed steps run through the timed API,
+        whose caller events sit between the kernels."""
+        torch = self.torch
+
+        def make_events(k):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+            for ev in evs:
+                ev.record(self.stream)  # creates the underlying event
+            arr = (ctypes.c_void_p * k)(*[ev.cuda_event for ev in evs])
+            return evs, arr
+
+        fev = [make_events(FWD_EVENTS) for _ in range(K)]
+        bev = [make_events(BWD_EVENTS) for _ in range(K)]
+        for k in range(K):
+            flush()
+            self.step(fev[k][1], bev[k][1])
+        self.check()
+        kern = {name: 0.0 for name in FWD_KERNELS + BWD_KERNELS}
+        for k in range(K):
+            fe, be = fev[k][0], bev[k][0]
+            for i, name in enumerate(FWD_KERNELS):
+                kern[name] += fe[i].elapsed_time(fe[i + 1])
+            for i, name in enumerate(BWD_KERNELS):
+                kern[name] += be[i].elapsed_time(be[i + 1])
+        return {k: v / K for k, v in kern.items()}
+
+    def pass_fracs(self, t_fwd, t_bwd, peak):
+        """Forward and backward call roofline fractions: the algorithmic bytes
+        of the call's kernels (forward: score pre-pass + main kernel; backward:
+        both main passes) over the call's event time."""
+        ab = algorithmic_bytes(self.n, self.e, self.H, self.D, self.s)
+        b_fwd = ab["scores"] + ab["fwd_main"]
+        b_bwd = ab["bwd_dst_main"] + ab["bwd_src_main"]
+        return (b_fwd / (t_fwd * 1e-3) / 1e9 / peak, b_bwd / (t_bwd * 1e-3) / 1e9 / peak,
+                b_fwd, b_bwd)
+
+    def kernel_fracs(self, kern, peak):
+        ab = algorithmic_bytes(self.n, self.e, self.H, self.D, self.s)
+        fr = {k: ab[k] / (kern[k] * 1e-3) / 1e9 / peak
+              for k in ("fwd_main", "bwd_dst_main", "bwd_src_main") if kern[k] > 0}
+        if kern["fwd_scores"] > 0:  # the backward reuses these scores: no bwd_scores kernel
+            fr["fwd_scores"] = ab["scores"] / (kern["fwd_scores"] * 1e-3) / 1e9 / peak
+        return fr
+
+    def dram(self, kern, peak):
+        """Real DRAM rate of each main kernel from its committed ncu record
+        (bytes per launch over its event time), where the record matches the
+        kernel sources."""
+        res = {}
+        for k in ("fwd_main", "bwd_dst_main", "bwd_src_main"):
+            rec = measured_entry(self.w.name, k)
+            if rec and kern[k] > 0:
+                gbs = rec["bytes_per_launch"] / (kern[k] * 1e-3) / 1e9
+                res[k] = {"traffic": rec["bytes_per_launch"], "dram_gbs": gbs,
+                          "dram_frac": gbs / peak, "l2_hit_pct": rec.get("l2_hit_pct")}
+        return res
+
+    def launches_per_step(self):
+        st = self.st
+        # forward: scores, main, hub merge; backward (scores reused): two main
+        # kernels and their hub merges, two attention-gradient kernels
+        return (2 + (st["csr"]["hubs"] > 0)) + (1 + (st["csr"]["hubs"] > 0)) + \
+            (1 + (st["csc"]["hubs"] > 0)) + 2
+
+    def release(self):
+        for name in ("g", "out", "lse", "dh", "da_s", "da_d", "ws", "h", "dout", "a_s", "a_d",
+                     "rp_d", "ci_d"):
+            if hasattr(self, name):
+                delattr(self, name)
+        self.torch.cuda.synchronize()
+        self.torch.cuda.empty_cache()
+
+
+def power_law_line(idx, dev, flush, steps, warmup, peak):
+    """A compact figure of one more workload: K flushed steps, the per-kernel
+    times, and the forward / backward call roofline fractions."""
+    S = GatSession(idx, dev)
+    S.prepare()
+    for _ in range(max(3, warmup)):
+        flush()
+        S.step()
+    S.check()
+    t_fwd, t_bwd, per_step = S.timed_steps(steps, flush)
+    S.check()
+    kern = S.kernel_times(min(steps, 10), flush)
+    ffr, bfr, b_fwd, b_bwd = S.pass_fracs(t_fwd, t_bwd, peak)
+    units = S.e * S.H
+    res = {"workload": S.w.name, "n_nodes": S.n, "n_edges": S.e, "H": S.H, "D": S.D,
+           "feature_dtype": S.w.dtype, "steps": steps,
+           "value": units / ((t_fwd + t_bwd) * 1e-3) / 1e9, "fwd_value": units / (t_fwd * 1e-3) / 1e9,
+           "ms_per_step": t_fwd + t_bwd, "ms_per_step_median": float(np.median(per_step)),
+           "fwd_ms": t_fwd, "bwd_ms": t_bwd, "fwd_frac": ffr, "bwd_frac": bfr,
+           "algorithmic_bytes_fwd": b_fwd, "algorithmic_bytes_bwd": b_bwd,
+           "kernels_ms": {k: kern[k] for k in ("fwd_scores", "fwd_main", "bwd_dst_main",
+                                                 "bwd_src_main")},
+           "kernel_hbm_frac": S.kernel_fracs(kern, peak), "prepare_ms": S.prepare_ms}
+    dram = S.dram(kern, peak)
+    if dram:
+        res["dram"] = dram
+    S.release()
+    return res
+
+
 def run_gnnagg(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -345,85 +579,25 @@ def run_gnnagg(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    w, rp, ci, h_np, a_s_np, a_d_np, dout_np = load_workload(args.config)
-    n, e, H, D = len(rp) - 1, len(ci), w.H, w.D
-    s = 4 if w.dtype == "f32" else 2
-    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
-
-    def dev_feat(x):
-        x = np.ascontiguousarray(x)
-        t = torch.from_numpy(x.view(np.int16) if w.dtype == "bf16" else x)
-        t = t.to(dev)
-        return t.view(torch.bfloat16) if w.dtype == "bf16" else t
-
-    rp_d = torch.from_numpy(rp).to(dev)
-    ci_d = torch.from_numpy(ci).to(dev)
-    h = dev_feat(h_np)
-    dout = dev_feat(dout_np)
-    a_s = torch.from_numpy(a_s_np).to(dev)
-    a_d = torch.from_numpy(a_d_np).to(dev)
+    S = GatSession(args.config, dev)
+    w, n, e, H, D = S.w, S.n, S.e, S.H, S.D
     flush = L2Flush(dev)  # harness memory, not counted in peak_mem_gb
     torch.cuda.synchronize()
     torch.cuda.reset_peak_memory_stats(dev)
     mem0 = torch.cuda.memory_allocated(dev)
-    t0 = time.perf_counter()
-    g = gnn.Graph(rp_d, ci_d)
-    prepare_ms = 1e3 * (time.perf_counter() - t0)
-    st = g.stats()
-    out = torch.empty_like(h)
-    lse = torch.empty((n, H), dtype=torch.float32, device=dev)
-    dh = torch.empty_like(h)
-    da_s = torch.empty((H, D), dtype=torch.float32, device=dev)
-    da_d = torch.empty((H, D), dtype=torch.float32, device=dev)
-    ws = g.workspace(H, D, tdt)
-    lib = _native.load()
-    dt_code = _native.F32 if w.dtype == "f32" else _native.BF16
-    P = ctypes.c_void_p
-
-    def ptr(t):
-        return P(t.data_ptr())
-
-    stream = torch.cuda.current_stream(dev)
-    sp = P(stream.cuda_stream)
-
-    def make_events(k):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
-        for ev in evs:
-            ev.record(stream)  # creates the underlying event
-        arr = (ctypes.c_void_p * k)(*[ev.cuda_event for ev in evs])
-        return evs, arr
-
-    def fwd(fe=None):
-        rc = lib.gat_agg_forward_timed(g.handle, H, D, dt_code, ptr(h), ptr(a_s), ptr(a_d),
-                                       w.slope, ptr(out), ptr(lse), ptr(ws), ws.numel(), sp,
-                                       fe, FWD_EVENTS if fe is not None else 0)
-        _native.check(rc, "forward")
-
-    # a step passes one workspace to both calls, so the backward takes the
-    # per-node scores the forward left there
-    def bwd(be=None):
-        rc = lib.gat_agg_backward_reuse(g.handle, H, D, dt_code, ptr(h), ptr(a_s), ptr(a_d),
-                                        w.slope, ptr(lse), ptr(dout), ptr(dh), ptr(da_s),
-                                        ptr(da_d), ptr(ws), ws.numel(), sp,
-                                        be, BWD_EVENTS if be is not None else 0)
-        _native.check(rc, "backward")
-
-    def step(fe=None, be=None):
-        fwd(fe)
-        bwd(be)
+    S.prepare()
+    g, stream = S.g, S.stream
 
     for _ in range(max(3, args.warmup)):
         flush()
-        step()
-    torch.cuda.synchronize()
-    gnn.check_device_error(g)
+        S.step()
+    S.check()
     peak_mem = torch.cuda.max_memory_allocated(dev) - mem0
 
     # the timed steps carry three events each (start, between the calls, end);
     # the per-kernel events of the timed API go on a separate pass below, so
     # that their own recording gaps stay out of the step time
     K = args.steps
-    tev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     sampler = ClockSampler(visible.split(",")[dev.index].strip() if visible else dev.index)
     if world > 1:
@@ -432,47 +606,17 @@ def run_gnnagg(args, rank, world):
     sampler.start()
     time.sleep(0.2)
     wall0 = time.perf_counter()
-    for k in range(K):
-        flush()  # outside the timed events
-        tev[k][0].record(stream)
-        fwd()
-        tev[k][1].record(stream)
-        bwd()
-        tev[k][2].record(stream)
-    torch.cuda.synchronize()
+    t_fwd, t_bwd, per_step = S.timed_steps(K, flush)
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    gnn.check_device_error(g)
-
-    t_fwd = t_bwd = 0.0
-    per_step = []
-    for a, b, c in tev:
-        tf, tb = a.elapsed_time(b), b.elapsed_time(c)
-        t_fwd += tf
-        t_bwd += tb
-        per_step.append(tf + tb)
-    t_fwd /= K
-    t_bwd /= K
+    S.check()
 
     # per-kernel times: the same flushed steps again, with the timed API's
     # events between kernels
     Ki = min(K, 50)
-    fev = [make_events(FWD_EVENTS) for _ in range(Ki)]
-    bev = [make_events(BWD_EVENTS) for _ in range(Ki)]
-    for k in range(Ki):
-        flush()
-        step(fev[k][1], bev[k][1])
-    torch.cuda.synchronize()
-    gnn.check_device_error(g)
-    kern = {name: 0.0 for name in FWD_KERNELS + BWD_KERNELS}
-    for k in range(Ki):
-        fe, be = fev[k][0], bev[k][0]
-        for i, name in enumerate(FWD_KERNELS):
-            kern[name] += fe[i].elapsed_time(fe[i + 1])
-        for i, name in enumerate(BWD_KERNELS):
-            kern[name] += be[i].elapsed_time(be[i + 1])
+    kern = S.kernel_times(Ki, flush)
 
     # secondary figure: the same steps back to back with no flush (warm L2)
     Kw = min(K, 50)
@@ -480,35 +624,23 @@ def run_gnnagg(args, rank, world):
            for _ in range(Kw)]
     for a, b in wev:
         a.record(stream)
-        step()
+        S.step()
         b.record(stream)
-    torch.cuda.synchronize()
-    gnn.check_device_error(g)
+    S.check()
     (warm_ms,) = max_over_ranks([sum(a.elapsed_time(b) for a, b in wev) / Kw], world, dev)
 
     # secondary figure: the same flushed step replayed from a CUDA graph of
     # the two calls (no host launch path between kernels)
     gs = torch.cuda.Stream(dev)
-    spg = P(gs.cuda_stream)
-
-    def step_on(spx):
-        rc = lib.gat_agg_forward_timed(g.handle, H, D, dt_code, ptr(h), ptr(a_s), ptr(a_d),
-                                       w.slope, ptr(out), ptr(lse), ptr(ws), ws.numel(), spx,
-                                       None, 0)
-        _native.check(rc, "forward")
-        rc = lib.gat_agg_backward_reuse(g.handle, H, D, dt_code, ptr(h), ptr(a_s), ptr(a_d),
-                                        w.slope, ptr(lse), ptr(dout), ptr(dh), ptr(da_s),
-                                        ptr(da_d), ptr(ws), ws.numel(), spx, None, 0)
-        _native.check(rc, "backward")
-
+    spg = ctypes.c_void_p(gs.cuda_stream)
     gs.wait_stream(stream)
     with torch.cuda.stream(gs):
-        step_on(spg)  # a warm-up on the capture stream
+        S.step(sp=spg)  # a warm-up on the capture stream
     stream.wait_stream(gs)
     torch.cuda.synchronize()
     cg = torch.cuda.CUDAGraph()
     with torch.cuda.graph(cg, stream=gs):
-        step_on(spg)
+        S.step(sp=spg)
     Kg = min(K, 50)
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(Kg)]
@@ -517,82 +649,96 @@ def run_gnnagg(args, rank, world):
         a.record(stream)
         cg.replay()
         b.record(stream)
-    torch.cuda.synchronize()
-    gnn.check_device_error(g)
+    S.check()
     (graph_ms,) = max_over_ranks([sum(a.elapsed_time(b) for a, b in gev) / Kg], world, dev)
-    kern = {k: v / Ki for k, v in kern.items()}
-    ms_step, t_fwd = max_over_ranks([t_fwd + t_bwd, t_fwd], world, dev)
+    del cg
+    ms_step, t_fwd, t_bwd = max_over_ranks([t_fwd + t_bwd, t_fwd, t_bwd], world, dev)
     units = e * H
     value = job_rate(units, world, ms_step)
     fwd_value = job_rate(units, world, t_fwd)
 
     # roofline of the dominant kernel
-    ab = algorithmic_bytes(n, e, H, D, s)
+    ab = algorithmic_bytes(n, e, H, D, S.s)
     main = {k: kern[k] for k in ("fwd_main", "bwd_dst_main", "bwd_src_main")}
     dom = max(main, key=main.get)
     peak, peak_kind = peaks()
     achieved = ab[dom] / (kern[dom] * 1e-3) / 1e9
-    rec = measured_entry(w.name, dom)
-    traffic = rec["bytes_per_launch"] if rec else None
-    step_bytes = ab["fwd_main"] + ab["bwd_dst_main"] + ab["bwd_src_main"] + ab["scores"]
+    dram = S.dram(kern, peak)
+    rec = dram.get(dom)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                "unit": "GB/s", "frac": achieved / peak,
+                "traffic": rec["traffic"] if rec else None,
                 "algorithmic_bytes": ab[dom], "peak_source": peak_kind}
     if rec:
         # real DRAM rate of the same kernel: ncu bytes per launch over its event time
-        roofline["dram_gbs"] = traffic / (kern[dom] * 1e-3) / 1e9
-        roofline["dram_frac"] = roofline["dram_gbs"] / peak
-        if "l2_hit_pct" in rec:
+        roofline["dram_gbs"] = rec["dram_gbs"]
+        roofline["dram_frac"] = rec["dram_frac"]
+        if rec.get("l2_hit_pct") is not None:
             roofline["l2_hit_pct"] = rec["l2_hit_pct"]
+    step_bytes = ab["fwd_main"] + ab["bwd_dst_main"] + ab["bwd_src_main"] + ab["scores"]
+    ffr, bfr, _, _ = S.pass_fracs(t_fwd, t_bwd, peak)
     io_bytes = sum(t.numel() * t.element_size()
-                   for t in (rp_d, ci_d, h, dout, a_s, a_d, out, lse, dh, da_s, da_d))
-    kernel_frac = {k: ab[k] / (kern[k] * 1e-3) / 1e9 / peak for k in main if kern[k] > 0}
-    if kern["fwd_scores"] > 0:  # the backward reuses these scores: no bwd_scores kernel
-        kernel_frac["fwd_scores"] = ab["scores"] / (kern["fwd_scores"] * 1e-3) / 1e9 / peak
-
-    # forward: scores, main, hub merge; backward (scores reused): two main
-    # kernels and their hub merges, two attention-gradient kernels
-    launches_per_step = (2 + (st["csr"]["hubs"] > 0)) + (1 + (st["csr"]["hubs"] > 0)) + \
-        (1 + (st["csc"]["hubs"] > 0)) + 2
+                   for t in (S.rp_d, S.ci_d, S.h, S.dout, S.a_s, S.a_d, S.out, S.lse, S.dh,
+                             S.da_s, S.da_d))
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             # arithmetic type: every kernel accumulates in float32 (bf16 rows are
             # widened as they are loaded); the storage type is config.feature_dtype
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "n_nodes": n, "n_edges": e, "H": H, "D": D,
-                       "feature_dtype": w.dtype,
-                       "max_in_degree": st["csr"]["max_deg"],
-                       "max_out_degree": st["csc"]["max_deg"],
-                       "l2": flush.describe(),
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "config": workload_config(w, S.rp, S.ci, world),
             "fwd_value": fwd_value, "fwd_ms": t_fwd, "bwd_ms": t_bwd,
+            # call-level fractions of the HBM roofline (algorithmic bytes of the
+            # call's kernels over the call's event time, of the measured peak)
+            "fwd_frac": ffr, "bwd_frac": bfr,
             "ms_per_step_median": float(np.median(per_step)),
             "warm": {"ms_per_step": warm_ms, "value": job_rate(units, world, warm_ms),
                      "steps": Kw, "l2": "not flushed between steps"},
             "cuda_graph": {"ms_per_step": graph_ms, "value": job_rate(units, world, graph_ms),
                            "steps": Kg, "l2": "flushed before every step",
                            "what": "the forward and backward calls captured once, replayed"},
-            "kernels_ms": kern, "kernel_hbm_frac": kernel_frac,
+            "kernels_ms": kern, "kernel_hbm_frac": S.kernel_fracs(kern, peak),
             "roofline": roofline,
+            "dram": dram,
             "step_roofline": {"achieved": step_bytes / (ms_step * 1e-3) / 1e9, "peak": peak,
                               "unit": "GB/s", "frac": step_bytes / (ms_step * 1e-3) / 1e9 / peak},
-            "gpu_launches": launches_per_step * K,
-            "prepare_ms": prepare_ms, "peak_mem_gb": peak_mem / 1e9,
-            "memory_gb": {"graph_buffer": g.buffer.numel() / 1e9, "workspace": ws.numel() / 1e9,
+            "gpu_launches": S.launches_per_step() * K,
+            "prepare_ms": S.prepare_ms, "peak_mem_gb": peak_mem / 1e9,
+            "memory_gb": {"graph_buffer": g.buffer.numel() / 1e9, "workspace": S.ws.numel() / 1e9,
                           "inputs_outputs": io_bytes / 1e9,
-                          "peak_above_inputs": peak_mem / 1e9},
+                          "peak_above_inputs": peak_mem / 1e9,
+                          "not_counted": "the L2-flush buffer and the 16 MiB array of the "
+                                         "allocation-free forward (not loaded by this run)"},
+            "l2_flush": flush.describe(),
             "clocks": clocks, "wall_s": wall}
 
     if not args.no_e2e:
-        line["e2e"] = e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world,
-                          dev, units)
+        line["e2e"] = e2e(args, g, w, S.h, S.dout, S.a_s, S.a_d, S.out, S.lse, S.dh, S.da_s,
+                          S.da_d, S.ws, world, dev, units)
+    h_np, a_s_np, a_d_np, dout_np = S.host
+    rp, ci = S.rp, S.ci
+    S.release()
+    del S, g
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(w, rp, ci, h_np, a_s_np, a_d_np, dout_np,
                                                args.cpu_budget_s, one_core=args.config <= 2)
+    del h_np, a_s_np, a_d_np, dout_np
+    subs = sub_configs(args)
+    if subs:
+        # the other power-law workloads (and the reordered R-MAT run), compact
+        line["power_law"] = [power_law_line(i, dev, flush, args.sub_steps, 3, peak)
+                             for i in subs]
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def sub_configs(args):
+    if args.no_sub:
+        return []
+    if args.sub is not None:
+        return [int(x) for x in args.sub.split(",") if x.strip()]
+    return list(SUB_CONFIGS) if args.config == DEFAULT_CONFIG else []
 
 
 def e2e(args, g, w, h, dout, a_s, a_d, out, lse, dh, da_s, da_d, ws, world, dev, units):

@@ -154,11 +154,48 @@ class Graph:
         return torch.empty(n, dtype=torch.uint8, device=self.device)
 
 
+def _check_tensor(g: Graph, t, name: str, shape, dtype=None, floating=False):
+    """Raise before any pointer reaches the library unless t is a contiguous
+    tensor of the given shape (and dtype) on the graph's CUDA device."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if floating and not t.is_floating_point():
+        raise TypeError(f"{name} must be a floating-point tensor, got {t.dtype}")
+    if not t.is_cuda or t.device != g.device:
+        raise ValueError(f"{name} must be on the graph's device {g.device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
 def _check_features(g: Graph, x: torch.Tensor, name: str):
-    if x.dim() != 3 or x.shape[0] != g.n:
+    if not isinstance(x, torch.Tensor) or x.dim() != 3 or x.shape[0] != g.n:
         raise ValueError(f"{name} must be [N, H, D] with N = {g.n}")
-    if not x.is_cuda or not x.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    _dtype_code(x.dtype)
+    _check_tensor(g, x, name, None)
+
+
+def _att(g: Graph, a, name: str, H: int, D: int) -> torch.Tensor:
+    """An attention vector [H, D] on the graph's device, widened to float32."""
+    _check_tensor(g, a, name, (H, D), floating=True)
+    return a.to(torch.float32).contiguous()
+
+
+def _given(g: Graph, t, name: str, shape, dtype, make):
+    """A caller-supplied output (checked) or a new one."""
+    return make() if t is None else _check_tensor(g, t, name, shape, dtype)
+
+
+def _check_ws(g: Graph, ws):
+    if ws is not None:
+        _check_tensor(g, ws, "ws", None, torch.uint8)
+        if ws.dim() != 1:
+            raise ValueError("ws must be a one-dimensional uint8 tensor")
+    return ws
 
 
 def gat_forward(g: Graph, h: torch.Tensor, a_src: torch.Tensor, a_dst: torch.Tensor,
@@ -167,13 +204,12 @@ def gat_forward(g: Graph, h: torch.Tensor, a_src: torch.Tensor, a_dst: torch.Ten
     _check_features(g, h, "h")
     N, H, D = h.shape
     dt = _dtype_code(h.dtype)
-    a_src = a_src.to(torch.float32).contiguous()
-    a_dst = a_dst.to(torch.float32).contiguous()
-    if out is None:
-        out = torch.empty_like(h)
-    if lse is None:
-        lse = torch.empty((N, H), dtype=torch.float32, device=h.device)
-    if ws is None:
+    a_src = _att(g, a_src, "a_src", H, D)
+    a_dst = _att(g, a_dst, "a_dst", H, D)
+    out = _given(g, out, "out", h.shape, h.dtype, lambda: torch.empty_like(h))
+    lse = _given(g, lse, "lse", (N, H), torch.float32,
+                 lambda: torch.empty((N, H), dtype=torch.float32, device=h.device))
+    if _check_ws(g, ws) is None:
         ws = g.workspace(H, D, h.dtype)
     rc = g._lib.gat_agg_forward(g.handle, H, D, dt, _ptr(h), _ptr(a_src), _ptr(a_dst),
                                 float(slope), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
@@ -196,16 +232,15 @@ def gat_backward(g: Graph, h: torch.Tensor, a_src: torch.Tensor, a_dst: torch.Te
         raise TypeError("dout must have h's dtype")
     N, H, D = h.shape
     dt = _dtype_code(h.dtype)
-    a_src = a_src.to(torch.float32).contiguous()
-    a_dst = a_dst.to(torch.float32).contiguous()
-    lse = lse.contiguous()
-    if dh is None:
-        dh = torch.empty_like(h)
-    if da_src is None:
-        da_src = torch.empty((H, D), dtype=torch.float32, device=h.device)
-    if da_dst is None:
-        da_dst = torch.empty((H, D), dtype=torch.float32, device=h.device)
-    if ws is None:
+    a_src = _att(g, a_src, "a_src", H, D)
+    a_dst = _att(g, a_dst, "a_dst", H, D)
+    _check_tensor(g, lse, "lse", (N, H), torch.float32)
+    dh = _given(g, dh, "dh", h.shape, h.dtype, lambda: torch.empty_like(h))
+    da_src = _given(g, da_src, "da_src", (H, D), torch.float32,
+                    lambda: torch.empty((H, D), dtype=torch.float32, device=h.device))
+    da_dst = _given(g, da_dst, "da_dst", (H, D), torch.float32,
+                    lambda: torch.empty((H, D), dtype=torch.float32, device=h.device))
+    if _check_ws(g, ws) is None:
         if reuse_scores:
             raise ValueError("reuse_scores needs the forward call's workspace")
         ws = g.workspace(H, D, h.dtype)
@@ -223,26 +258,27 @@ def gat_backward(g: Graph, h: torch.Tensor, a_src: torch.Tensor, a_dst: torch.Te
 
 
 def _row_width(g: Graph, x: torch.Tensor, name: str) -> int:
-    if x.dim() < 2 or x.shape[0] != g.n or not x.is_cuda or not x.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous CUDA tensor [N, ...] with N = {g.n}")
+    if not isinstance(x, torch.Tensor) or x.dim() < 2 or x.shape[0] != g.n:
+        raise ValueError(f"{name} must be a tensor [N, ...] with N = {g.n}")
+    _check_tensor(g, x, name, None)
     F = 1
     for d in x.shape[1:]:
         F *= d
     return F
 
 
-def _gcn_call(fn, g, x, norm, out, ws, stream, what):
+def _gcn_call(fname, g, x, norm, out, ws, stream, what):
     F = _row_width(g, x, "features")
     dt = _dtype_code(x.dtype)
     if norm not in _native.NORMS:
         raise ValueError(f"norm must be one of {sorted(_native.NORMS)}")
-    if out is None:
-        out = torch.empty_like(x)
-    if ws is None:
+    out = _given(g, out, "out", x.shape, x.dtype, lambda: torch.empty_like(x))
+    if _check_ws(g, ws) is None:
         n = g._lib.gcn_agg_workspace_bytes(g.handle, F, dt)
         if n == 0:
             raise GnnError(_native.ERR_UNSUPPORTED, f"(F={F}, {x.dtype})")
         ws = torch.empty(n, dtype=torch.uint8, device=x.device)
+    fn = getattr(g._lib, fname)
     rc = fn(g.handle, F, dt, _native.NORMS[norm], _ptr(x), _ptr(out), _ptr(ws), ws.numel(),
             _stream(stream, x.device))
     _native.check(rc, what)
@@ -251,12 +287,12 @@ def _gcn_call(fn, g, x, norm, out, ws, stream, what):
 
 def gcn_forward(g: Graph, x: torch.Tensor, norm: str = "sym", out=None, ws=None, stream=None):
     """out = A~ x (x [N, ...] float32 or bfloat16, features flattened per node)."""
-    return _gcn_call(g._lib.gcn_agg_forward, g, x, norm, out, ws, stream, "gcn_agg_forward")
+    return _gcn_call("gcn_agg_forward", g, x, norm, out, ws, stream, "gcn_agg_forward")
 
 
 def gcn_backward(g: Graph, dout: torch.Tensor, norm: str = "sym", dx=None, ws=None, stream=None):
     """dx = A~^T dout."""
-    return _gcn_call(g._lib.gcn_agg_backward, g, dout, norm, dx, ws, stream, "gcn_agg_backward")
+    return _gcn_call("gcn_agg_backward", g, dout, norm, dx, ws, stream, "gcn_agg_backward")
 
 
 class GCNAggregate(torch.autograd.Function):
@@ -290,10 +326,11 @@ def gatv2_forward(g: Graph, xl: torch.Tensor, xr: torch.Tensor, att: torch.Tenso
     if xr.shape != xl.shape or xr.dtype != xl.dtype:
         raise ValueError("xr must match xl in shape and dtype")
     N, H, D = xl.shape
-    att = att.to(torch.float32).contiguous()
-    out = torch.empty_like(xl) if out is None else out
-    lse = torch.empty((N, H), dtype=torch.float32, device=xl.device) if lse is None else lse
-    ws = _gatv2_ws(g, H, D, xl.dtype, ws, xl.device)
+    att = _att(g, att, "att", H, D)
+    out = _given(g, out, "out", xl.shape, xl.dtype, lambda: torch.empty_like(xl))
+    lse = _given(g, lse, "lse", (N, H), torch.float32,
+                 lambda: torch.empty((N, H), dtype=torch.float32, device=xl.device))
+    ws = _gatv2_ws(g, H, D, xl.dtype, _check_ws(g, ws), xl.device)
     rc = g._lib.gatv2_agg_forward(g.handle, H, D, _dtype_code(xl.dtype), _ptr(xl), _ptr(xr),
                                   _ptr(att), float(slope), _ptr(out), _ptr(lse), _ptr(ws),
                                   ws.numel(), _stream(stream, xl.device))
@@ -311,13 +348,15 @@ def gatv2_backward(g: Graph, xl: torch.Tensor, xr: torch.Tensor, att: torch.Tens
     if xr.shape != xl.shape or dout.shape != xl.shape or dout.dtype != xl.dtype:
         raise ValueError("xr and dout must match xl")
     N, H, D = xl.shape
-    att = att.to(torch.float32).contiguous()
-    dxl = torch.empty_like(xl) if dxl is None else dxl
-    dxr = torch.empty_like(xl) if dxr is None else dxr
-    datt = torch.empty((H, D), dtype=torch.float32, device=xl.device) if datt is None else datt
-    ws = _gatv2_ws(g, H, D, xl.dtype, ws, xl.device)
+    att = _att(g, att, "att", H, D)
+    _check_tensor(g, lse, "lse", (N, H), torch.float32)
+    dxl = _given(g, dxl, "dxl", xl.shape, xl.dtype, lambda: torch.empty_like(xl))
+    dxr = _given(g, dxr, "dxr", xl.shape, xl.dtype, lambda: torch.empty_like(xl))
+    datt = _given(g, datt, "datt", (H, D), torch.float32,
+                  lambda: torch.empty((H, D), dtype=torch.float32, device=xl.device))
+    ws = _gatv2_ws(g, H, D, xl.dtype, _check_ws(g, ws), xl.device)
     rc = g._lib.gatv2_agg_backward(g.handle, H, D, _dtype_code(xl.dtype), _ptr(xl), _ptr(xr),
-                                   _ptr(att), float(slope), _ptr(lse.contiguous()), _ptr(dout),
+                                   _ptr(att), float(slope), _ptr(lse), _ptr(dout),
                                    _ptr(dxl), _ptr(dxr), _ptr(datt), _ptr(ws), ws.numel(),
                                    _stream(stream, xl.device))
     _native.check(rc, "gatv2_agg_backward")
@@ -364,9 +403,10 @@ def transformer_forward(g: Graph, q: torch.Tensor, key: torch.Tensor, val: torch
     """out [N,H,D] (q's dtype) and lse [N,H] float32; scale defaults to 1/sqrt(D)."""
     N, H, D = _gt_inputs(g, q, key, val)
     scale = D ** -0.5 if scale is None else float(scale)
-    out = torch.empty_like(q) if out is None else out
-    lse = torch.empty((N, H), dtype=torch.float32, device=q.device) if lse is None else lse
-    ws = _gt_ws(g, H, D, q.dtype, ws, q.device)
+    out = _given(g, out, "out", q.shape, q.dtype, lambda: torch.empty_like(q))
+    lse = _given(g, lse, "lse", (N, H), torch.float32,
+                 lambda: torch.empty((N, H), dtype=torch.float32, device=q.device))
+    ws = _gt_ws(g, H, D, q.dtype, _check_ws(g, ws), q.device)
     rc = g._lib.transformer_agg_forward(g.handle, H, D, _dtype_code(q.dtype), _ptr(q), _ptr(key),
                                         _ptr(val), scale, _ptr(out), _ptr(lse), _ptr(ws),
                                         ws.numel(), _stream(stream, q.device))
@@ -383,12 +423,13 @@ def transformer_backward(g: Graph, q: torch.Tensor, key: torch.Tensor, val: torc
     if dout.shape != q.shape or dout.dtype != q.dtype:
         raise ValueError("dout must match q")
     scale = D ** -0.5 if scale is None else float(scale)
-    dq = torch.empty_like(q) if dq is None else dq
-    dkey = torch.empty_like(q) if dkey is None else dkey
-    dval = torch.empty_like(q) if dval is None else dval
-    ws = _gt_ws(g, H, D, q.dtype, ws, q.device)
+    _check_tensor(g, lse, "lse", (N, H), torch.float32)
+    dq = _given(g, dq, "dq", q.shape, q.dtype, lambda: torch.empty_like(q))
+    dkey = _given(g, dkey, "dkey", q.shape, q.dtype, lambda: torch.empty_like(q))
+    dval = _given(g, dval, "dval", q.shape, q.dtype, lambda: torch.empty_like(q))
+    ws = _gt_ws(g, H, D, q.dtype, _check_ws(g, ws), q.device)
     rc = g._lib.transformer_agg_backward(g.handle, H, D, _dtype_code(q.dtype), _ptr(q),
-                                         _ptr(key), _ptr(val), scale, _ptr(lse.contiguous()),
+                                         _ptr(key), _ptr(val), scale, _ptr(lse),
                                          _ptr(dout), _ptr(dq), _ptr(dkey), _ptr(dval), _ptr(ws),
                                          ws.numel(), _stream(stream, q.device))
     _native.check(rc, "transformer_agg_backward")
@@ -430,9 +471,10 @@ def reduce_forward(g: Graph, x: torch.Tensor, op: str = "max", out=None, arg=Non
     dt = _dtype_code(x.dtype)
     if op not in _native.REDUCE_OPS:
         raise ValueError(f"op must be one of {sorted(_native.REDUCE_OPS)}")
-    out = torch.empty_like(x) if out is None else out
-    arg = torch.empty(x.shape, dtype=torch.int32, device=x.device) if arg is None else arg
-    ws = _reduce_ws(g, F, dt, ws, x.device)
+    out = _given(g, out, "out", x.shape, x.dtype, lambda: torch.empty_like(x))
+    arg = _given(g, arg, "arg", x.shape, torch.int32,
+                 lambda: torch.empty(x.shape, dtype=torch.int32, device=x.device))
+    ws = _reduce_ws(g, F, dt, _check_ws(g, ws), x.device)
     rc = g._lib.reduce_agg_forward(g.handle, F, dt, _native.REDUCE_OPS[op], _ptr(x), _ptr(out),
                                    _ptr(arg), _ptr(ws), ws.numel(), _stream(stream, x.device))
     _native.check(rc, "reduce_agg_forward")
@@ -443,11 +485,10 @@ def reduce_backward(g: Graph, arg: torch.Tensor, dout: torch.Tensor, dx=None, ws
                     stream=None):
     """dx = the gradient of sum(out * dout) w.r.t. x, from the forward's arg."""
     F = _row_width(g, dout, "dout")
-    if arg.dtype != torch.int32 or arg.shape != dout.shape or not arg.is_contiguous():
-        raise ValueError("arg must be a contiguous int32 tensor shaped like dout")
+    _check_tensor(g, arg, "arg", dout.shape, torch.int32)
     dt = _dtype_code(dout.dtype)
-    dx = torch.empty_like(dout) if dx is None else dx
-    ws = _reduce_ws(g, F, dt, ws, dout.device)
+    dx = _given(g, dx, "dx", dout.shape, dout.dtype, lambda: torch.empty_like(dout))
+    ws = _reduce_ws(g, F, dt, _check_ws(g, ws), dout.device)
     rc = g._lib.reduce_agg_backward(g.handle, F, dt, _ptr(arg), _ptr(dout), _ptr(dx), _ptr(ws),
                                     ws.numel(), _stream(stream, dout.device))
     _native.check(rc, "reduce_agg_backward")

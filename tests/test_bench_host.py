@@ -56,3 +56,23 @@ def test_oracle_sample_rate_stays_within_its_budget():
                                             max_reps=5)
     assert time.perf_counter() - t0 < 5.0
     assert rate > 0 and "100.0% of E" in sample and "run(s)" in sample
+
+
+def test_both_arms_print_the_same_config(capsys):
+    args = bench.parse_args(["--impl", "reference", "--config", "1", "--steps", "1",
+                             "--warmup", "0"])
+    assert bench.run_reference(args, rank=0, world=1) == 0
+    line = json.loads(capsys.readouterr().out)
+    w, rp, ci, *_ = bench.load_workload(1)
+    # the GPU arm prints workload_config(...) of the same workload and world
+    assert line["config"] == bench.workload_config(w, rp, ci, 1)
+    assert line["config"]["max_in_degree"] == int(np.diff(rp).max())
+    assert "one thread" in line["cpu_baseline"]["sample"]
+
+
+def test_default_workload_and_compact_lines():
+    assert bench.DEFAULT_CONFIG == 5
+    assert bench.sub_configs(bench.parse_args([])) == [3, 4, 6]
+    assert bench.sub_configs(bench.parse_args(["--config", "2"])) == []
+    assert bench.sub_configs(bench.parse_args(["--no-sub"])) == []
+    assert bench.sub_configs(bench.parse_args(["--config", "2", "--sub", "3"])) == [3]
