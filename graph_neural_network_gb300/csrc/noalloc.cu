@@ -4,6 +4,8 @@
 // partial states live: in a fixed-size array that belongs to this library
 // (one per GPU that loads it, held until the process exits) instead of a
 // workspace the caller allocates.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -16,20 +18,64 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+
+// The array's device address on each device, with the id of the context it
+// was looked up in: a device reset (or a released and re-created primary
+// context) loads the module again at a new address, so a cached address is
+// used only while the current context is the one it came from.
+struct ScratchAddr {
+  unsigned long long ctx_id;
+  void* addr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Id of the calling thread's current context, 0 when there is none or the
+// driver cannot say (the address is then looked up again).
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool resolved = false;
+  if (!resolved) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) ==
+            cudaSuccess &&
+        q2 == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+      get_id = reinterpret_cast<CtxGetIdFn>(f2);
+    }
+    resolved = true;
+  }
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 // Device address of g_noalloc_scratch on `dev` (which must be current).  In
 // host code the symbol's name is only a host-side stand-in, so the address
-// is looked up once per device and cached.
+// is looked up with cudaGetSymbolAddress the first time a context of the
+// device calls, and cached for that context.
 cudaError_t scratch_on_device(int dev, void** addr) {
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr& c = g_scratch_addr[dev];
+  const unsigned long long id = current_ctx_id();
+  if (!c.addr || id == 0 || c.ctx_id != id) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    c.addr = p;
+    c.ctx_id = current_ctx_id();  // the lookup may have created the context
   }
-  *addr = g_scratch_addr[dev];
+  *addr = c.addr;
   return cudaSuccess;
 }
 

@@ -210,9 +210,12 @@ gnn_status gat_agg_backward_reuse(const gnn_graph* g, int H, int D, gnn_dtype dt
  * (D + 2) * 4 bytes) exceeds that size is rejected with
  * GNN_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  * The first call on a device, with that device current, looks up the
- * array's device address (cudaGetSymbolAddress) and caches it; make that
- * first call before any stream capture.  The device must be the one the
- * graph was prepared on (else GNN_ERR_INVALID_ARG).
+ * array's device address (cudaGetSymbolAddress) and caches it together with
+ * the id of the current context; make that first call before any stream
+ * capture.  After a device reset (or a new primary context) the next call
+ * sees another context id and looks the address up again, so make that
+ * call before any capture too.  The device must be the one the graph was
+ * prepared on (else GNN_ERR_INVALID_ARG).
  * Every call shares the one array: calls that overlap on the GPU (on
  * different streams, or from several threads) race and must be serialised
  * by the caller.  The array keeps the last call's contents; the call zeroes
