@@ -358,10 +358,19 @@ int oracle_gat_backward(int64_t n, const int32_t* row_ptr, const int32_t* col, i
 
 /*
  * Backward for selected nodes only: dh rows of the n_sel listed (distinct)
- * nodes, each from its own neighbourhood: its in-edges for ds_dst, and every
- * edge j -> i that ends at one of its out-neighbours i (found by a scan of the
- * whole CSR) for the value term and ds_src.  dh [n_sel][H][D]; dh_mag may be
- * NULL.  Used where the whole-graph oracle would take too long.
+ * nodes.  Row j gathers the value term and ds_src(j) from every edge j -> i
+ * (found by a scan of the whole CSR, ascending edge position) and ds_dst(j)
+ * from its own in-edges.  Two phases, so that a source with many
+ * out-neighbours costs one pass over their rows, not one per edge:
+ *   1. for every destination i that an edge from a listed node reaches, and
+ *      for every listed node itself: the softmax statistics of each head,
+ *      s_dst(i), lse_i, Delta_i (and ds_dst for the listed nodes), from the
+ *      row's two-pass softmax;
+ *   2. for each listed j and each such edge: alpha_ij = exp(e_ij - lse_i),
+ *      da_ij = dout_i . h_j, dz_ij = alpha_ij (da_ij - Delta_i) g_ij, and
+ *      dh_j = sum alpha_ij dout_i + ds_src(j) a_src + ds_dst(j) a_dst.
+ * dh [n_sel][H][D]; dh_mag may be NULL.  Used where the whole-graph oracle
+ * would take too long.
  */
 int oracle_gat_backward_rows(int64_t n, const int32_t* row_ptr, const int32_t* col, int H, int D,
                              int dtype, const void* h, const double* a_src, const double* a_dst,
@@ -372,13 +381,15 @@ int oracle_gat_backward_rows(int64_t n, const int32_t* row_ptr, const int32_t* c
   if (rc) return rc;
   if (!dout || !sel || n_sel < 0) return 1;
   int64_t* target = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
-  if (!target) return 3;
-  for (int64_t v = 0; v < n; ++v) target[v] = -1;
+  int64_t* slot = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  if (!target || !slot) { free(target); free(slot); return 3; }
+  for (int64_t v = 0; v < n; ++v) target[v] = slot[v] = -1;
   for (int64_t t = 0; t < n_sel; ++t) {
-    if (sel[t] < 0 || sel[t] >= n || target[sel[t]] >= 0) { free(target); return 1; }
+    if (sel[t] < 0 || sel[t] >= n || target[sel[t]] >= 0) { free(target); free(slot); return 1; }
     target[sel[t]] = t;
   }
-  /* in-edge lists of the targets: (destination i, edge position p), ascending p */
+  /* out-edge lists of the targets: (destination i, edge position p - row_ptr[i]),
+     ascending p; destinations needing statistics get a slot */
   int64_t* cnt = (int64_t*)calloc((size_t)n_sel + 1, sizeof(int64_t));
   const int64_t E = row_ptr[n];
   for (int64_t p = 0; p < E; ++p)
@@ -388,53 +399,42 @@ int oracle_gat_backward_rows(int64_t n, const int32_t* row_ptr, const int32_t* c
   int64_t* edge_dst = (int64_t*)malloc(sizeof(int64_t) * (size_t)(cnt[n_sel] + 1));
   int64_t* edge_pos = (int64_t*)malloc(sizeof(int64_t) * (size_t)(cnt[n_sel] + 1));
   memcpy(fill, cnt, sizeof(int64_t) * (size_t)(n_sel + 1));
-  for (int64_t i = 0; i < n; ++i)
+  int64_t n_u = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    int needed = target[i] >= 0;
     for (int64_t p = row_ptr[i]; p < row_ptr[i + 1]; ++p)
       if (target[col[p]] >= 0) {
         const int64_t t = target[col[p]];
         edge_dst[fill[t]] = i;
         edge_pos[fill[t]] = p - row_ptr[i];
         fill[t]++;
+        needed = 1;
       }
+    if (needed) slot[i] = n_u++;
+  }
+  int64_t* u_node = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_u + 1));
+  /* per slot and head: s_dst, lse, Delta, ds_dst, |dz| sum */
+  double* st = (double*)malloc(sizeof(double) * (size_t)(5 * n_u * H + 1));
+  for (int64_t i = 0; i < n; ++i)
+    if (slot[i] >= 0) u_node[slot[i]] = i;
   const int64_t maxdeg = max_in_degree(&g);
+  /* phase 1: statistics of every needed destination, from its own row */
 #pragma omp parallel
   {
     double* z = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
     double* alpha = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
     double* da = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
-#pragma omp for schedule(dynamic, 1)
-    for (int64_t t = 0; t < n_sel; ++t) {
-      const int64_t j = sel[t];
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t u = 0; u < n_u; ++u) {
+      const int64_t i = u_node[u];
       for (int k = 0; k < H; ++k) {
-        double* row = dh + (t * H + k) * (int64_t)D;
-        double* rmag = dh_mag ? dh_mag + (t * H + k) * (int64_t)D : NULL;
-        for (int d = 0; d < D; ++d) {
-          row[d] = 0.0;
-          if (rmag) rmag[d] = 0.0;
-        }
-        double ds_src = 0.0, msrc = 0.0;
-        for (int64_t x = cnt[t]; x < cnt[t + 1]; ++x) {
-          const int64_t i = edge_dst[x], q = edge_pos[x];
-          double ds_i, mag_i;
-          row_softmax(&g, i, k, z, alpha);
-          const double dl = row_backward_stats(&g, dout, i, k, z, alpha, da, &ds_i, &mag_i);
-          ds_src += alpha[q] * (da[q] - dl) * leaky_grad(z[q], slope);
-          msrc += alpha[q] * (fabs(da[q]) + fabs(dl));
-          for (int d = 0; d < D; ++d) {
-            const double xv = feat(&g, dout, i, k, d);
-            row[d] += alpha[q] * xv;
-            if (rmag) rmag[d] += alpha[q] * fabs(xv);
-          }
-        }
-        double ds_dst = 0.0, mdst = 0.0;
-        if (row_ptr[j + 1] > row_ptr[j]) {
-          row_softmax(&g, j, k, z, alpha);
-          row_backward_stats(&g, dout, j, k, z, alpha, da, &ds_dst, &mdst);
-        }
-        for (int d = 0; d < D; ++d) {
-          const double as = a_src[k * D + d], ad = a_dst[k * D + d];
-          row[d] += ds_src * as + ds_dst * ad;
-          if (rmag) rmag[d] += msrc * fabs(as) + mdst * fabs(ad);
+        double* s = st + (u * H + k) * 5;
+        s[0] = head_dot(&g, a_dst, h, i, k);
+        s[1] = -INFINITY;
+        s[2] = s[3] = s[4] = 0.0;
+        if (row_ptr[i + 1] > row_ptr[i]) {
+          s[1] = row_softmax(&g, i, k, z, alpha);
+          s[2] = row_backward_stats(&g, dout, i, k, z, alpha, da, &s[3], &s[4]);
         }
       }
     }
@@ -442,7 +442,44 @@ int oracle_gat_backward_rows(int64_t n, const int32_t* row_ptr, const int32_t* c
     free(alpha);
     free(da);
   }
-  free(target); free(cnt); free(fill); free(edge_dst); free(edge_pos);
+  /* phase 2: each listed source from the statistics of its out-neighbours */
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t t = 0; t < n_sel; ++t) {
+    const int64_t j = sel[t];
+    for (int k = 0; k < H; ++k) {
+      double* row = dh + (t * H + k) * (int64_t)D;
+      double* rmag = dh_mag ? dh_mag + (t * H + k) * (int64_t)D : NULL;
+      for (int d = 0; d < D; ++d) {
+        row[d] = 0.0;
+        if (rmag) rmag[d] = 0.0;
+      }
+      const double ss = head_dot(&g, a_src, h, j, k);
+      double ds_src = 0.0, msrc = 0.0;
+      for (int64_t x = cnt[t]; x < cnt[t + 1]; ++x) {
+        const int64_t i = edge_dst[x];
+        const double* s = st + (slot[i] * H + k) * 5;
+        const double zz = s[0] + ss;
+        const double alpha = exp(leaky(zz, slope) - s[1]);
+        double da = 0.0;
+        for (int d = 0; d < D; ++d) da += feat(&g, dout, i, k, d) * feat(&g, h, j, k, d);
+        ds_src += alpha * (da - s[2]) * leaky_grad(zz, slope);
+        msrc += alpha * (fabs(da) + fabs(s[2]));
+        for (int d = 0; d < D; ++d) {
+          const double xv = feat(&g, dout, i, k, d);
+          row[d] += alpha * xv;
+          if (rmag) rmag[d] += alpha * fabs(xv);
+        }
+      }
+      const double* sj = st + (slot[j] * H + k) * 5;
+      for (int d = 0; d < D; ++d) {
+        const double as = a_src[k * D + d], ad = a_dst[k * D + d];
+        row[d] += ds_src * as + sj[3] * ad;
+        if (rmag) rmag[d] += msrc * fabs(as) + sj[4] * fabs(ad);
+      }
+    }
+  }
+  free(target); free(slot); free(cnt); free(fill); free(edge_dst); free(edge_pos);
+  free(u_node); free(st);
   return 0;
 }
 

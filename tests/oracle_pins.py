@@ -315,6 +315,16 @@ def pin_sampled_modes(o):
     bs = o.backward_rows(rp, ci, h, a_s, a_d, 0.2, dout, sel, with_mag=True)
     close(bs["dh"], b["dh"][sel], 1e-12, 1e-13, "sampled dh")
     close(bs["dh_mag"], b["dh_mag"][sel], 1e-12, 1e-13, "sampled dh_mag")
+    # the per-node rows against the dense autograd directly, on two graphs
+    # (the hub of the irregular graph reaches every node)
+    for rp_x, ci_x, sel_x, seed in ((rp, ci, sel, 13),
+                                    (*workload.erdos_renyi(48, 5.0, 17), [1, 2, 30, 47], 17)):
+        nx = len(rp_x) - 1
+        hx, asx, adx, dx = random_inputs(nx, 2, 4, seed, np.float32)
+        ref = dense_torch(rp_x, ci_x, hx.astype(np.float64), asx.astype(np.float64),
+                          adx.astype(np.float64), 0.2, dx.astype(np.float64))
+        rows = o.backward_rows(rp_x, ci_x, hx, asx, adx, 0.2, dx, sel_x)
+        close(rows["dh"], ref["dh"][sel_x], 1e-10, 1e-12, "sampled dh vs autograd")
     ag = o.att_grads(rp, ci, h, a_s, a_d, 0.2, dout, with_mag=True)
     for k in ("da_src", "da_dst", "da_src_mag", "da_dst_mag"):
         close(ag[k], b[k], 1e-12, 1e-13, "row-grouped " + k)

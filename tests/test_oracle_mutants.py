@@ -23,6 +23,12 @@ MUTANTS = {
                               "dh[(j * H + k) * (int64_t)D + d] += x;"),
     "row_source_offset": ("const int64_t j = g->col[b + q];\n    z[q]",
                           "const int64_t j = g->col[b + (q + 1) % deg];\n    z[q]"),
+    # the per-node backward rows
+    "rows_alpha_from_max": ("const double alpha = exp(leaky(zz, slope) - s[1]);",
+                            "const double alpha = exp(leaky(zz, slope) - s[0]);"),
+    "rows_drop_dst_term": ("row[d] += ds_src * as + sj[3] * ad;", "row[d] += ds_src * as;"),
+    "rows_delta_sign": ("ds_src += alpha * (da - s[2]) * leaky_grad(zz, slope);",
+                        "ds_src += alpha * (da + s[2]) * leaky_grad(zz, slope);"),
 }
 
 
