@@ -219,8 +219,12 @@ __global__ void __launch_bounds__(kSortWarps * 32) k_radix_scatter(
 
 // ---- degree buckets -------------------------------------------------------
 
+// Also writes the key and value arrays of the light-list sort: light nodes
+// get key light_max_deg - degree (descending degree first), every other node
+// light_max_deg + 1 (after all light nodes); the value is the node id.
 __global__ void k_classify(const int32_t* ptr, int64_t n, gnn_tiling t, int32_t* f_light,
-                           int32_t* f_mid, int32_t* f_hub, int32_t* f_chunks, int32_t* max_deg) {
+                           int32_t* f_mid, int32_t* f_hub, int32_t* f_chunks, int32_t* max_deg,
+                           int32_t* light_key, int32_t* light_id) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   int32_t mx = 0;
   for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < n; v += stride) {
@@ -229,6 +233,8 @@ __global__ void k_classify(const int32_t* ptr, int64_t n, gnn_tiling t, int32_t*
     const bool light = d <= t.light_max_deg;
     const bool mid = !light && d <= t.cta_max_deg;
     const bool hub = !light && !mid;
+    light_key[v] = light ? t.light_max_deg - d : t.light_max_deg + 1;
+    light_id[v] = int32_t(v);
     f_light[v] = light;
     f_mid[v] = mid;
     f_hub[v] = hub;
@@ -239,18 +245,18 @@ __global__ void k_classify(const int32_t* ptr, int64_t n, gnn_tiling t, int32_t*
   if ((threadIdx.x & 31) == 0) atomicMax(max_deg, mx);
 }
 
-// After the scans f_* hold each node's position in its bucket list.
+// After the scans f_* hold each node's position in its bucket list.  The
+// light list is written by the sort instead.
 __global__ void k_fill_buckets(const int32_t* ptr, int64_t n, gnn_tiling t,
-                               const int32_t* p_light, const int32_t* p_mid,
-                               const int32_t* p_hub, const int32_t* p_chunk,
-                               const int32_t* n_chunks_total, int32_t* light, int4* items,
-                               int4* hubs) {
+                               const int32_t* p_mid, const int32_t* p_hub,
+                               const int32_t* p_chunk, const int32_t* n_chunks_total,
+                               int4* items, int4* hubs) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const int32_t nch_total = *n_chunks_total;
   for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < n; v += stride) {
     const int32_t b = ptr[v], e = ptr[v + 1], d = e - b;
     if (d <= t.light_max_deg) {
-      light[p_light[v]] = int32_t(v);
+      // light: placed by the degree sort
     } else if (d <= t.cta_max_deg) {
       items[nch_total + p_mid[v]] = make_int4(int32_t(v), b, e, -1);
     } else {
@@ -316,15 +322,45 @@ ScratchBuffers carve_scratch(Carve& c, int64_t n, int64_t e) {
   s.f_hub = c.take<int32_t>(n + 1);
   s.f_chunk = c.take<int32_t>(n + 1);
   s.outdeg = c.take<int32_t>(n + 1);
-  s.k1 = c.take<int32_t>(e);
-  s.v1 = c.take<int32_t>(e);
-  s.k2 = c.take<int32_t>(e);
-  s.v2 = c.take<int32_t>(e);
-  const int64_t hist_n = 256 * sort_blocks(e);
+  // sort buffers serve the CSC sort (e pairs) and the light-list sort (n pairs)
+  const int64_t m = std::max(n, e);
+  s.k1 = c.take<int32_t>(m);
+  s.v1 = c.take<int32_t>(m);
+  s.k2 = c.take<int32_t>(m);
+  s.v2 = c.take<int32_t>(m);
+  const int64_t hist_n = 256 * sort_blocks(m);
   s.hist = c.take<int32_t>(hist_n);
   s.partial = c.take<int32_t>((std::max(hist_n, n + 1) + kScanTile - 1) / kScanTile + 1);
   s.totals = c.take<int32_t>(16);
   return s;
+}
+
+// Stable LSD radix sort of m (key, value) pairs on the low `bits` bits of the
+// keys (8 bits per pass); the sorted values go to vout.  Intermediate passes
+// use s.k1/v1 then s.k2/v2 alternately, so kin and vin must not be s.k1 or
+// s.v1.
+cudaError_t radix_sort_pairs(const int32_t* kin, const int32_t* vin, int64_t m, int bits,
+                             int32_t* vout, const ScratchBuffers& s, cudaStream_t st) {
+  const int passes = std::max(1, (bits + 7) / 8);
+  const int64_t nb = sort_blocks(m);
+  int32_t* kb[2] = {s.k1, s.k2};
+  int32_t* vb[2] = {s.v1, s.v2};
+  cudaError_t e;
+  for (int p = 0; p < passes; ++p) {
+    const bool last = p == passes - 1;
+    int32_t* ko = last ? nullptr : kb[p & 1];
+    int32_t* vo = last ? vout : vb[p & 1];
+    k_radix_hist<<<unsigned(nb), kSortWarps * 32, 0, st>>>(kin, m, 8 * p, s.hist, nb);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = scan_excl(s.hist, s.hist, 256 * nb, s.totals + 1, s.partial, st)) != cudaSuccess)
+      return e;
+    k_radix_scatter<<<unsigned(nb), kSortWarps * 32, 0, st>>>(kin, vin, ko, vo, m, 8 * p, s.hist,
+                                                              nb);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kin = ko;
+    vin = vo;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t build_buckets(const int32_t* ptr, int64_t n, const gnn_tiling& t,
@@ -334,16 +370,22 @@ cudaError_t build_buckets(const int32_t* ptr, int64_t n, const gnn_tiling& t,
   cudaError_t e;
   if (n == 0) return cudaSuccess;
   k_classify<<<grid_for(n, 256), 256, 0, st>>>(ptr, n, t, s.f_light, s.f_mid, s.f_hub,
-                                                s.f_chunk, counters + 4);
+                                                s.f_chunk, counters + 4, s.k2, s.v2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = scan_excl(s.f_light, s.f_light, n, counters + 0, s.partial, st)) != cudaSuccess) return e;
   if ((e = scan_excl(s.f_mid, s.f_mid, n, counters + 1, s.partial, st)) != cudaSuccess) return e;
   if ((e = scan_excl(s.f_hub, s.f_hub, n, counters + 2, s.partial, st)) != cudaSuccess) return e;
   if ((e = scan_excl(s.f_chunk, s.f_chunk, n, counters + 3, s.partial, st)) != cudaSuccess) return e;
-  k_fill_buckets<<<grid_for(n, 256), 256, 0, st>>>(ptr, n, t, s.f_light, s.f_mid, s.f_hub,
-                                                   s.f_chunk, counters + 3, d.light, d.items,
-                                                   d.hubs);
-  return cudaGetLastError();
+  k_fill_buckets<<<grid_for(n, 256), 256, 0, st>>>(ptr, n, t, s.f_mid, s.f_hub, s.f_chunk,
+                                                   counters + 3, d.items, d.hubs);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // light list: light nodes by descending degree, ties by ascending id (the
+  // sort is stable), so that the nodes a warp takes at once have nearly the
+  // same number of edges; the non-light nodes sorted after them fill the
+  // rest of the n-entry array and are never read
+  int bits = 1;
+  while ((int64_t(1) << bits) <= int64_t(t.light_max_deg) + 1) ++bits;
+  return radix_sort_pairs(s.k2, s.v2, n, bits, d.light, s, st);
 }
 
 }  // namespace
@@ -401,29 +443,10 @@ gnn_status prepare_graph(gnn_graph* g, const int32_t* row_ptr, const int32_t* co
   if (e > 0) {
     int bits = 0;
     while (bits < 31 && (int64_t(1) << bits) < n) ++bits;
-    const int passes = std::max(1, (bits + 7) / 8);
-    const int64_t nb = sort_blocks(e);
     int32_t* v0 = s.k2;  // row id per CSR position; consumed by pass 0
     k_expand_rows<<<grid_for(e, 256), 256, 0, st>>>(row_ptr, n, e, v0);
     if (cuda_fail(cudaGetLastError())) return GNN_ERR_CUDA;
-    const int32_t* kin = col;
-    const int32_t* vin = v0;
-    int32_t* kb[2] = {s.k1, s.k2};
-    int32_t* vb[2] = {s.v1, s.v2};
-    for (int p = 0; p < passes; ++p) {
-      const bool last = p == passes - 1;
-      int32_t* kout = last ? nullptr : kb[p & 1];
-      int32_t* vout = last ? row_idx : vb[p & 1];
-      k_radix_hist<<<unsigned(nb), kSortWarps * 32, 0, st>>>(kin, e, 8 * p, s.hist, nb);
-      if (cuda_fail(cudaGetLastError())) return GNN_ERR_CUDA;
-      if (cuda_fail(scan_excl(s.hist, s.hist, 256 * nb, s.totals + 1, s.partial, st)))
-        return GNN_ERR_CUDA;
-      k_radix_scatter<<<unsigned(nb), kSortWarps * 32, 0, st>>>(kin, vin, kout, vout, e, 8 * p,
-                                                                s.hist, nb);
-      if (cuda_fail(cudaGetLastError())) return GNN_ERR_CUDA;
-      kin = kout;
-      vin = vout;
-    }
+    if (cuda_fail(radix_sort_pairs(col, v0, e, bits, row_idx, s, st))) return GNN_ERR_CUDA;
   }
 
   // degree buckets of both directions

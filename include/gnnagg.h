@@ -109,7 +109,10 @@ size_t gnn_graph_scratch_bytes(int64_t n_nodes, int64_t n_edges);
  *   tiling: NULL = defaults.
  * Validation: row_ptr[0] = 0, non-decreasing, row_ptr[n] = n_edges, every
  * col_idx in [0, n_nodes); a failure returns GNN_ERR_INVALID_GRAPH.  The CSC
- * lists each column's rows in ascending order (deterministic).  The call
+ * lists each column's rows in ascending order (deterministic).  Each light
+ * list holds its nodes by descending degree, ties by ascending id, so that
+ * the nodes one warp takes at a time have nearly the same edge count (the
+ * order of work only: results do not depend on it).  The call
  * synchronises `stream` twice (after validation, and to read bucket counts).
  * On success *out receives a handle owned by the caller (gnn_graph_destroy). */
 gnn_status gnn_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t* row_ptr_d,

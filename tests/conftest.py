@@ -28,3 +28,24 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With GNN_PARITY_REPORT set, write every GPU comparison's accounting
+    (elements, elements passing only through the float32 summation term,
+    worst strict ratio), aggregated by what was compared."""
+    path = os.environ.get("GNN_PARITY_REPORT")
+    mod = sys.modules.get("gpu_util")
+    if not path or mod is None:
+        return
+    import json
+    agg = {}
+    for r in mod.REPORT:
+        a = agg.setdefault(r["what"], {"n": 0, "mag_only": 0, "worst_strict_ratio": 0.0,
+                                       "comparisons": 0})
+        a["n"] += r["n"]
+        a["mag_only"] += r["mag_only"]
+        a["worst_strict_ratio"] = max(a["worst_strict_ratio"], r["worst_strict_ratio"])
+        a["comparisons"] += 1
+    with open(path, "w") as f:
+        json.dump(agg, f, indent=1, sort_keys=True)

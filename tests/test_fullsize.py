@@ -1,6 +1,9 @@
 """Full-size workloads, in the launch configuration bench.py times (default
-tiling): sampled outputs against the oracle computed node by node, and the
-attention-vector gradients against the oracle's row-parallel sum."""
+tiling, one workspace shared by the forward and the backward): the GAT
+forward on every row, the GAT backward on every row of the two smaller graphs
+and on sampled rows (with the largest CSC hubs) of the others, the
+attention-vector gradients over the whole graph, and sampled rows of the
+other aggregation families."""
 import numpy as np
 import pytest
 import torch
@@ -25,40 +28,85 @@ def _backward_cost(rp, ci):
     return np.bincount(ci, weights=indeg[dst], minlength=len(rp) - 1)
 
 
+CHUNK = 1 << 18   # nodes per oracle call when every row is compared
+
+
+def _gat_bench_launch(case, w):
+    """Forward and backward in the launch configuration bench.py times:
+    default tiling, one workspace for both calls, so that the backward takes
+    the per-node scores the forward left there."""
+    import graph_neural_network_gb300 as gnn
+    g = gpu_util.device_graph(case)
+    h = gpu_util.to_device(case["h"], w.dtype)
+    dout = gpu_util.to_device(case["dout"], w.dtype)
+    a_s = torch.from_numpy(case["a_src"]).cuda()
+    a_d = torch.from_numpy(case["a_dst"]).cuda()
+    ws = g.workspace(w.H, w.D, h.dtype)
+    out, lse = gnn.gat_forward(g, h, a_s, a_d, w.slope, ws=ws)
+    dh, da_s, da_d = gnn.gat_backward(g, h, a_s, a_d, w.slope, lse, dout, ws=ws,
+                                      reuse_scores=True)
+    torch.cuda.synchronize()
+    gnn.check_device_error(g)
+    return dict(graph=g, out_t=out, lse_t=lse, dh_t=dh, da_src_t=da_s, da_dst_t=da_d)
+
+
 @pytest.mark.parametrize("idx", [2, 3, 4, 5, 6])
-def test_full_size_sampled_parity(idx):
+def test_full_size_parity(idx):
+    """Every row of out and lse against the oracle (strict bound); dh on every
+    row for the two smaller graphs, else on 2,000 random rows, the 24 largest
+    out-degrees (CSC hubs of many chunks) and the ragged tail; da_src and
+    da_dst over the whole graph."""
     w = workload.CONFIGS[idx]
     rp, ci = workload.make_graph(w)
     n = len(rp) - 1
     h, a_s, a_d, dout = workload.make_features(w, n)
     case = dict(row_ptr=rp, col=ci, h=h, dout=dout, a_src=a_s, a_dst=a_d, H=w.H, D=w.D,
                 dtype=w.dtype, slope=w.slope)
-    gpu = run_gpu(case, fetch=False)
+    gpu = _gat_bench_launch(case, w)
+    # forward: every row, in chunks of nodes
+    for c0 in range(0, n, CHUNK):
+        sel = np.arange(c0, min(n, c0 + CHUNK))
+        f = oracle.forward(rp, ci, h, a_s, a_d, w.slope, sel=sel, with_mag=True)
+        assert_close(_rows(gpu["out_t"], sel), f["out"], w.dtype, f["out_mag"], f"cfg{idx} out",
+                     strict=True)
+        assert_close(_rows(gpu["lse_t"], sel), f["lse"], w.dtype, None, f"cfg{idx} lse",
+                     strict=True)
+        del f
     rng = np.random.default_rng(1000 + idx)
-    indeg = np.diff(rp)
     outdeg = np.bincount(ci, minlength=n)
-    # forward: random nodes, the largest in-degrees (hub split + merge), ragged tail
-    sel_f = np.unique(np.concatenate([rng.choice(n, 3000, replace=False),
-                                      np.argsort(indeg)[-64:], np.arange(n - 17, n)]))
-    f = oracle.forward(rp, ci, h, a_s, a_d, w.slope, sel=sel_f, with_mag=True)
-    assert_close(_rows(gpu["out_t"], sel_f), f["out"], w.dtype, f["out_mag"], f"cfg{idx} out")
-    assert_close(_rows(gpu["lse_t"], sel_f), f["lse"], w.dtype, None, f"cfg{idx} lse")
-    # backward rows: random nodes plus the largest out-degrees the oracle can afford
-    cost = _backward_cost(rp, ci)
-    cheap = np.nonzero(cost < 2e5)[0]
-    top = [j for j in np.argsort(outdeg)[::-1][:400] if cost[j] < 3e7][:24]
-    sel_b = np.unique(np.concatenate([rng.choice(cheap, min(400, len(cheap)), replace=False),
-                                      np.asarray(top, np.int64)]))
-    b = oracle.backward_rows(rp, ci, h, a_s, a_d, w.slope, dout, sel_b, with_mag=True)
-    assert_close(_rows(gpu["dh_t"], sel_b), b["dh"], w.dtype, b["dh_mag"], f"cfg{idx} dh")
-    ag = oracle.att_grads(rp, ci, h, a_s, a_d, w.slope, dout, with_mag=True)
-    assert_close(to_f64(gpu["da_src_t"]), ag["da_src"], w.dtype, ag["da_src_mag"], "da_src")
-    assert_close(to_f64(gpu["da_dst_t"]), ag["da_dst"], w.dtype, ag["da_dst_mag"], "da_dst")
-    assert outdeg[top].max() > 4096 or idx == 2      # the CSC hub path was sampled
-    # SpMM-family propagation (symmetric normalisation) on the same graph and rows
+    top = np.argsort(outdeg)[::-1][:24]
+    if idx in (2, 3):
+        b = oracle.backward(rp, ci, h, a_s, a_d, w.slope, dout, with_mag=True)
+        for c0 in range(0, n, CHUNK):
+            sel = np.arange(c0, min(n, c0 + CHUNK))
+            assert_close(_rows(gpu["dh_t"], sel), b["dh"][sel], w.dtype, b["dh_mag"][sel],
+                         f"cfg{idx} dh")
+        da = {k: b[k] for k in ("da_src", "da_dst", "da_src_mag", "da_dst_mag")}
+        del b
+    else:
+        sel_b = np.unique(np.concatenate([rng.choice(n, 2000, replace=False), top,
+                                          np.arange(n - 9, n)]))
+        b = oracle.backward_rows(rp, ci, h, a_s, a_d, w.slope, dout, sel_b, with_mag=True)
+        assert_close(_rows(gpu["dh_t"], sel_b), b["dh"], w.dtype, b["dh_mag"], f"cfg{idx} dh")
+        da = oracle.att_grads(rp, ci, h, a_s, a_d, w.slope, dout, with_mag=True)
+    assert_close(to_f64(gpu["da_src_t"]), da["da_src"], w.dtype, da["da_src_mag"],
+                 f"cfg{idx} da_src")
+    assert_close(to_f64(gpu["da_dst_t"]), da["da_dst"], w.dtype, da["da_dst_mag"],
+                 f"cfg{idx} da_dst")
+    assert outdeg[top].max() > 4096 or idx == 2      # the CSC hub path was compared
+    # SpMM-family propagation (symmetric normalisation) and the max reduction
+    # on the same graph: sampled rows
     import graph_neural_network_gb300 as gnn
     g = gpu["graph"]
+    del gpu
     F = w.H * w.D
+    indeg = np.diff(rp)
+    cost = _backward_cost(rp, ci)
+    sel_f = np.unique(np.concatenate([rng.choice(n, 3000, replace=False),
+                                      np.argsort(indeg)[-64:], np.arange(n - 17, n)]))
+    cheap = np.nonzero(cost < 2e5)[0]
+    sel_s = np.unique(np.concatenate([rng.choice(cheap, min(400, len(cheap)), replace=False),
+                                      np.asarray([j for j in top if cost[j] < 3e7], np.int64)]))
     x = gpu_util.to_device(h.reshape(n, F), w.dtype)
     dy = gpu_util.to_device(dout.reshape(n, F), w.dtype)
     out = gnn.gcn_forward(g, x, "sym")
@@ -66,8 +114,8 @@ def test_full_size_sampled_parity(idx):
     torch.cuda.synchronize()
     sf = oracle.spmm_forward(rp, ci, h.reshape(n, F), "sym", sel=sel_f, with_mag=True)
     assert_close(_rows(out, sel_f), sf["out"], w.dtype, sf["out_mag"], f"cfg{idx} gcn out")
-    sb = oracle.spmm_backward_rows(rp, ci, dout.reshape(n, F), "sym", sel_b, with_mag=True)
-    assert_close(_rows(dx, sel_b), sb["dx"], w.dtype, sb["dx_mag"], f"cfg{idx} gcn dx")
+    sb = oracle.spmm_backward_rows(rp, ci, dout.reshape(n, F), "sym", sel_s, with_mag=True)
+    assert_close(_rows(dx, sel_s), sb["dx"], w.dtype, sb["dx_mag"], f"cfg{idx} gcn dx")
     # max reduction: sampled rows bit for bit, sampled gradient rows
     rout, rarg = gnn.reduce_forward(g, x, "max")
     rdx = gnn.reduce_backward(g, rarg, dy)
@@ -76,7 +124,7 @@ def test_full_size_sampled_parity(idx):
     sel_t = torch.from_numpy(np.asarray(sel_f, np.int64)).to(rarg.device)
     assert np.array_equal(rarg[sel_t].cpu().numpy(), rf["arg"]), f"cfg{idx} max arg"
     assert np.array_equal(_rows(rout, sel_f), rf["out"]), f"cfg{idx} max out"
-    cheap_r = sel_b[cost[sel_b] < 2e4][:150]     # the oracle recomputes every row they win
+    cheap_r = sel_s[cost[sel_s] < 2e4][:150]     # the oracle recomputes every row they win
     rb = oracle.reduce_backward_rows(rp, ci, h.reshape(n, F), "max", dout.reshape(n, F), cheap_r,
                                      with_mag=True)
     assert_close(_rows(rdx, cheap_r), rb["dx"], w.dtype, rb["dx_mag"], f"cfg{idx} max dx")

@@ -97,9 +97,37 @@ def test_bitwise_deterministic(tiling):
     rp, ci = testgraphs.with_in_degrees(THRESHOLD_DEGREES, n_nodes=3000, seed=37)
     case = make_case(rp, ci, 4, 32, "bf16", 37)
     a = run_gpu(case, tiling)
-    b = run_gpu(case, tiling)
-    for k in ("out", "lse", "dh", "da_src", "da_dst"):
-        assert np.array_equal(a[k], b[k], equal_nan=True), k
+    for _ in range(2):
+        b = run_gpu(case, tiling)
+        for k in ("out", "lse", "dh", "da_src", "da_dst"):
+            assert np.array_equal(a[k], b[k], equal_nan=True), k
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_hub_of_1e5_equal_scores_is_the_mean(dtype):
+    """One destination with 100,000 distinct in-neighbours and all scores
+    equal (a_src = a_dst = 0): out is the fp64 mean of the neighbour rows and
+    lse = ln(100,000), within the plain tolerance, in the default tiling (a
+    hub of 49 chunks merged in chunk order), and bitwise the same over three
+    runs."""
+    deg = 100_000
+    n = deg + 1
+    # node 0 gathers from every other node; the others keep one self-loop
+    rp = np.concatenate([[0], deg + np.arange(n, dtype=np.int64)]).astype(np.int32)
+    ci = np.concatenate([np.arange(1, n), np.arange(1, n)]).astype(np.int32)
+    D = 32 if dtype == "f32" else 64
+    case = make_case(rp, ci, 2, D, dtype, 53)
+    case["a_src"][:] = 0
+    case["a_dst"][:] = 0
+    runs = [run_gpu(case, backward=False) for _ in range(3)]
+    assert runs[0]["graph"].stats()["csr"]["hub_chunks"] == 49
+    h = case["h"] if dtype == "f32" else workload.bf16_bits_to_f32(case["h"])
+    mean = h[1:].astype(np.float64).mean(axis=0)
+    assert_close(runs[0]["out"][0], mean, dtype, None, f"hub mean {dtype}", strict=True)
+    assert_close(runs[0]["lse"][0], np.full(2, np.log(deg)), "f32", None, f"hub lse {dtype}",
+                 strict=True)
+    for r in runs[1:]:
+        assert np.array_equal(r["out"], runs[0]["out"]) and np.array_equal(r["lse"], runs[0]["lse"])
 
 
 def test_side_stream_matches_default_stream():

@@ -24,6 +24,7 @@ def host_buckets(ptr, tiling):
     light_max, cta_max, chunk = tiling
     deg = np.diff(ptr)
     light = np.nonzero(deg <= light_max)[0]
+    light = light[np.argsort(-deg[light], kind="stable")]   # descending degree, ties by id
     mid = np.nonzero((deg > light_max) & (deg <= cta_max))[0]
     hub = np.nonzero(deg > cta_max)[0]
     items, hubs, slot = [], [], 0
