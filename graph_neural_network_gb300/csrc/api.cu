@@ -34,6 +34,20 @@ bool make_shape(int H, int D, gnn_dtype dt, Shape* s) {
   return true;
 }
 
+bool make_wide_shape(const Shape& s, Shape* w) {
+  if (s.hv < 2 || s.rv > 64) return false;
+  *w = s;
+  w->rv = s.rv / 2;
+  w->hv = s.hv / 2;
+  w->lpr = 1;
+  while (w->lpr < w->rv) w->lpr <<= 1;
+  w->nv = 1;
+  w->hv_log2 = s.hv_log2 - 1;
+  w->lpr_log2 = 0;
+  while ((1 << w->lpr_log2) < w->lpr) ++w->lpr_log2;
+  return true;
+}
+
 WsLayout ws_layout(const gnn_graph* g, const Shape& s) {
   WsLayout L;
   const size_t HD = size_t(s.H) * s.D;

@@ -333,6 +333,125 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
   s = t;
 }
 
+// ---- lane vectors of 16 or 32 bytes -------------------------------------------
+//
+// The attention kernels can give each lane 32 contiguous bytes of a row (two
+// 16-byte halves, loaded by one 256-bit load) instead of 16, where a head
+// spans at least 32 bytes: the per-edge work that does not depend on the
+// number of elements a lane holds (addresses, the per-edge statistics, the
+// score and its exponential) is then shared by twice as many elements.
+
+template <int VB>
+struct RawV;
+template <>
+struct RawV<16> {
+  uint4 a;
+};
+template <>
+struct RawV<32> {
+  uint4 a, b;
+};
+
+// Elements of T in a VB-byte lane vector, and edges each lane keeps in flight
+// per batch (the same 64 bytes either way).
+template <typename T, int VB>
+struct ElemsOf {
+  static constexpr int n = VB / int(sizeof(T));
+};
+template <int VB>
+struct UnrollOf {
+  static constexpr int value = 64 / VB;
+};
+
+template <int VB>
+__device__ __forceinline__ RawV<VB> ldv(const void* p);
+template <>
+__device__ __forceinline__ RawV<16> ldv<16>(const void* p) {
+  return RawV<16>{ld16(p)};
+}
+// One 256-bit read-only load (32-byte aligned).
+template <>
+__device__ __forceinline__ RawV<32> ldv<32>(const void* p) {
+  RawV<32> r;
+  asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r.a.x), "=r"(r.a.y), "=r"(r.a.z), "=r"(r.a.w), "=r"(r.b.x), "=r"(r.b.y),
+        "=r"(r.b.z), "=r"(r.b.w)
+      : "l"(p));
+  return r;
+}
+
+template <int VB>
+__device__ __forceinline__ RawV<VB> zero_raw();
+template <>
+__device__ __forceinline__ RawV<16> zero_raw<16>() {
+  return RawV<16>{make_uint4(0, 0, 0, 0)};
+}
+template <>
+__device__ __forceinline__ RawV<32> zero_raw<32>() {
+  return RawV<32>{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+}
+
+// Widen a lane vector to float (two spellings, as unpack / unpack_alt).
+template <typename T, int VB>
+__device__ __forceinline__ void unpackv(const RawV<VB>& r, float (&x)[ElemsOf<T, VB>::n]) {
+  constexpr int H16 = VecOf<T>::n;
+  float* p = x;
+  unpack<T>(r.a, *reinterpret_cast<float(*)[H16]>(p));
+  if constexpr (VB == 32) unpack<T>(r.b, *reinterpret_cast<float(*)[H16]>(p + H16));
+}
+template <typename T, int VB>
+__device__ __forceinline__ void unpack_altv(const RawV<VB>& r, float (&x)[ElemsOf<T, VB>::n]) {
+  constexpr int H16 = VecOf<T>::n;
+  float* p = x;
+  unpack_alt<T>(r.a, *reinterpret_cast<float(*)[H16]>(p));
+  if constexpr (VB == 32) unpack_alt<T>(r.b, *reinterpret_cast<float(*)[H16]>(p + H16));
+}
+
+// Narrow and store a lane vector (plain stores, 16 bytes each).
+template <typename T, int VB>
+__device__ __forceinline__ void storev(void* dst, const float (&x)[ElemsOf<T, VB>::n]) {
+  constexpr int H16 = VecOf<T>::n;
+  const float* p = x;
+  st16(dst, pack<T>(*reinterpret_cast<const float(*)[H16]>(p)));
+  if constexpr (VB == 32)
+    st16(reinterpret_cast<char*>(dst) + 16, pack<T>(*reinterpret_cast<const float(*)[H16]>(p + H16)));
+}
+
+template <int VB>
+__device__ __forceinline__ const char* row_at(const void* base, int64_t node, int rv) {
+  return reinterpret_cast<const char*>(base) + node * int64_t(rv) * VB;
+}
+
+// This lane's slices of an attention vector [H][D] (float) for VB-byte lane
+// vectors, times `scale`.
+template <typename T, int NV, int VB>
+__device__ __forceinline__ void load_att_v(const float* a, const Lane<NV>& L, float scale,
+                                           float (&w)[NV][ElemsOf<T, VB>::n]) {
+  constexpr int V = ElemsOf<T, VB>::n;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+#pragma unroll
+    for (int c4 = 0; c4 < V; c4 += 4) {
+      float4 t = L.ok[v] ? ld16f(a + L.q[v] * V + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[v][c4 + 0] = t.x * scale;
+      w[v][c4 + 1] = t.y * scale;
+      w[v][c4 + 2] = t.z * scale;
+      w[v][c4 + 3] = t.w * scale;
+    }
+  }
+}
+
+// This lane's vectors of row `node` of x (VB-byte lane vectors), widened
+// (zeros where q >= rv).
+template <typename T, int NV, int VB>
+__device__ __forceinline__ void load_row_v(const void* x, int64_t node, const Shape& s,
+                                           const Lane<NV>& L, float (&r)[NV][ElemsOf<T, VB>::n]) {
+  const char* row = row_at<VB>(x, node, s.rv);
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+    unpackv<T, VB>(L.ok[v] ? ldv<VB>(row + VB * L.q[v]) : zero_raw<VB>(), r[v]);
+}
+
 // This lane's slice (vector q) of row `node` when a row needs at most one
 // vector per lane, widened (zeros when !ok).
 template <typename T>

@@ -74,33 +74,34 @@ __device__ __forceinline__ float leaky_grad(float z, float slope) { return z > 0
 // pass 1: destination side (CSR)
 // ---------------------------------------------------------------------------
 
-// Edges beg + sg, beg + sg + SG, ... < end, until end (kFixed false) or in
-// exactly `trips` batches (kFixed true; the same count on every lane of the
-// warp, batches past end add nothing).
-template <typename T, int NV, bool kFixed>
+// Batches of kUnroll edges per lane: the batch at `base` holds edges
+// base + sg + u * SG, the next one starts `step` edges further; until end
+// (kFixed false) or in exactly `trips` batches (kFixed true; the same count
+// on every lane of the warp, batches past end add nothing).
+template <typename T, int NV, int VB, bool kFixed>
 __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
-                                          int sg, int SG, int trips, int (&jn)[kUnroll],
-                                          const float (&gi)[NV][VecOf<T>::n],
+                                          int sg, int SG, int step, int trips,
+                                          int (&jn)[UnrollOf<VB>::value],
+                                          const float (&gi)[NV][ElemsOf<T, VB>::n],
                                           const float (&sd2)[NV], const float (&lse2)[NV],
                                           float (&SA)[NV], float (&SB)[NV], float (&SD)[NV]) {
-  constexpr int V = VecOf<T>::n;
-  constexpr int U = kUnroll;
-  const int step = SG * U;
+  constexpr int V = ElemsOf<T, VB>::n;
+  constexpr int U = UnrollOf<VB>::value;
   const int H = A.s.H;
   int base = beg;
   for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
-    uint4 raw[U][NV];
+    RawV<VB> raw[U][NV];
     float ss[U * NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         const bool ok = j[u] >= 0 && L.ok[v];
-        raw[u][v] = ok ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v]) : make_uint4(0, 0, 0, 0);
+        raw[u][v] = ok ? ldv<VB>(row_at<VB>(A.h, j[u], A.s.rv) + VB * L.q[v]) : zero_raw<VB>();
         ss[u * NV + v] = ok ? __ldg(A.ssrc + int64_t(j[u]) * H + L.k[v]) : 0.f;
       }
     if (kFixed ? t + 1 < trips : base + step < end)
@@ -111,7 +112,7 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         float x[V];
-        unpack<T>(raw[u][v], x);
+        unpackv<T, VB>(raw[u][v], x);
         dd[u * NV + v] = dot<V>(x, gi[v]);
       }
     head_sums<U * NV>(dd, A.s.hv_log2);
@@ -135,15 +136,17 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
 // edges are spread over the warp's sub-groups (beg + g, beg + g + G, ...)
 // and the sums added over them; otherwise this lane's sub-group takes them
 // all in `trips` batches.  jn: sources of the first batch.
-template <typename T, int NV>
+template <typename T, int NV, int VB>
 __device__ __forceinline__ void dst_node(const BwdArgs& A, const Lane<NV>& L, int i,
                                          const int32_t* cols, int colbase, int beg, int end,
-                                         bool split, int trips, int (&jn)[kUnroll],
-                                         float (&sd2)[NV], float (&lse2)[NV], float (&SA)[NV],
-                                         float (&SB)[NV], float (&SD)[NV]) {
-  constexpr int V = VecOf<T>::n;
+                                         bool split, int step, int trips,
+                                         int (&jn)[UnrollOf<VB>::value], float (&sd2)[NV],
+                                         float (&lse2)[NV], float (&SA)[NV], float (&SB)[NV],
+                                         float (&SD)[NV]) {
+  constexpr int V = ElemsOf<T, VB>::n;
+  constexpr int U = UnrollOf<VB>::value;
   float gi[NV][V];
-  load_row<T, NV>(A.dout, i, A.s, L, gi);
+  load_row_v<T, NV, VB>(A.dout, i, A.s, L, gi);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     sd2[v] = L.ok[v] ? __ldg(A.sdst + int64_t(i) * A.s.H + L.k[v]) : 0.f;
@@ -151,8 +154,8 @@ __device__ __forceinline__ void dst_node(const BwdArgs& A, const Lane<NV>& L, in
     SA[v] = SB[v] = SD[v] = 0.f;
   }
   if (split) {
-    dst_edges<T, NV, false>(A, L, cols, colbase, beg, end, L.g, L.G, 0, jn, gi, sd2, lse2, SA,
-                            SB, SD);
+    dst_edges<T, NV, VB, false>(A, L, cols, colbase, beg, end, L.g, L.G, step, 0, jn, gi, sd2,
+                                lse2, SA, SB, SD);
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       SA[v] = subgroup_sum(SA[v], A.s);
@@ -160,16 +163,16 @@ __device__ __forceinline__ void dst_node(const BwdArgs& A, const Lane<NV>& L, in
       SD[v] = subgroup_sum(SD[v], A.s);
     }
   } else {
-    dst_edges<T, NV, true>(A, L, cols, colbase, beg, end, 0, 1, trips, jn, gi, sd2, lse2, SA, SB,
-                           SD);
+    dst_edges<T, NV, VB, true>(A, L, cols, colbase, beg, end, 0, 1, U, trips, jn, gi, sd2, lse2,
+                               SA, SB, SD);
   }
 }
 
 // kSub: light nodes take one sub-group each (rows narrower than a warp);
 // otherwise one warp each.
-template <typename T, int NV, bool kSub>
+template <typename T, int NV, int VB, bool kSub>
 __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_main(const BwdArgs A) {
-  constexpr int V = VecOf<T>::n;
+  constexpr int U = UnrollOf<VB>::value;
   const DirArgs& D = A.csr;
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
@@ -192,11 +195,13 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_ma
       if (idx >= D.n_items) break;
       const int4 it = D.items[idx];
       if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
-      const int per = (it.z - it.y + kWarps - 1) / kWarps;
-      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
-      int jn[kUnroll];
-      batch_ids<kUnroll>(cols, it.y & ~3, wb, we, L.g, L.G, jn);
-      dst_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, true, 0, jn, sd2, lse2, SA, SB, SD);
+      // batches of kUnroll * G edges dealt to the warps in turn
+      const int batch = U * L.G;
+      const int wb = it.y + wid * batch;
+      int jn[U];
+      batch_ids<U>(cols, it.y & ~3, wb, it.z, L.g, L.G, jn);
+      dst_node<T, NV, VB>(A, L, it.x, cols, it.y & ~3, wb, it.z, true, kWarps * batch, 0, jn, sd2,
+                          lse2, SA, SB, SD);
       if (L.g == 0)
 #pragma unroll
         for (int v = 0; v < NV; ++v)
@@ -251,13 +256,13 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_ma
         const int e0 = __shfl_sync(kFull, my_e, src);  // every lane shuffles
         const int end = i >= 0 ? e0 : beg;
         if (!__any_sync(kFull, i >= 0)) break;
-        int trips = (end - beg + kUnroll - 1) / kUnroll;
+        int trips = (end - beg + U - 1) / U;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
-        int jn[kUnroll];
-        batch_ids<kUnroll>(D.idx, 0, beg, end, 0, 1, jn);
-        dst_node<T, NV>(A, L, i >= 0 ? i : 0, D.idx, 0, beg, end, false, trips, jn, sd2, lse2, SA,
-                        SB, SD);
+        int jn[U];
+        batch_ids<U>(D.idx, 0, beg, end, 0, 1, jn);
+        dst_node<T, NV, VB>(A, L, i >= 0 ? i : 0, D.idx, 0, beg, end, false, 0, trips, jn, sd2, lse2,
+                            SA, SB, SD);
         if (i >= 0)
 #pragma unroll
           for (int v = 0; v < NV; ++v)
@@ -283,16 +288,17 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_ma
     }
     int i = __shfl_sync(kFull, my_i, 0);
     int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
-    int jn[kUnroll];
-    batch_ids<kUnroll>(D.idx, 0, beg, end, L.g, L.G, jn);
+    int jn[U];
+    batch_ids<U>(D.idx, 0, beg, end, L.g, L.G, jn);
     for (int q = 0; q < kGrab && i >= 0; ++q) {
       const int nq = (q + 1) & (kGrab - 1);
       const int i2 = q + 1 < kGrab ? __shfl_sync(kFull, my_i, nq) : -1;
       const int b2 = __shfl_sync(kFull, my_b, nq);
       const int e2 = __shfl_sync(kFull, my_e, nq);
-      int jn2[kUnroll];
-      batch_ids<kUnroll>(D.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
-      dst_node<T, NV>(A, L, i, D.idx, 0, beg, end, true, 0, jn, sd2, lse2, SA, SB, SD);
+      int jn2[U];
+      batch_ids<U>(D.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
+      dst_node<T, NV, VB>(A, L, i, D.idx, 0, beg, end, true, U * L.G, 0, jn, sd2, lse2, SA, SB,
+                          SD);
       if (L.g == 0)
 #pragma unroll
         for (int v = 0; v < NV; ++v)
@@ -303,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_ma
       beg = b2;
       end = e2;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) jn[u] = jn2[u];
+      for (int u = 0; u < U; ++u) jn[u] = jn2[u];
     }
   }
 }
@@ -335,31 +341,30 @@ __global__ void __launch_bounds__(kThreads) bwd_dst_merge(const BwdArgs A) {
 // pass 2: source side (CSC)
 // ---------------------------------------------------------------------------
 
-template <typename T, int NV, bool kFixed>
+template <typename T, int NV, int VB, bool kFixed>
 __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
-                                          int sg, int SG, int trips, int (&in)[kUnroll],
-                                          const float (&xj)[NV][VecOf<T>::n],
-                                          const float (&ss2)[NV], float (&acc)[NV][VecOf<T>::n],
-                                          float (&SZ)[NV]) {
-  constexpr int V = VecOf<T>::n;
-  constexpr int U = kUnroll;
-  const int step = SG * U;
+                                          int sg, int SG, int step, int trips,
+                                          int (&in)[UnrollOf<VB>::value],
+                                          const float (&xj)[NV][ElemsOf<T, VB>::n],
+                                          const float (&ss2)[NV],
+                                          float (&acc)[NV][ElemsOf<T, VB>::n], float (&SZ)[NV]) {
+  constexpr int V = ElemsOf<T, VB>::n;
+  constexpr int U = UnrollOf<VB>::value;
   const int H = A.s.H;
   int base = beg;
   for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int i[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) i[u] = in[u];
-    uint4 raw[U][NV];
+    RawV<VB> raw[U][NV];
     float4 st[U][NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         const bool ok = i[u] >= 0 && L.ok[v];
-        raw[u][v] = ok ? ld16(row_base<T>(A.dout, i[u], A.s.rv) + 16 * L.q[v])
-                       : make_uint4(0, 0, 0, 0);
+        raw[u][v] = ok ? ldv<VB>(row_at<VB>(A.dout, i[u], A.s.rv) + VB * L.q[v]) : zero_raw<VB>();
         st[u][v] = ok ? ld16f(A.stats + int64_t(i[u]) * H + L.k[v])
                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
@@ -371,7 +376,7 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         float g[V];
-        unpack<T>(raw[u][v], g);
+        unpackv<T, VB>(raw[u][v], g);
         dd[u * NV + v] = dot<V>(g, xj[v]);
       }
     head_sums<U * NV>(dd, A.s.hv_log2);
@@ -384,7 +389,7 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
         const float al = i[u] >= 0 ? ex2(leaky(z, A.slope) - st[u][v].y) : 0.f;
         SZ[v] = fmaf(al * (da - st[u][v].z), leaky_grad(z, A.slope), SZ[v]);
         float g[V];
-        unpack_alt<T>(raw[u][v], g);
+        unpack_altv<T, VB>(raw[u][v], g);
         axpy<V>(acc[v], al, g);
       }
   }
@@ -392,14 +397,16 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
 
 // Source-side sums of node j over its out-edges [beg, end) (in:
 // destinations of the first batch).  split / trips as for dst_node.
-template <typename T, int NV>
+template <typename T, int NV, int VB>
 __device__ __forceinline__ void src_node(const BwdArgs& A, const Lane<NV>& L, int j,
                                          const int32_t* cols, int colbase, int beg, int end,
-                                         bool split, int trips, int (&in)[kUnroll],
-                                         float (&acc)[NV][VecOf<T>::n], float (&SZ)[NV]) {
-  constexpr int V = VecOf<T>::n;
+                                         bool split, int step, int trips,
+                                         int (&in)[UnrollOf<VB>::value],
+                                         float (&acc)[NV][ElemsOf<T, VB>::n], float (&SZ)[NV]) {
+  constexpr int V = ElemsOf<T, VB>::n;
+  constexpr int U = UnrollOf<VB>::value;
   float xj[NV][V], ss2[NV];
-  load_row<T, NV>(A.h, j, A.s, L, xj);
+  load_row_v<T, NV, VB>(A.h, j, A.s, L, xj);
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     ss2[v] = L.ok[v] ? __ldg(A.ssrc + int64_t(j) * A.s.H + L.k[v]) : 0.f;
@@ -408,7 +415,8 @@ __device__ __forceinline__ void src_node(const BwdArgs& A, const Lane<NV>& L, in
     for (int c = 0; c < V; ++c) acc[v][c] = 0.f;
   }
   if (split) {
-    src_edges<T, NV, false>(A, L, cols, colbase, beg, end, L.g, L.G, 0, in, xj, ss2, acc, SZ);
+    src_edges<T, NV, VB, false>(A, L, cols, colbase, beg, end, L.g, L.G, step, 0, in, xj, ss2,
+                                acc, SZ);
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       SZ[v] = subgroup_sum(SZ[v], A.s);
@@ -416,20 +424,21 @@ __device__ __forceinline__ void src_node(const BwdArgs& A, const Lane<NV>& L, in
       for (int c = 0; c < V; ++c) acc[v][c] = subgroup_sum(acc[v][c], A.s);
     }
   } else {
-    src_edges<T, NV, true>(A, L, cols, colbase, beg, end, 0, 1, trips, in, xj, ss2, acc, SZ);
+    src_edges<T, NV, VB, true>(A, L, cols, colbase, beg, end, 0, 1, U, trips, in, xj, ss2, acc,
+                               SZ);
   }
 }
 
 // dh_j = acc + ds_src a_src + ds_dst a_dst (natural units), ds_src(j) = SZ.
-template <typename T, int NV>
+template <typename T, int NV, int VB>
 __device__ __forceinline__ void write_src(const BwdArgs& A, const Lane<NV>& L, int64_t j,
-                                          const float (&acc)[NV][VecOf<T>::n],
+                                          const float (&acc)[NV][ElemsOf<T, VB>::n],
                                           const float (&SZ)[NV]) {
-  constexpr int V = VecOf<T>::n;
+  constexpr int V = ElemsOf<T, VB>::n;
   float as[NV][V], ad[NV][V];
-  load_att<T, NV>(A.a_src, L, 1.f, as);
-  load_att<T, NV>(A.a_dst, L, 1.f, ad);
-  char* orow = reinterpret_cast<char*>(A.dh) + j * int64_t(A.s.rv) * 16;
+  load_att_v<T, NV, VB>(A.a_src, L, 1.f, as);
+  load_att_v<T, NV, VB>(A.a_dst, L, 1.f, ad);
+  char* orow = reinterpret_cast<char*>(A.dh) + j * int64_t(A.s.rv) * VB;
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     if (!L.ok[v]) continue;
@@ -437,14 +446,15 @@ __device__ __forceinline__ void write_src(const BwdArgs& A, const Lane<NV>& L, i
     float x[V];
 #pragma unroll
     for (int c = 0; c < V; ++c) x[c] = fmaf(dsd, ad[v][c], fmaf(SZ[v], as[v][c], acc[v][c]));
-    st16(orow + 16 * L.q[v], pack<T>(x));
+    storev<T, VB>(orow + VB * L.q[v], x);
     if (L.head_leader(A.s, v)) A.ds_src[j * A.s.H + L.k[v]] = SZ[v];
   }
 }
 
-template <typename T, int NV, bool kSub>
+template <typename T, int NV, int VB, bool kSub>
 __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(const BwdArgs A) {
-  constexpr int V = VecOf<T>::n;
+  constexpr int V = ElemsOf<T, VB>::n;
+  constexpr int U = UnrollOf<VB>::value;
   const DirArgs& D = A.csc;
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
@@ -469,11 +479,13 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
       if (idx >= D.n_items) break;
       const int4 it = D.items[idx];
       if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
-      const int per = (it.z - it.y + kWarps - 1) / kWarps;
-      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
-      int in[kUnroll];
-      batch_ids<kUnroll>(cols, it.y & ~3, wb, we, L.g, L.G, in);
-      src_node<T, NV>(A, L, it.x, cols, it.y & ~3, wb, we, true, 0, in, acc, SZ);
+      // batches of kUnroll * G edges dealt to the warps in turn
+      const int batch = U * L.G;
+      const int wb = it.y + wid * batch;
+      int in[U];
+      batch_ids<U>(cols, it.y & ~3, wb, it.z, L.g, L.G, in);
+      src_node<T, NV, VB>(A, L, it.x, cols, it.y & ~3, wb, it.z, true, kWarps * batch, 0, in, acc,
+                          SZ);
       if (L.g == 0)
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
@@ -498,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
           }
         }
         if (it.w < 0) {
-          write_src<T, NV>(A, L, it.x, acc, SZ);
+          write_src<T, NV, VB>(A, L, it.x, acc, SZ);
         } else {
 #pragma unroll
           for (int v = 0; v < NV; ++v) {
@@ -538,13 +550,13 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
         const int e0 = __shfl_sync(kFull, my_e, src);  // every lane shuffles
         const int end = j >= 0 ? e0 : beg;
         if (!__any_sync(kFull, j >= 0)) break;
-        int trips = (end - beg + kUnroll - 1) / kUnroll;
+        int trips = (end - beg + U - 1) / U;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
-        int in[kUnroll];
-        batch_ids<kUnroll>(D.idx, 0, beg, end, 0, 1, in);
-        src_node<T, NV>(A, L, j >= 0 ? j : 0, D.idx, 0, beg, end, false, trips, in, acc, SZ);
-        if (j >= 0) write_src<T, NV>(A, L, j, acc, SZ);
+        int in[U];
+        batch_ids<U>(D.idx, 0, beg, end, 0, 1, in);
+        src_node<T, NV, VB>(A, L, j >= 0 ? j : 0, D.idx, 0, beg, end, false, 0, trips, in, acc, SZ);
+        if (j >= 0) write_src<T, NV, VB>(A, L, j, acc, SZ);
       }
     }
     return;
@@ -564,22 +576,22 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<NV>::value) bwd_src_main(c
     }
     int j = __shfl_sync(kFull, my_j, 0);
     int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
-    int in[kUnroll];
-    batch_ids<kUnroll>(D.idx, 0, beg, end, L.g, L.G, in);
+    int in[U];
+    batch_ids<U>(D.idx, 0, beg, end, L.g, L.G, in);
     for (int q = 0; q < kGrab && j >= 0; ++q) {
       const int nq = (q + 1) & (kGrab - 1);
       const int j2 = q + 1 < kGrab ? __shfl_sync(kFull, my_j, nq) : -1;
       const int b2 = __shfl_sync(kFull, my_b, nq);
       const int e2 = __shfl_sync(kFull, my_e, nq);
-      int in2[kUnroll];
-      batch_ids<kUnroll>(D.idx, 0, b2, j2 >= 0 ? e2 : b2, L.g, L.G, in2);
-      src_node<T, NV>(A, L, j, D.idx, 0, beg, end, true, 0, in, acc, SZ);
-      if (L.g == 0) write_src<T, NV>(A, L, j, acc, SZ);
+      int in2[U];
+      batch_ids<U>(D.idx, 0, b2, j2 >= 0 ? e2 : b2, L.g, L.G, in2);
+      src_node<T, NV, VB>(A, L, j, D.idx, 0, beg, end, true, U * L.G, 0, in, acc, SZ);
+      if (L.g == 0) write_src<T, NV, VB>(A, L, j, acc, SZ);
       j = j2;
       beg = b2;
       end = e2;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) in[u] = in2[u];
+      for (int u = 0; u < U; ++u) in[u] = in2[u];
     }
   }
 }
@@ -614,7 +626,7 @@ __global__ void __launch_bounds__(kThreads) bwd_src_merge(const BwdArgs A) {
       }
     }
   }
-  write_src<T, NV>(A, L, hb.x, acc, SZ);
+  write_src<T, NV, 16>(A, L, hb.x, acc, SZ);
 }
 
 // ---------------------------------------------------------------------------
@@ -715,23 +727,63 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
 }
 
+// Launch a kernel template instantiated for the 16-byte lane geometry M.s.
+template <typename T, template <typename, int> class K>
+cudaError_t launch16(const BwdArgs& M, unsigned grid, size_t smem, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  switch (M.s.nv) {
+    case 1: e = K<T, 1>::launch(M, grid, smem, st); break;
+    case 2: e = K<T, 2>::launch(M, grid, smem, st); break;
+    default: e = K<T, 4>::launch(M, grid, smem, st); break;
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <typename T, int NV>
-cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t st,
-                     const cudaEvent_t* ev, bool reuse_scores) {
-  constexpr int V = VecOf<T>::n;
-  const int H = A.s.H, row_f = A.s.rv * V;
+struct DstMerge {
+  static cudaError_t launch(const BwdArgs& M, unsigned grid, size_t, cudaStream_t st) {
+    bwd_dst_merge<T, NV><<<grid, kThreads, 0, st>>>(M);
+    return cudaSuccess;
+  }
+};
+template <typename T, int NV>
+struct SrcMerge {
+  static cudaError_t launch(const BwdArgs& M, unsigned grid, size_t, cudaStream_t st) {
+    bwd_src_merge<T, NV><<<grid, kThreads, 0, st>>>(M);
+    return cudaSuccess;
+  }
+};
+template <typename T, int NV>
+struct DaPartial {
+  static cudaError_t launch(const BwdArgs& M, unsigned grid, size_t smem, cudaStream_t st) {
+    cudaError_t e = set_smem(da_partial<T, NV>, smem);
+    if (e != cudaSuccess) return e;
+    da_partial<T, NV><<<grid, kThreads, smem, st>>>(M);
+    return cudaSuccess;
+  }
+};
+
+// A.s is the lane geometry of the two main kernels (VB-byte lane vectors);
+// s16 the one of 16-byte vectors, used by the score pre-pass, the hub merges
+// and the attention-vector gradients.
+template <typename T, int NV, int VB>
+cudaError_t launch_t(const BwdArgs& A, const Shape& s16, gnn_dtype dt, int sm_count,
+                     cudaStream_t st, const cudaEvent_t* ev, bool reuse_scores) {
+  const int H = A.s.H, row_f = A.s.H * A.s.D;
+  BwdArgs M = A;
+  M.s = s16;
   cudaError_t e;
   auto mark = [&](int k) {
     if (ev) cudaEventRecord(ev[k], st);
   };
   if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), st)) != cudaSuccess) return e;
-  // rows narrower than a warp: light nodes one sub-group each (only NV = 1:
-  // rows of more than 512 bytes always fill the warp)
+  // rows narrower than a warp: light nodes one sub-group each (NV = 1)
   const bool sub = NV == 1 && A.s.lpr < 32;
   mark(0);
   // the forward call left the same scores at the same place in ws
   if (!reuse_scores &&
-      (e = launch_node_scores(A.s, dt, A.h, A.a_src, A.a_dst, A.n, const_cast<float*>(A.ssrc),
+      (e = launch_node_scores(s16, dt, A.h, A.a_src, A.a_dst, A.n, const_cast<float*>(A.ssrc),
                               const_cast<float*>(A.sdst), sm_count, st)) != cudaSuccess)
     return e;
   mark(1);
@@ -740,7 +792,7 @@ cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t 
     const int64_t work = A.csr.n_items + (A.csr.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
     const size_t smem = size_t(A.csr.col_off) + size_t(kWarps) * H * 3 * 4;
     if (work > 0) {
-      auto kernel = sub ? bwd_dst_main<T, NV, NV == 1> : bwd_dst_main<T, NV, false>;
+      auto kernel = sub ? bwd_dst_main<T, NV, VB, NV == 1> : bwd_dst_main<T, NV, VB, false>;
       if ((e = set_smem(kernel, smem)) != cudaSuccess) return e;
       const int64_t cap = persistent_blocks(kernel, smem, sm_count);
       const int64_t blocks = work < cap ? work : cap;
@@ -748,10 +800,10 @@ cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t 
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     mark(2);
-    if (A.csr.n_hubs > 0) {
-      bwd_dst_merge<T, NV><<<unsigned((A.csr.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if (A.csr.n_hubs > 0 &&
+        (e = launch16<T, DstMerge>(M, unsigned((A.csr.n_hubs + kWarps - 1) / kWarps), 0, st)) !=
+            cudaSuccess)
+      return e;
     mark(3);
   }
   // pass 2
@@ -759,7 +811,7 @@ cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t 
     const int64_t work = A.csc.n_items + (A.csc.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
     const size_t smem = size_t(A.csc.col_off) + size_t(kWarps) * (H + row_f) * 4;
     if (work > 0) {
-      auto kernel = sub ? bwd_src_main<T, NV, NV == 1> : bwd_src_main<T, NV, false>;
+      auto kernel = sub ? bwd_src_main<T, NV, VB, NV == 1> : bwd_src_main<T, NV, VB, false>;
       if ((e = set_smem(kernel, smem)) != cudaSuccess) return e;
       const int64_t cap = persistent_blocks(kernel, smem, sm_count);
       const int64_t blocks = work < cap ? work : cap;
@@ -767,18 +819,16 @@ cudaError_t launch_t(const BwdArgs& A, gnn_dtype dt, int sm_count, cudaStream_t 
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     mark(4);
-    if (A.csc.n_hubs > 0) {
-      bwd_src_merge<T, NV><<<unsigned((A.csc.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if (A.csc.n_hubs > 0 &&
+        (e = launch16<T, SrcMerge>(M, unsigned((A.csc.n_hubs + kWarps - 1) / kWarps), 0, st)) !=
+            cudaSuccess)
+      return e;
     mark(5);
   }
   // attention-vector gradients
   {
-    const size_t smem = size_t(kWarps) * (32 / A.s.lpr) * 2 * row_f * 4;
-    if ((e = set_smem(da_partial<T, NV>, smem)) != cudaSuccess) return e;
-    da_partial<T, NV><<<unsigned(A.da_blocks), kThreads, smem, st>>>(A);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t smem = size_t(kWarps) * (32 / s16.lpr) * 2 * row_f * 4;
+    if ((e = launch16<T, DaPartial>(M, unsigned(A.da_blocks), smem, st)) != cudaSuccess) return e;
     mark(6);
     da_final<<<unsigned((2 * row_f + kWarps - 1) / kWarps), kThreads, 0, st>>>(
         A.da_part, A.da_blocks, row_f, A.da_src, A.da_dst);
@@ -834,17 +884,25 @@ cudaError_t launch_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt, co
   A.da_blocks = L.da_blocks;
   A.ctr = reinterpret_cast<int*>(ws + L.bwd_ctr);
   A.err = g->err;
+  // 32-byte lane vectors where a head spans 32 bytes or more, the row fits
+  // one warp and the gathered and own rows start on 32-byte boundaries
+  Shape w;
+  if (make_wide_shape(s, &w) && aligned32(h) && aligned32(dout)) {
+    A.s = w;
+    if (dt == GNN_F32) return launch_t<float, 1, 32>(A, s, dt, g->sm_count, st, ev, reuse_scores);
+    return launch_t<__nv_bfloat16, 1, 32>(A, s, dt, g->sm_count, st, ev, reuse_scores);
+  }
   if (dt == GNN_F32) {
     switch (s.nv) {
-      case 1: return launch_t<float, 1>(A, dt, g->sm_count, st, ev, reuse_scores);
-      case 2: return launch_t<float, 2>(A, dt, g->sm_count, st, ev, reuse_scores);
-      case 4: return launch_t<float, 4>(A, dt, g->sm_count, st, ev, reuse_scores);
+      case 1: return launch_t<float, 1, 16>(A, s, dt, g->sm_count, st, ev, reuse_scores);
+      case 2: return launch_t<float, 2, 16>(A, s, dt, g->sm_count, st, ev, reuse_scores);
+      case 4: return launch_t<float, 4, 16>(A, s, dt, g->sm_count, st, ev, reuse_scores);
     }
   } else {
     switch (s.nv) {
-      case 1: return launch_t<__nv_bfloat16, 1>(A, dt, g->sm_count, st, ev, reuse_scores);
-      case 2: return launch_t<__nv_bfloat16, 2>(A, dt, g->sm_count, st, ev, reuse_scores);
-      case 4: return launch_t<__nv_bfloat16, 4>(A, dt, g->sm_count, st, ev, reuse_scores);
+      case 1: return launch_t<__nv_bfloat16, 1, 16>(A, s, dt, g->sm_count, st, ev, reuse_scores);
+      case 2: return launch_t<__nv_bfloat16, 2, 16>(A, s, dt, g->sm_count, st, ev, reuse_scores);
+      case 4: return launch_t<__nv_bfloat16, 4, 16>(A, s, dt, g->sm_count, st, ev, reuse_scores);
     }
   }
   return cudaErrorInvalidValue;

@@ -54,10 +54,10 @@ struct FwdArgs {
   int col_off;       // bytes of shared memory before the per-warp states
 };
 
-// Running softmax state of the vectors a lane owns.
-template <typename T, int NV>
+// Running softmax state of the vectors a lane owns (VB-byte lane vectors).
+template <typename T, int NV, int VB = 16>
 struct Online {
-  static constexpr int V = VecOf<T>::n;
+  static constexpr int V = ElemsOf<T, VB>::n;
   float m[NV], l[NV], acc[NV][V];
 
   __device__ __forceinline__ void init() {
@@ -98,35 +98,37 @@ struct Online {
   }
 };
 
-// Stream the edges beg + sg, beg + sg + SG, ... < end through the online
-// softmax, kUnroll edges per lane and batch: until end (kFixed false; every
-// lane of the warp then has the same beg and end), or for exactly `trips`
-// batches (kFixed true; the same count on every lane, batches past end
-// change nothing).
+// Stream edges through the online softmax, kUnroll edges per lane and batch:
+// the batch at `base` holds edges base + sg + u * SG (u < kUnroll), and the
+// next batch starts `step` edges further (SG * kUnroll when one warp takes
+// every batch, more when the batches are dealt out to several warps).  Runs
+// until end (kFixed false; every lane of the warp then has the same beg and
+// end), or for exactly `trips` batches (kFixed true; the same count on every
+// lane, batches past end change nothing).
 // cols[x - colbase] is the source of edge x; jn holds the sources of the
 // first batch (already loaded).
-template <typename T, int NV, bool kFixed>
+template <typename T, int NV, int VB, bool kFixed>
 __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
-                                          int sg, int SG, int trips, int (&jn)[kUnroll],
-                                          const float (&sd2)[NV], Online<T, NV>& st) {
-  constexpr int V = VecOf<T>::n;
-  constexpr int U = kUnroll;
-  const int step = SG * U;
+                                          int sg, int SG, int step, int trips,
+                                          int (&jn)[UnrollOf<VB>::value], const float (&sd2)[NV],
+                                          Online<T, NV, VB>& st) {
+  constexpr int V = ElemsOf<T, VB>::n;
+  constexpr int U = UnrollOf<VB>::value;
   const int H = A.s.H;
   int base = beg;
   for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
-    uint4 raw[U][NV];
+    RawV<VB> raw[U][NV];
     float sc[U * NV];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         const bool ok = j[u] >= 0 && L.ok[v];
-        raw[u][v] = ok ? ld16(row_base<T>(A.h, j[u], A.s.rv) + 16 * L.q[v]) : make_uint4(0, 0, 0, 0);
+        raw[u][v] = ok ? ldv<VB>(row_at<VB>(A.h, j[u], A.s.rv) + VB * L.q[v]) : zero_raw<VB>();
         sc[u * NV + v] = ok ? __ldg(A.ssrc + int64_t(j[u]) * H + L.k[v]) : 0.f;
       }
     if (kFixed ? t + 1 < trips : base + step < end)
@@ -154,7 +156,7 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
         const float pu = ex2(sc[u * NV + v] - mr);
         st.l[v] += pu;
         float x[V];
-        unpack<T>(raw[u][v], x);
+        unpackv<T, VB>(raw[u][v], x);
         axpy<V>(st.acc[v], pu, x);
       }
       st.m[v] = mn;
@@ -162,14 +164,14 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
   }
 }
 
-// The edges beg + g, beg + g + G, ... < end of one node, spread over the
-// warp's sub-groups (every lane sees the same beg and end).
-template <typename T, int NV>
+// The edges of one node from beg on, spread over the warp's sub-groups
+// (every lane sees the same beg and end), batches `step` edges apart.
+template <typename T, int NV, int VB>
 __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
-                                          int (&jn)[kUnroll], const float (&sd2)[NV],
-                                          Online<T, NV>& st) {
-  fwd_edges<T, NV, false>(A, L, cols, colbase, beg, end, L.g, L.G, 0, jn, sd2, st);
+                                          int step, int (&jn)[UnrollOf<VB>::value],
+                                          const float (&sd2)[NV], Online<T, NV, VB>& st) {
+  fwd_edges<T, NV, VB, false>(A, L, cols, colbase, beg, end, L.g, L.G, step, 0, jn, sd2, st);
 }
 
 // This lane's base-2 destination score halves of node i.
@@ -181,11 +183,11 @@ __device__ __forceinline__ void node_sdst(const FwdArgs& A, const Lane<NV>& L, i
 }
 
 // out = acc / l, lse = (m + log2 l) ln 2; a node without edges gets 0 and -inf.
-template <typename T, int NV>
+template <typename T, int NV, int VB>
 __device__ __forceinline__ void write_node(const FwdArgs& A, const Lane<NV>& L, int64_t node,
-                                           const Online<T, NV>& st) {
-  constexpr int V = VecOf<T>::n;
-  char* orow = reinterpret_cast<char*>(A.out) + node * int64_t(A.s.rv) * 16;
+                                           const Online<T, NV, VB>& st) {
+  constexpr int V = ElemsOf<T, VB>::n;
+  char* orow = reinterpret_cast<char*>(A.out) + node * int64_t(A.s.rv) * VB;
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     if (!L.ok[v]) continue;
@@ -194,7 +196,7 @@ __device__ __forceinline__ void write_node(const FwdArgs& A, const Lane<NV>& L, 
 #pragma unroll
     for (int c = 0; c < V; ++c) x[c] = st.acc[v][c];
     scale<V>(x, inv);
-    st16(orow + 16 * L.q[v], pack<T>(x));
+    storev<T, VB>(orow + VB * L.q[v], x);
     if (L.head_leader(A.s, v))
       A.lse[node * A.s.H + L.k[v]] =
           st.l[v] > 0.f ? (st.m[v] + __log2f(st.l[v])) * kLn2 : -INFINITY;
@@ -202,10 +204,11 @@ __device__ __forceinline__ void write_node(const FwdArgs& A, const Lane<NV>& L, 
 }
 
 // One block item: a whole mid node (slot < 0) or one chunk of a hub.
-template <typename T, int NV>
+template <typename T, int NV, int VB>
 __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, int wid,
                                          const int4 it, unsigned char* smem, uint32_t& parity) {
-  constexpr int V = VecOf<T>::n;
+  constexpr int V = ElemsOf<T, VB>::n;
+  constexpr int U = UnrollOf<VB>::value;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
   int32_t* cols = reinterpret_cast<int32_t*>(smem + 16);
   float* wm = reinterpret_cast<float*>(smem + A.col_off);
@@ -214,17 +217,18 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, in
   const int row_f = A.s.rv * V;
   const int i = it.x, beg = it.y, end = it.z, slot = it.w;
   if (!stage_edges(cols, A.idx, beg, end, bar, parity, A.err)) return false;
-  const int len = end - beg;
-  const int per = (len + kWarps - 1) / kWarps;
-  const int wb = min(end, beg + wid * per), we = min(end, wb + per);
+  // batches of kUnroll * G edges are dealt to the warps in turn: warp w
+  // takes batches w, w + kWarps, ... (at most one batch of padding per item)
+  const int batch = U * L.G;
+  const int wb = beg + wid * batch;
   const int colbase = beg & ~3;
-  int jn[kUnroll];
-  batch_ids<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
+  int jn[U];
+  batch_ids<U>(cols, colbase, wb, end, L.g, L.G, jn);
   float sd2[NV];
   node_sdst<NV>(A, L, i, sd2);
-  Online<T, NV> st;
+  Online<T, NV, VB> st;
   st.init();
-  fwd_edges<T, NV>(A, L, cols, colbase, wb, we, jn, sd2, st);
+  fwd_edges<T, NV, VB>(A, L, cols, colbase, wb, end, kWarps * batch, jn, sd2, st);
   st.merge_subgroups(A.s);
   if (L.g == 0) {
 #pragma unroll
@@ -241,7 +245,7 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, in
   __syncthreads();
   if (wid == 0 && L.g == 0) {
     // warp 0 folds the warps' states in warp order
-    Online<T, NV> tot;
+    Online<T, NV, VB> tot;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       tot.m[v] = L.ok[v] ? wm[L.k[v]] : -INFINITY;
@@ -260,7 +264,7 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, in
       }
     }
     if (slot < 0) {
-      write_node<T, NV>(A, L, i, tot);
+      write_node<T, NV, VB>(A, L, i, tot);
     } else {
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
@@ -282,8 +286,9 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& A, const Lane<NV>& L, in
 // kSub: light nodes take one sub-group each (rows narrower than a warp);
 // otherwise one warp each.  Two instantiations keep each loop's register
 // allocation its own.
-template <typename T, int NV, bool kSub>
+template <typename T, int NV, int VB, bool kSub>
 __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) fwd_main(const FwdArgs A) {
+  constexpr int U = UnrollOf<VB>::value;
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -298,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) fwd_main(c
       __syncthreads();
       const int it = s_item;
       if (it >= A.n_items) break;
-      if (!fwd_item<T, NV>(A, L, wid, A.items[it], smem, parity)) return;
+      if (!fwd_item<T, NV, VB>(A, L, wid, A.items[it], smem, parity)) return;
     }
   }
 
@@ -326,17 +331,17 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) fwd_main(c
         const int e0 = __shfl_sync(kFull, my_e, src);  // every lane shuffles
         const int end = i >= 0 ? e0 : beg;
         if (!__any_sync(kFull, i >= 0)) break;
-        int trips = (end - beg + kUnroll - 1) / kUnroll;
+        int trips = (end - beg + U - 1) / U;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
-        int jn[kUnroll];
-        batch_ids<kUnroll>(A.idx, 0, beg, end, 0, 1, jn);
+        int jn[U];
+        batch_ids<U>(A.idx, 0, beg, end, 0, 1, jn);
         float sd2[NV];
         node_sdst<NV>(A, L, i >= 0 ? i : 0, sd2);
-        Online<T, NV> st;
+        Online<T, NV, VB> st;
         st.init();
-        fwd_edges<T, NV, true>(A, L, A.idx, 0, beg, end, 0, 1, trips, jn, sd2, st);
-        if (i >= 0) write_node<T, NV>(A, L, i, st);
+        fwd_edges<T, NV, VB, true>(A, L, A.idx, 0, beg, end, 0, 1, U, trips, jn, sd2, st);
+        if (i >= 0) write_node<T, NV, VB>(A, L, i, st);
       }
     }
     return;
@@ -356,28 +361,28 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) fwd_main(c
     }
     int i = __shfl_sync(kFull, my_i, 0);
     int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
-    int jn[kUnroll];
-    batch_ids<kUnroll>(A.idx, 0, beg, end, L.g, L.G, jn);
+    int jn[U];
+    batch_ids<U>(A.idx, 0, beg, end, L.g, L.G, jn);
     for (int q = 0; q < kGrab && i >= 0; ++q) {
       // the next node's range and first sources, loaded while this one runs
       const int nq = (q + 1) & (kGrab - 1);
       const int i2 = q + 1 < kGrab ? __shfl_sync(kFull, my_i, nq) : -1;
       const int b2 = __shfl_sync(kFull, my_b, nq);
       const int e2 = __shfl_sync(kFull, my_e, nq);
-      int jn2[kUnroll];
-      batch_ids<kUnroll>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
+      int jn2[U];
+      batch_ids<U>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
       float sd2[NV];
       node_sdst<NV>(A, L, i, sd2);
-      Online<T, NV> st;
+      Online<T, NV, VB> st;
       st.init();
-      fwd_edges<T, NV>(A, L, A.idx, 0, beg, end, jn, sd2, st);
+      fwd_edges<T, NV, VB>(A, L, A.idx, 0, beg, end, U * L.G, jn, sd2, st);
       st.merge_subgroups(A.s);
-      if (L.g == 0) write_node<T, NV>(A, L, i, st);
+      if (L.g == 0) write_node<T, NV, VB>(A, L, i, st);
       i = i2;
       beg = b2;
       end = e2;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) jn[u] = jn2[u];
+      for (int u = 0; u < U; ++u) jn[u] = jn2[u];
     }
   }
 }
@@ -391,7 +396,7 @@ __global__ void __launch_bounds__(kThreads) fwd_merge(const FwdArgs A) {
   if (t >= A.n_hubs || L.g != 0) return;
   const int4 hb = A.hubs[t];
   const int row_f = A.s.rv * V;
-  Online<T, NV> st;
+  Online<T, NV, 16> st;
   st.init();
   for (int c = 0; c < hb.z; ++c) {
     const int64_t slot = int64_t(hb.y) + c;
@@ -412,24 +417,38 @@ __global__ void __launch_bounds__(kThreads) fwd_merge(const FwdArgs A) {
       st.merge(v, ml.x, ml.y, ab);
     }
   }
-  write_node<T, NV>(A, L, hb.x, st);
+  write_node<T, NV, 16>(A, L, hb.x, st);
 }
 
-template <typename T, int NV>
-cudaError_t launch_t(const FwdArgs& A, gnn_dtype dt, const float* a_src, const float* a_dst,
-                     int64_t n, int sm_count, cudaStream_t stream, const cudaEvent_t* ev) {
-  constexpr int V = VecOf<T>::n;
+template <typename T>
+cudaError_t launch_merge(const FwdArgs& M, cudaStream_t stream) {
+  const unsigned grid = unsigned((M.n_hubs + kWarps - 1) / kWarps);
+  switch (M.s.nv) {
+    case 1: fwd_merge<T, 1><<<grid, kThreads, 0, stream>>>(M); break;
+    case 2: fwd_merge<T, 2><<<grid, kThreads, 0, stream>>>(M); break;
+    default: fwd_merge<T, 4><<<grid, kThreads, 0, stream>>>(M); break;
+  }
+  return cudaGetLastError();
+}
+
+// A.s is the lane geometry of the main kernel (VB-byte lane vectors); s16
+// the one of 16-byte vectors, used by the score pre-pass and the hub merge.
+template <typename T, int NV, int VB>
+cudaError_t launch_t(const FwdArgs& A, const Shape& s16, gnn_dtype dt, const float* a_src,
+                     const float* a_dst, int64_t n, int sm_count, cudaStream_t stream,
+                     const cudaEvent_t* ev) {
   cudaError_t e;
   if ((e = cudaMemsetAsync(A.ctr, 0, kCounters * sizeof(int), stream)) != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[0], stream);
-  if ((e = launch_node_scores(A.s, dt, A.h, a_src, a_dst, n, const_cast<float*>(A.ssrc),
+  if ((e = launch_node_scores(s16, dt, A.h, a_src, a_dst, n, const_cast<float*>(A.ssrc),
                               const_cast<float*>(A.sdst), sm_count, stream)) != cudaSuccess)
     return e;
   if (ev) cudaEventRecord(ev[1], stream);
   if (A.n_items + A.n_light > 0) {
-    const size_t smem = size_t(A.col_off) + size_t(kWarps) * (2 * A.s.H + A.s.rv * V) * 4;
-    // rows of more than 512 bytes always fill the warp (NV > 1)
-    auto kernel = (NV == 1 && A.s.lpr < 32) ? fwd_main<T, NV, NV == 1> : fwd_main<T, NV, false>;
+    const size_t smem = size_t(A.col_off) + size_t(kWarps) * (2 * A.s.H + A.s.H * A.s.D) * 4;
+    // rows that do not fill the warp give each light node a sub-group (NV = 1)
+    auto kernel = (NV == 1 && A.s.lpr < 32) ? fwd_main<T, NV, VB, NV == 1>
+                                             : fwd_main<T, NV, VB, false>;
     if (smem > 48 * 1024 &&
         (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(smem))) != cudaSuccess)
@@ -442,8 +461,9 @@ cudaError_t launch_t(const FwdArgs& A, gnn_dtype dt, const float* a_src, const f
   }
   if (ev) cudaEventRecord(ev[2], stream);
   if (A.n_hubs > 0) {
-    fwd_merge<T, NV><<<unsigned((A.n_hubs + kWarps - 1) / kWarps), kThreads, 0, stream>>>(A);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    FwdArgs M = A;
+    M.s = s16;
+    if ((e = launch_merge<T>(M, stream)) != cudaSuccess) return e;
   }
   if (ev) cudaEventRecord(ev[3], stream);
   return cudaGetLastError();
@@ -476,17 +496,29 @@ cudaError_t launch_forward(const gnn_graph* g, const Shape& s, gnn_dtype dt, con
   A.ctr = reinterpret_cast<int*>(ws + L.fwd_ctr);
   A.err = g->err;
   A.col_off = int(16 + align_up(size_t(g->csr.max_item + 4) * 4, 16));
+  // 32-byte lane vectors where a head spans 32 bytes or more, the row fits
+  // one warp and the feature rows start on 32-byte boundaries
+  Shape w;
+  if (make_wide_shape(s, &w) && aligned32(h)) {
+    A.s = w;
+    if (dt == GNN_F32)
+      return launch_t<float, 1, 32>(A, s, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+    return launch_t<__nv_bfloat16, 1, 32>(A, s, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+  }
   if (dt == GNN_F32) {
     switch (s.nv) {
-      case 1: return launch_t<float, 1>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
-      case 2: return launch_t<float, 2>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
-      case 4: return launch_t<float, 4>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+      case 1: return launch_t<float, 1, 16>(A, s, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+      case 2: return launch_t<float, 2, 16>(A, s, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+      case 4: return launch_t<float, 4, 16>(A, s, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
     }
   } else {
     switch (s.nv) {
-      case 1: return launch_t<__nv_bfloat16, 1>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
-      case 2: return launch_t<__nv_bfloat16, 2>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
-      case 4: return launch_t<__nv_bfloat16, 4>(A, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+      case 1:
+        return launch_t<__nv_bfloat16, 1, 16>(A, s, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+      case 2:
+        return launch_t<__nv_bfloat16, 2, 16>(A, s, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
+      case 4:
+        return launch_t<__nv_bfloat16, 4, 16>(A, s, dt, a_src, a_dst, g->n, g->sm_count, st, ev);
     }
   }
   return cudaErrorInvalidValue;

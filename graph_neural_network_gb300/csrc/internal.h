@@ -70,6 +70,10 @@ struct WsLayout {
 constexpr int kCounters = 8;
 
 bool make_shape(int H, int D, gnn_dtype dt, Shape* s);
+// The geometry of 32-byte lane vectors for the same rows (false when a head
+// spans less than 32 bytes or a row more than 1024).
+bool make_wide_shape(const Shape& s, Shape* w);
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 WsLayout ws_layout(const gnn_graph* g, const Shape& s);
 
 // Kernel launchers (gat_fwd.cu, gat_bwd.cu); return the launch error.

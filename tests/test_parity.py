@@ -6,7 +6,8 @@ import torch
 
 import workload
 from workload import testgraphs
-from gpu_util import assert_close, compare, device_graph, make_case, run_gpu, run_oracle, to_device
+from gpu_util import (assert_close, compare, device_graph, make_case, run_gpu, run_oracle,
+                      to_device, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -174,3 +175,37 @@ def test_autograd_function():
     assert_close(h.grad.cpu().numpy(), ref["dh"], "f32", ref["dh_mag"], "autograd dh")
     assert_close(a_s.grad.cpu().numpy(), ref["da_src"], "f32", ref["da_src_mag"], "da_src")
     assert_close(a_d.grad.cpu().numpy(), ref["da_dst"], "f32", ref["da_dst_mag"], "da_dst")
+
+
+def _offset_copy(x, dtype):
+    """x on the device at an address 16 bytes past a 32-byte boundary."""
+    t = to_device(x, dtype)
+    pad = 16 // t.element_size()
+    buf = torch.empty(t.numel() + pad, dtype=t.dtype, device="cuda")
+    view = buf[pad:].view(t.shape)
+    view.copy_(t)
+    assert view.data_ptr() % 32 == 16
+    return view
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rows_off_32_byte_boundaries_take_16_byte_vectors(dtype):
+    """Heads of 64 bytes or more run with 32-byte lane vectors when the rows
+    start on 32-byte boundaries, else with 16-byte ones; both against the
+    oracle, on the same graph."""
+    import graph_neural_network_gb300 as gnn
+    rp, ci = testgraphs.with_in_degrees(THRESHOLD_DEGREES, n_nodes=2500, seed=59)
+    D = 32 if dtype == "f32" else 64
+    case = make_case(rp, ci, 2, D, dtype, 59)
+    ref = run_oracle(case)
+    g = device_graph(case, (8, 64, 16))
+    a_s = torch.from_numpy(case["a_src"]).cuda()
+    a_d = torch.from_numpy(case["a_dst"]).cuda()
+    for h, dout in ((to_device(case["h"], dtype), to_device(case["dout"], dtype)),
+                    (_offset_copy(case["h"], dtype), _offset_copy(case["dout"], dtype))):
+        out, lse = gnn.gat_forward(g, h, a_s, a_d, 0.2)
+        dh, da_s, da_d = gnn.gat_backward(g, h, a_s, a_d, 0.2, lse, dout)
+        torch.cuda.synchronize()
+        gpu = dict(out=to_f64(out), lse=to_f64(lse), dh=to_f64(dh), da_src=to_f64(da_s),
+                   da_dst=to_f64(da_d))
+        compare(gpu, ref, dtype, what=f"offset {h.data_ptr() % 32}")
