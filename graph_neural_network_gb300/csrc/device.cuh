@@ -417,6 +417,46 @@ __device__ __forceinline__ void storev(void* dst, const float (&x)[ElemsOf<T, VB
     st16(reinterpret_cast<char*>(dst) + 16, pack<T>(*reinterpret_cast<const float(*)[H16]>(p + H16)));
 }
 
+// a . b over the bfloat16 elements of two lane vectors in float32: every
+// product of two bfloat16 values is exact in float32, so each step is one
+// fused multiply-add of the widened values; even and odd elements go to two
+// sums added at the end (the same order as dot() on widened vectors, so the
+// result is bit for bit the same).
+template <int VB>
+__device__ __forceinline__ float dot_bf16(const RawV<VB>& a, const RawV<VB>& b) {
+  const uint32_t* pa = reinterpret_cast<const uint32_t*>(&a);
+  const uint32_t* pb = reinterpret_cast<const uint32_t*>(&b);
+  float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+  for (int w = 0; w < VB / 4; ++w)
+    asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %2;\n mov.b32 {bl, bh}, %3;\n"
+        " fma.rn.f32.bf16 %0, al, bl, %0;\n fma.rn.f32.bf16 %1, ah, bh, %1;\n}"
+        : "+f"(d0), "+f"(d1)
+        : "r"(pa[w]), "r"(pb[w]));
+  return d0 + d1;
+}
+
+// A node's own row vector that is dotted with one gathered vector per edge:
+// float32 rows are kept widened; bfloat16 rows stay packed and go through
+// dot_bf16 (no widening of either operand).
+template <typename T, int VB>
+struct OwnVec {
+  float x[ElemsOf<T, VB>::n];
+  __device__ __forceinline__ void set(const RawV<VB>& r) { unpackv<T, VB>(r, x); }
+  __device__ __forceinline__ float dot_with(const RawV<VB>& g) const {
+    constexpr int V = ElemsOf<T, VB>::n;
+    float y[V];
+    unpackv<T, VB>(g, y);
+    return dot<V>(y, x);
+  }
+};
+template <int VB>
+struct OwnVec<__nv_bfloat16, VB> {
+  RawV<VB> r;
+  __device__ __forceinline__ void set(const RawV<VB>& v) { r = v; }
+  __device__ __forceinline__ float dot_with(const RawV<VB>& g) const { return dot_bf16<VB>(g, r); }
+};
+
 template <int VB>
 __device__ __forceinline__ const char* row_at(const void* base, int64_t node, int rv) {
   return reinterpret_cast<const char*>(base) + node * int64_t(rv) * VB;

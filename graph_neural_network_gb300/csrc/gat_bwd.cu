@@ -83,7 +83,7 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
                                           int sg, int SG, int step, int trips,
                                           int (&jn)[UnrollOf<VB>::value],
-                                          const float (&gi)[NV][ElemsOf<T, VB>::n],
+                                          const OwnVec<T, VB> (&gi)[NV],
                                           const float (&sd2)[NV], const float (&lse2)[NV],
                                           float (&SA)[NV], float (&SB)[NV], float (&SD)[NV]) {
   constexpr int V = ElemsOf<T, VB>::n;
@@ -111,9 +111,7 @@ __device__ __forceinline__ void dst_edges(const BwdArgs& A, const Lane<NV>& L,
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
-        float x[V];
-        unpackv<T, VB>(raw[u][v], x);
-        dd[u * NV + v] = dot<V>(x, gi[v]);
+        dd[u * NV + v] = gi[v].dot_with(raw[u][v]);
       }
     head_sums<U * NV>(dd, A.s.hv_log2);
 #pragma unroll
@@ -143,10 +141,13 @@ __device__ __forceinline__ void dst_node(const BwdArgs& A, const Lane<NV>& L, in
                                          int (&jn)[UnrollOf<VB>::value], float (&sd2)[NV],
                                          float (&lse2)[NV], float (&SA)[NV], float (&SB)[NV],
                                          float (&SD)[NV]) {
-  constexpr int V = ElemsOf<T, VB>::n;
   constexpr int U = UnrollOf<VB>::value;
-  float gi[NV][V];
-  load_row_v<T, NV, VB>(A.dout, i, A.s, L, gi);
+  OwnVec<T, VB> gi[NV];
+  {
+    const char* row = row_at<VB>(A.dout, i, A.s.rv);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) gi[v].set(L.ok[v] ? ldv<VB>(row + VB * L.q[v]) : zero_raw<VB>());
+  }
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     sd2[v] = L.ok[v] ? __ldg(A.sdst + int64_t(i) * A.s.H + L.k[v]) : 0.f;
@@ -346,7 +347,7 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
                                           int sg, int SG, int step, int trips,
                                           int (&in)[UnrollOf<VB>::value],
-                                          const float (&xj)[NV][ElemsOf<T, VB>::n],
+                                          const OwnVec<T, VB> (&xj)[NV],
                                           const float (&ss2)[NV],
                                           float (&acc)[NV][ElemsOf<T, VB>::n], float (&SZ)[NV]) {
   constexpr int V = ElemsOf<T, VB>::n;
@@ -375,9 +376,7 @@ __device__ __forceinline__ void src_edges(const BwdArgs& A, const Lane<NV>& L,
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
-        float g[V];
-        unpackv<T, VB>(raw[u][v], g);
-        dd[u * NV + v] = dot<V>(g, xj[v]);
+        dd[u * NV + v] = xj[v].dot_with(raw[u][v]);
       }
     head_sums<U * NV>(dd, A.s.hv_log2);
 #pragma unroll
@@ -405,8 +404,13 @@ __device__ __forceinline__ void src_node(const BwdArgs& A, const Lane<NV>& L, in
                                          float (&acc)[NV][ElemsOf<T, VB>::n], float (&SZ)[NV]) {
   constexpr int V = ElemsOf<T, VB>::n;
   constexpr int U = UnrollOf<VB>::value;
-  float xj[NV][V], ss2[NV];
-  load_row_v<T, NV, VB>(A.h, j, A.s, L, xj);
+  OwnVec<T, VB> xj[NV];
+  float ss2[NV];
+  {
+    const char* row = row_at<VB>(A.h, j, A.s.rv);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) xj[v].set(L.ok[v] ? ldv<VB>(row + VB * L.q[v]) : zero_raw<VB>());
+  }
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     ss2[v] = L.ok[v] ? __ldg(A.ssrc + int64_t(j) * A.s.H + L.k[v]) : 0.f;
