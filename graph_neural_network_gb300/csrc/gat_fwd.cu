@@ -30,6 +30,9 @@ namespace gnn {
 namespace {
 
 constexpr int kGrab = 4;  // light nodes a warp takes per counter access
+// How far (base 2) a score may exceed the running state's reference value
+// before the state is rescaled to it.
+constexpr float kSlack = 16.f;
 
 struct FwdArgs {
   Shape s;
@@ -141,16 +144,34 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
         const float e = z > 0.f ? z : A.slope * z;
         sc[u * NV + v] = j[u] >= 0 ? e : -INFINITY;
       }
+    // The reference value m of the running state is raised only when a score
+    // exceeds it by more than kSlack (base 2), which after a node's first
+    // batch is rare: most batches skip rescaling the accumulator.  Weights
+    // stay below 2^kSlack, and out = acc / l, lse = m + log2 l hold for any
+    // reference value.  The vote keeps the branch uniform over the warp.
+    bool raise = false;
+    float bmx[NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       float bm = sc[v];
 #pragma unroll
       for (int u = 1; u < U; ++u) bm = fmaxf(bm, sc[u * NV + v]);
-      const float mn = fmaxf(st.m[v], bm);
-      const float mr = (mn == -INFINITY) ? 0.f : mn;
-      const float s0 = ex2(st.m[v] - mr);
-      st.l[v] *= s0;
-      scale<V>(st.acc[v], s0);
+      bmx[v] = bm;
+      raise |= bm > st.m[v] + kSlack;
+    }
+    if (__any_sync(kFull, raise)) {
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        if (!(bmx[v] > st.m[v] + kSlack)) continue;
+        const float s0 = ex2(st.m[v] - bmx[v]);
+        st.l[v] *= s0;
+        scale<V>(st.acc[v], s0);
+        st.m[v] = bmx[v];
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const float mr = (st.m[v] == -INFINITY) ? 0.f : st.m[v];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const float pu = ex2(sc[u * NV + v] - mr);
@@ -159,7 +180,6 @@ __device__ __forceinline__ void fwd_edges(const FwdArgs& A, const Lane<NV>& L,
         unpackv<T, VB>(raw[u][v], x);
         axpy<V>(st.acc[v], pu, x);
       }
-      st.m[v] = mn;
     }
   }
 }

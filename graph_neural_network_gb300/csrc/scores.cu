@@ -9,29 +9,29 @@ namespace {
 
 constexpr int kNodesPerIter = 4;  // node rows in flight per sub-group
 
-template <typename T, int NV>
+template <typename T, int NV, int VB>
 __global__ void __launch_bounds__(kThreads) node_scores(const Shape s, const void* h,
                                                         const float* a_src, const float* a_dst,
                                                         int64_t n, float* ssrc, float* sdst) {
-  constexpr int V = VecOf<T>::n;
-  constexpr int U = kNodesPerIter;
+  constexpr int V = ElemsOf<T, VB>::n;
+  constexpr int U = kNodesPerIter * 16 / VB;  // the same bytes in flight per lane
   const Lane<NV> L(s);
   float as2[NV][V], ad2[NV][V];
-  load_att<T, NV>(a_src, L, kLog2e, as2);
-  load_att<T, NV>(a_dst, L, kLog2e, ad2);
+  load_att_v<T, NV, VB>(a_src, L, kLog2e, as2);
+  load_att_v<T, NV, VB>(a_dst, L, kLog2e, ad2);
   const int64_t stride = int64_t(gridDim.x) * kWarps * L.G;
   // warp-uniform loop over groups of G consecutive nodes; sub-group g takes
   // node base + g of each group
   for (int64_t base = (int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * L.G; base < n;
        base += U * stride) {
-    uint4 raw[U][NV];
+    RawV<VB> raw[U][NV];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t node = base + u * stride + L.g;
 #pragma unroll
       for (int v = 0; v < NV; ++v)
-        raw[u][v] = (node < n && L.ok[v]) ? ld16(row_base<T>(h, node, s.rv) + 16 * L.q[v])
-                                          : make_uint4(0, 0, 0, 0);
+        raw[u][v] = (node < n && L.ok[v]) ? ldv<VB>(row_at<VB>(h, node, s.rv) + VB * L.q[v])
+                                          : zero_raw<VB>();
     }
     float d[2 * U * NV];
 #pragma unroll
@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kThreads) node_scores(const Shape s, const voi
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         float x[V];
-        unpack<T>(raw[u][v], x);
+        unpackv<T, VB>(raw[u][v], x);
         d[u * NV + v] = dot<V>(x, as2[v]);
         d[U * NV + u * NV + v] = dot<V>(x, ad2[v]);
       }
@@ -58,15 +58,16 @@ __global__ void __launch_bounds__(kThreads) node_scores(const Shape s, const voi
   }
 }
 
-template <typename T, int NV>
+template <typename T, int NV, int VB>
 cudaError_t launch_t(const Shape& s, const void* h, const float* a_src, const float* a_dst,
                      int64_t n, float* ssrc, float* sdst, int sm_count, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  const int64_t per_block = int64_t(kWarps) * (32 >> s.lpr_log2) * kNodesPerIter;
+  const int64_t per_block = int64_t(kWarps) * (32 >> s.lpr_log2) * (kNodesPerIter * 16 / VB);
   int64_t blocks = (n + per_block - 1) / per_block;
   const int64_t cap = int64_t(sm_count > 0 ? sm_count : 1) * 8;
   if (blocks > cap) blocks = cap;
-  node_scores<T, NV><<<unsigned(blocks), kThreads, 0, st>>>(s, h, a_src, a_dst, n, ssrc, sdst);
+  node_scores<T, NV, VB><<<unsigned(blocks), kThreads, 0, st>>>(s, h, a_src, a_dst, n, ssrc,
+                                                                sdst);
   return cudaGetLastError();
 }
 
@@ -75,17 +76,27 @@ cudaError_t launch_t(const Shape& s, const void* h, const float* a_src, const fl
 cudaError_t launch_node_scores(const Shape& s, gnn_dtype dt, const void* h, const float* a_src,
                                const float* a_dst, int64_t n, float* ssrc, float* sdst,
                                int sm_count, cudaStream_t st) {
+  // 32-byte lane vectors where the attention kernels use them
+  Shape w;
+  if (make_wide_shape(s, &w) && aligned32(h)) {
+    if (dt == GNN_F32)
+      return launch_t<float, 1, 32>(w, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
+    return launch_t<__nv_bfloat16, 1, 32>(w, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
+  }
   if (dt == GNN_F32) {
     switch (s.nv) {
-      case 1: return launch_t<float, 1>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
-      case 2: return launch_t<float, 2>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
-      case 4: return launch_t<float, 4>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
+      case 1: return launch_t<float, 1, 16>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
+      case 2: return launch_t<float, 2, 16>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
+      case 4: return launch_t<float, 4, 16>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
     }
   } else {
     switch (s.nv) {
-      case 1: return launch_t<__nv_bfloat16, 1>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
-      case 2: return launch_t<__nv_bfloat16, 2>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
-      case 4: return launch_t<__nv_bfloat16, 4>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
+      case 1:
+        return launch_t<__nv_bfloat16, 1, 16>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
+      case 2:
+        return launch_t<__nv_bfloat16, 2, 16>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
+      case 4:
+        return launch_t<__nv_bfloat16, 4, 16>(s, h, a_src, a_dst, n, ssrc, sdst, sm_count, st);
     }
   }
   return cudaErrorInvalidValue;
