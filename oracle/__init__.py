@@ -53,11 +53,11 @@ def _bind(path: str):
     lib.oracle_gat_forward.restype = i32
     lib.oracle_gat_node_stats.argtypes = common + [P, i64, P, P, P, P]
     lib.oracle_gat_node_stats.restype = i32
-    lib.oracle_gat_backward.argtypes = common + [P, P, P, P, P, P]
+    lib.oracle_gat_backward.argtypes = common + [P, P, P, P, P, P, P, P]
     lib.oracle_gat_backward.restype = i32
-    lib.oracle_gat_backward_rows.argtypes = common + [P, i64, P, P, P]
+    lib.oracle_gat_backward_rows.argtypes = common + [P, i64, P, P, P, P]
     lib.oracle_gat_backward_rows.restype = i32
-    lib.oracle_gat_att_grads.argtypes = common + [P, P, P, P]
+    lib.oracle_gat_att_grads.argtypes = common + [P, P, P, P, P]
     lib.oracle_gat_att_grads.restype = i32
     spmm = [i64, P, P, i64, i32, P, i32]
     lib.oracle_spmm_forward.argtypes = spmm + [i64, P, P, P]
@@ -173,7 +173,11 @@ class Oracle:
         _check(rc, "node_stats")
         return dict(lse=lse, delta=delta, ds_dst=ds)
 
-    def backward(self, row_ptr, col, h, a_src, a_dst, slope, dout, with_mag=False):
+    def backward(self, row_ptr, col, h, a_src, a_dst, slope, dout, with_mag=False,
+                 with_kink=False):
+        """Whole-graph backward.  with_kink adds, per element, how far dh and da
+        can move between the two LeakyReLU derivatives of edges whose z lies
+        within float32 rounding of the kink (dh_kink, da_src_kink, da_dst_kink)."""
         row_ptr, col, h, a_src, a_dst, n, H, D, dt = _prep(row_ptr, col, h, a_src, a_dst)
         dout = np.ascontiguousarray(dout)
         assert dout.shape == h.shape and dout.dtype == h.dtype
@@ -182,15 +186,21 @@ class Oracle:
         da_dst = np.empty((H, D), np.float64)
         dh_mag = np.empty((n, H, D), np.float64) if with_mag else None
         da_mag = np.empty((2, H, D), np.float64) if with_mag else None
+        dh_kink = np.empty((n, H, D), np.float64) if with_kink else None
+        da_kink = np.empty((2, H, D), np.float64) if with_kink else None
         rc = self.lib.oracle_gat_backward(n, _p(row_ptr), _p(col), H, D, dt, _p(h), _p(a_src),
                                          _p(a_dst), float(slope), _p(dout), _p(dh), _p(da_src),
-                                         _p(da_dst), _p(dh_mag), _p(da_mag))
+                                         _p(da_dst), _p(dh_mag), _p(da_mag), _p(dh_kink),
+                                         _p(da_kink))
         _check(rc, "backward")
         return dict(dh=dh, da_src=da_src, da_dst=da_dst, dh_mag=dh_mag,
                     da_src_mag=None if da_mag is None else da_mag[0],
-                    da_dst_mag=None if da_mag is None else da_mag[1])
+                    da_dst_mag=None if da_mag is None else da_mag[1], dh_kink=dh_kink,
+                    da_src_kink=None if da_kink is None else da_kink[0],
+                    da_dst_kink=None if da_kink is None else da_kink[1])
 
-    def att_grads(self, row_ptr, col, h, a_src, a_dst, slope, dout, with_mag=False):
+    def att_grads(self, row_ptr, col, h, a_src, a_dst, slope, dout, with_mag=False,
+                  with_kink=False):
         """da_src, da_dst summed per destination row (parallel over rows)."""
         row_ptr, col, h, a_src, a_dst, n, H, D, dt = _prep(row_ptr, col, h, a_src, a_dst)
         dout = np.ascontiguousarray(dout)
@@ -198,15 +208,19 @@ class Oracle:
         da_src = np.empty((H, D), np.float64)
         da_dst = np.empty((H, D), np.float64)
         mag = np.empty((2, H, D), np.float64) if with_mag else None
+        kink = np.empty((2, H, D), np.float64) if with_kink else None
         rc = self.lib.oracle_gat_att_grads(n, _p(row_ptr), _p(col), H, D, dt, _p(h), _p(a_src),
                                            _p(a_dst), float(slope), _p(dout), _p(da_src),
-                                           _p(da_dst), _p(mag))
+                                           _p(da_dst), _p(mag), _p(kink))
         _check(rc, "att_grads")
         return dict(da_src=da_src, da_dst=da_dst,
                     da_src_mag=None if mag is None else mag[0],
-                    da_dst_mag=None if mag is None else mag[1])
+                    da_dst_mag=None if mag is None else mag[1],
+                    da_src_kink=None if kink is None else kink[0],
+                    da_dst_kink=None if kink is None else kink[1])
 
-    def backward_rows(self, row_ptr, col, h, a_src, a_dst, slope, dout, sel, with_mag=False):
+    def backward_rows(self, row_ptr, col, h, a_src, a_dst, slope, dout, sel, with_mag=False,
+                      with_kink=False):
         """dh rows of the listed (distinct) nodes only, each from its neighbourhood."""
         row_ptr, col, h, a_src, a_dst, n, H, D, dt = _prep(row_ptr, col, h, a_src, a_dst)
         dout = np.ascontiguousarray(dout)
@@ -214,11 +228,12 @@ class Oracle:
         sel = _sel(sel)
         dh = np.empty((len(sel), H, D), np.float64)
         dh_mag = np.empty((len(sel), H, D), np.float64) if with_mag else None
+        dh_kink = np.empty((len(sel), H, D), np.float64) if with_kink else None
         rc = self.lib.oracle_gat_backward_rows(n, _p(row_ptr), _p(col), H, D, dt, _p(h), _p(a_src),
                                               _p(a_dst), float(slope), _p(dout), len(sel), _p(sel),
-                                              _p(dh), _p(dh_mag))
+                                              _p(dh), _p(dh_mag), _p(dh_kink))
         _check(rc, "backward_rows")
-        return dict(dh=dh, dh_mag=dh_mag)
+        return dict(dh=dh, dh_mag=dh_mag, dh_kink=dh_kink)
 
 
     # ---- SpMM family (spmm_oracle.c) ----------------------------------------

@@ -140,6 +140,45 @@ static double row_backward_stats(const gat_inputs* g, const void* dout, int64_t 
   return delta;
 }
 
+/* sum_d |a[k][d] x[v][k][d]|: the size of a score half, for the rounding
+ * bound of its float32 value. */
+static double head_dot_mag(const gat_inputs* g, const double* a, const void* x, int64_t v, int k) {
+  double s = 0.0;
+  for (int d = 0; d < g->D; ++d) s += fabs(a[k * g->D + d] * feat(g, x, v, k, d));
+  return s;
+}
+
+/* Largest |z| at which a float32 evaluation of z = s_dst(i) + s_src(j) (two
+ * sums of D products, then their sum) can still have the wrong sign: the
+ * worst-case rounding bound (D + 2) 2^-24 (|s_dst|_mag + |s_src|_mag), with a
+ * factor of two to spare. */
+static double kink_width(const gat_inputs* g, double mag_dst, double mag_src) {
+  return (double)(g->D + 4) * ldexp(1.0, -23) * (mag_dst + mag_src);
+}
+
+/*
+ * The LeakyReLU derivative of an edge is a decision on the sign of z_ij.
+ * Within the rounding bound of a float32 z both derivatives are results of
+ * the method at that precision, so a check must accept either.  amb[q]
+ * (q = 0 .. deg(i)-1) receives |1 - slope| alpha_q |da_q - Delta| for the
+ * in-edges of (i, k) whose |z| is within that bound and 0 for the others:
+ * how far dz_iq, and with it ds_dst(i) and ds_src(j), can move between the
+ * two derivatives.  Returns the sum over the row.
+ */
+static double row_kink(const gat_inputs* g, int64_t i, int k, const double* z,
+                       const double* alpha, const double* da, double delta, double* amb) {
+  const int64_t b = g->row_ptr[i], deg = (int64_t)g->row_ptr[i + 1] - b;
+  const double md = head_dot_mag(g, g->a_dst, g->h, i, k);
+  double tot = 0.0;
+  for (int64_t q = 0; q < deg; ++q) {
+    const int64_t j = g->col[b + q];
+    const double tau = kink_width(g, md, head_dot_mag(g, g->a_src, g->h, j, k));
+    amb[q] = fabs(z[q]) <= tau ? fabs(1.0 - g->slope) * alpha[q] * fabs(da[q] - delta) : 0.0;
+    tot += amb[q];
+  }
+  return tot;
+}
+
 static int check_inputs(const gat_inputs* g) {
   if (g->n < 0 || g->H < 1 || g->D < 1 || g->dtype < 0 || g->dtype > 2) return 1;
   if (!g->row_ptr || (g->n > 0 && (!g->h || !g->a_src || !g->a_dst))) return 1;
@@ -260,14 +299,18 @@ int oracle_gat_node_stats(int64_t n, const int32_t* row_ptr, const int32_t* col,
 
 /*
  * Backward over the whole graph: dh [n][H][D], da_src and da_dst [H][D].
- * dh_mag [n][H][D] and da_mag [2][H][D] (src, dst) may be NULL.
- * Destination statistics are computed in parallel over nodes; the source-side
- * scatter runs in edge order on one thread, so the result is deterministic.
+ * dh_mag [n][H][D] and da_mag [2][H][D] (src, dst) may be NULL, and so may
+ * dh_kink [n][H][D] and da_kink [2][H][D]: per element, how far the result
+ * can move between the two LeakyReLU derivatives of edges at the kink
+ * (row_kink).  Destination statistics are computed in parallel over nodes;
+ * the source-side scatter runs in edge order on one thread, so the result is
+ * deterministic.
  */
 int oracle_gat_backward(int64_t n, const int32_t* row_ptr, const int32_t* col, int H, int D,
                         int dtype, const void* h, const double* a_src, const double* a_dst,
                         double slope, const void* dout, double* dh, double* da_src,
-                        double* da_dst, double* dh_mag, double* da_mag) {
+                        double* da_dst, double* dh_mag, double* da_mag, double* dh_kink,
+                        double* da_kink) {
   gat_inputs g = {n, row_ptr, col, H, D, dtype, h, a_src, a_dst, slope};
   int rc = check_inputs(&g);
   if (rc) return rc;
@@ -279,8 +322,12 @@ int oracle_gat_backward(int64_t n, const int32_t* row_ptr, const int32_t* col, i
   double* delta = (double*)calloc((size_t)NH + 1, sizeof(double));
   double* mag_dst = (double*)calloc((size_t)NH + 1, sizeof(double));
   double* mag_src = (double*)calloc((size_t)NH + 1, sizeof(double));
-  if (!ds_dst || !ds_src || !delta || !mag_dst || !mag_src) {
+  const int kink = dh_kink || da_kink;
+  double* kink_dst = kink ? (double*)calloc((size_t)NH + 1, sizeof(double)) : NULL;
+  double* kink_src = kink ? (double*)calloc((size_t)NH + 1, sizeof(double)) : NULL;
+  if (!ds_dst || !ds_src || !delta || !mag_dst || !mag_src || (kink && (!kink_dst || !kink_src))) {
     free(ds_dst); free(ds_src); free(delta); free(mag_dst); free(mag_src);
+    free(kink_dst); free(kink_src);
     return 3;
   }
   /* destination side: Delta_i and ds_dst(i) */
@@ -289,6 +336,7 @@ int oracle_gat_backward(int64_t n, const int32_t* row_ptr, const int32_t* col, i
     double* z = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
     double* alpha = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
     double* da = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
+    double* amb = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
 #pragma omp for schedule(dynamic, 16)
     for (int64_t i = 0; i < n; ++i) {
       if (row_ptr[i + 1] == row_ptr[i]) continue;
@@ -296,11 +344,13 @@ int oracle_gat_backward(int64_t n, const int32_t* row_ptr, const int32_t* col, i
         row_softmax(&g, i, k, z, alpha);
         delta[i * H + k] = row_backward_stats(&g, dout, i, k, z, alpha, da, &ds_dst[i * H + k],
                                               &mag_dst[i * H + k]);
+        if (kink) kink_dst[i * H + k] = row_kink(&g, i, k, z, alpha, da, delta[i * H + k], amb);
       }
     }
     free(z);
     free(alpha);
     free(da);
+    free(amb);
   }
   /* source side: scatter alpha_ij dout_i and dz_ij onto j, in edge order */
   memset(dh, 0, sizeof(double) * (size_t)NHD);
@@ -320,6 +370,10 @@ int oracle_gat_backward(int64_t n, const int32_t* row_ptr, const int32_t* col, i
           for (int d = 0; d < D; ++d) da += feat(&g, dout, i, k, d) * feat(&g, h, j, k, d);
           ds_src[j * H + k] += alpha[q] * (da - dl) * leaky_grad(z[q], slope);
           mag_src[j * H + k] += alpha[q] * (fabs(da) + fabs(dl));
+          if (kink &&
+              fabs(z[q]) <= kink_width(&g, head_dot_mag(&g, a_dst, h, i, k),
+                                       head_dot_mag(&g, a_src, h, j, k)))
+            kink_src[j * H + k] += fabs(1.0 - slope) * alpha[q] * fabs(da - dl);
           for (int d = 0; d < D; ++d) {
             const double x = feat(&g, dout, i, k, d);
             dh[(j * H + k) * (int64_t)D + d] += alpha[q] * x;
@@ -337,6 +391,7 @@ int oracle_gat_backward(int64_t n, const int32_t* row_ptr, const int32_t* col, i
       da_src[k * D + d] = 0.0;
       da_dst[k * D + d] = 0.0;
       if (da_mag) da_mag[k * D + d] = da_mag[(H + k) * D + d] = 0.0;
+      if (da_kink) da_kink[k * D + d] = da_kink[(H + k) * D + d] = 0.0;
     }
   for (int64_t j = 0; j < n; ++j)
     for (int k = 0; k < H; ++k)
@@ -351,8 +406,15 @@ int oracle_gat_backward(int64_t n, const int32_t* row_ptr, const int32_t* col, i
           da_mag[k * D + d] += mag_src[j * H + k] * fabs(hv);
           da_mag[(H + k) * D + d] += mag_dst[j * H + k] * fabs(hv);
         }
+        if (dh_kink)
+          dh_kink[x] = kink_src[j * H + k] * fabs(as) + kink_dst[j * H + k] * fabs(ad);
+        if (da_kink) {
+          da_kink[k * D + d] += kink_src[j * H + k] * fabs(hv);
+          da_kink[(H + k) * D + d] += kink_dst[j * H + k] * fabs(hv);
+        }
       }
   free(ds_dst); free(ds_src); free(delta); free(mag_dst); free(mag_src);
+  free(kink_dst); free(kink_src);
   return 0;
 }
 
@@ -369,13 +431,13 @@ int oracle_gat_backward(int64_t n, const int32_t* row_ptr, const int32_t* col, i
  *   2. for each listed j and each such edge: alpha_ij = exp(e_ij - lse_i),
  *      da_ij = dout_i . h_j, dz_ij = alpha_ij (da_ij - Delta_i) g_ij, and
  *      dh_j = sum alpha_ij dout_i + ds_src(j) a_src + ds_dst(j) a_dst.
- * dh [n_sel][H][D]; dh_mag may be NULL.  Used where the whole-graph oracle
- * would take too long.
+ * dh [n_sel][H][D]; dh_mag and dh_kink (as for oracle_gat_backward) may be
+ * NULL.  Used where the whole-graph oracle would take too long.
  */
 int oracle_gat_backward_rows(int64_t n, const int32_t* row_ptr, const int32_t* col, int H, int D,
                              int dtype, const void* h, const double* a_src, const double* a_dst,
                              double slope, const void* dout, int64_t n_sel, const int64_t* sel,
-                             double* dh, double* dh_mag) {
+                             double* dh, double* dh_mag, double* dh_kink) {
   gat_inputs g = {n, row_ptr, col, H, D, dtype, h, a_src, a_dst, slope};
   int rc = check_inputs(&g);
   if (rc) return rc;
@@ -413,8 +475,10 @@ int oracle_gat_backward_rows(int64_t n, const int32_t* row_ptr, const int32_t* c
     if (needed) slot[i] = n_u++;
   }
   int64_t* u_node = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_u + 1));
-  /* per slot and head: s_dst, lse, Delta, ds_dst, |dz| sum */
-  double* st = (double*)malloc(sizeof(double) * (size_t)(5 * n_u * H + 1));
+  /* per slot and head: s_dst, lse, Delta, ds_dst, |dz| sum, |s_dst| size,
+     kink ambiguity of ds_dst */
+  enum { NS = 7 };
+  double* st = (double*)malloc(sizeof(double) * (size_t)(NS * n_u * H + 1));
   for (int64_t i = 0; i < n; ++i)
     if (slot[i] >= 0) u_node[slot[i]] = i;
   const int64_t maxdeg = max_in_degree(&g);
@@ -424,23 +488,27 @@ int oracle_gat_backward_rows(int64_t n, const int32_t* row_ptr, const int32_t* c
     double* z = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
     double* alpha = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
     double* da = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
+    double* amb = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
 #pragma omp for schedule(dynamic, 16)
     for (int64_t u = 0; u < n_u; ++u) {
       const int64_t i = u_node[u];
       for (int k = 0; k < H; ++k) {
-        double* s = st + (u * H + k) * 5;
+        double* s = st + (u * H + k) * NS;
         s[0] = head_dot(&g, a_dst, h, i, k);
         s[1] = -INFINITY;
-        s[2] = s[3] = s[4] = 0.0;
+        s[2] = s[3] = s[4] = s[6] = 0.0;
+        s[5] = head_dot_mag(&g, a_dst, h, i, k);
         if (row_ptr[i + 1] > row_ptr[i]) {
           s[1] = row_softmax(&g, i, k, z, alpha);
           s[2] = row_backward_stats(&g, dout, i, k, z, alpha, da, &s[3], &s[4]);
+          if (dh_kink) s[6] = row_kink(&g, i, k, z, alpha, da, s[2], amb);
         }
       }
     }
     free(z);
     free(alpha);
     free(da);
+    free(amb);
   }
   /* phase 2: each listed source from the statistics of its out-neighbours */
 #pragma omp parallel for schedule(dynamic, 1)
@@ -454,27 +522,31 @@ int oracle_gat_backward_rows(int64_t n, const int32_t* row_ptr, const int32_t* c
         if (rmag) rmag[d] = 0.0;
       }
       const double ss = head_dot(&g, a_src, h, j, k);
-      double ds_src = 0.0, msrc = 0.0;
+      const double ss_mag = head_dot_mag(&g, a_src, h, j, k);
+      double ds_src = 0.0, msrc = 0.0, ksrc = 0.0;
       for (int64_t x = cnt[t]; x < cnt[t + 1]; ++x) {
         const int64_t i = edge_dst[x];
-        const double* s = st + (slot[i] * H + k) * 5;
+        const double* s = st + (slot[i] * H + k) * NS;
         const double zz = s[0] + ss;
         const double alpha = exp(leaky(zz, slope) - s[1]);
         double da = 0.0;
         for (int d = 0; d < D; ++d) da += feat(&g, dout, i, k, d) * feat(&g, h, j, k, d);
         ds_src += alpha * (da - s[2]) * leaky_grad(zz, slope);
         msrc += alpha * (fabs(da) + fabs(s[2]));
+        if (fabs(zz) <= kink_width(&g, s[5], ss_mag))
+          ksrc += fabs(1.0 - slope) * alpha * fabs(da - s[2]);
         for (int d = 0; d < D; ++d) {
           const double xv = feat(&g, dout, i, k, d);
           row[d] += alpha * xv;
           if (rmag) rmag[d] += alpha * fabs(xv);
         }
       }
-      const double* sj = st + (slot[j] * H + k) * 5;
+      const double* sj = st + (slot[j] * H + k) * NS;
       for (int d = 0; d < D; ++d) {
         const double as = a_src[k * D + d], ad = a_dst[k * D + d];
         row[d] += ds_src * as + sj[3] * ad;
         if (rmag) rmag[d] += msrc * fabs(as) + sj[4] * fabs(ad);
+        if (dh_kink) dh_kink[(t * H + k) * (int64_t)D + d] = ksrc * fabs(as) + sj[6] * fabs(ad);
       }
     }
   }
@@ -489,12 +561,13 @@ int oracle_gat_backward_rows(int64_t n, const int32_t* row_ptr, const int32_t* c
  * da_dst = sum_i ds_dst(i) h_i.  (The same sums as oracle_gat_backward's,
  * grouped by destination instead of by source.)  Rows are split statically
  * over threads and the per-thread float64 sums are added in thread order.
- * da_src, da_dst [H][D]; da_mag [2][H][D] may be NULL.
+ * da_src, da_dst [H][D]; da_mag and da_kink [2][H][D] (as for
+ * oracle_gat_backward) may be NULL.
  */
 int oracle_gat_att_grads(int64_t n, const int32_t* row_ptr, const int32_t* col, int H, int D,
                          int dtype, const void* h, const double* a_src, const double* a_dst,
                          double slope, const void* dout, double* da_src, double* da_dst,
-                         double* da_mag) {
+                         double* da_mag, double* da_kink) {
   gat_inputs g = {n, row_ptr, col, H, D, dtype, h, a_src, a_dst, slope};
   int rc = check_inputs(&g);
   if (rc) return rc;
@@ -502,7 +575,8 @@ int oracle_gat_att_grads(int64_t n, const int32_t* row_ptr, const int32_t* col, 
   const int64_t HD = (int64_t)H * D;
   const int64_t maxdeg = max_in_degree(&g);
   int nt = oracle_num_threads();
-  double* part = (double*)calloc((size_t)(nt * 4 * HD), sizeof(double));
+  /* per thread: src, dst, src mag, dst mag, src kink, dst kink */
+  double* part = (double*)calloc((size_t)(nt * 6 * HD), sizeof(double));
   if (!part) return 3;
 #pragma omp parallel num_threads(nt)
   {
@@ -510,10 +584,11 @@ int oracle_gat_att_grads(int64_t n, const int32_t* row_ptr, const int32_t* col, 
 #ifdef _OPENMP
     t = omp_get_thread_num();
 #endif
-    double* ps = part + (int64_t)t * 4 * HD; /* src, dst, src mag, dst mag */
+    double* ps = part + (int64_t)t * 6 * HD;
     double* z = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
     double* alpha = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
     double* da = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
+    double* amb = (double*)malloc(sizeof(double) * (size_t)(maxdeg + 1));
 #pragma omp for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
       const int64_t b = row_ptr[i], deg = (int64_t)row_ptr[i + 1] - b;
@@ -522,6 +597,7 @@ int oracle_gat_att_grads(int64_t n, const int32_t* row_ptr, const int32_t* col, 
         double ds, mag;
         row_softmax(&g, i, k, z, alpha);
         const double dl = row_backward_stats(&g, dout, i, k, z, alpha, da, &ds, &mag);
+        const double kd = da_kink ? row_kink(&g, i, k, z, alpha, da, dl, amb) : 0.0;
         for (int64_t q = 0; q < deg; ++q) {
           const int64_t j = col[b + q];
           const double dz = alpha[q] * (da[q] - dl) * leaky_grad(z[q], slope);
@@ -530,32 +606,41 @@ int oracle_gat_att_grads(int64_t n, const int32_t* row_ptr, const int32_t* col, 
             const double x = feat(&g, h, j, k, d);
             ps[k * D + d] += dz * x;
             ps[2 * HD + k * D + d] += dm * fabs(x);
+            if (da_kink) ps[4 * HD + k * D + d] += amb[q] * fabs(x);
           }
         }
         for (int d = 0; d < D; ++d) {
           const double x = feat(&g, h, i, k, d);
           ps[HD + k * D + d] += ds * x;
           ps[3 * HD + k * D + d] += mag * fabs(x);
+          ps[5 * HD + k * D + d] += kd * fabs(x);
         }
       }
     }
     free(z);
     free(alpha);
     free(da);
+    free(amb);
   }
   for (int64_t x = 0; x < HD; ++x) {
-    double s = 0.0, d = 0.0, ms = 0.0, md = 0.0;
+    double s = 0.0, d = 0.0, ms = 0.0, md = 0.0, ks = 0.0, kd = 0.0;
     for (int t = 0; t < nt; ++t) {
-      s += part[(int64_t)t * 4 * HD + x];
-      d += part[(int64_t)t * 4 * HD + HD + x];
-      ms += part[(int64_t)t * 4 * HD + 2 * HD + x];
-      md += part[(int64_t)t * 4 * HD + 3 * HD + x];
+      s += part[(int64_t)t * 6 * HD + x];
+      d += part[(int64_t)t * 6 * HD + HD + x];
+      ms += part[(int64_t)t * 6 * HD + 2 * HD + x];
+      md += part[(int64_t)t * 6 * HD + 3 * HD + x];
+      ks += part[(int64_t)t * 6 * HD + 4 * HD + x];
+      kd += part[(int64_t)t * 6 * HD + 5 * HD + x];
     }
     da_src[x] = s;
     da_dst[x] = d;
     if (da_mag) {
       da_mag[x] = ms;
       da_mag[HD + x] = md;
+    }
+    if (da_kink) {
+      da_kink[x] = ks;
+      da_kink[HD + x] = kd;
     }
   }
   free(part);

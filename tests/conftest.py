@@ -41,10 +41,13 @@ def pytest_sessionfinish(session, exitstatus):
     import json
     agg = {}
     for r in mod.REPORT:
-        a = agg.setdefault(r["what"], {"n": 0, "mag_only": 0, "worst_strict_ratio": 0.0,
+        a = agg.setdefault(r["what"], {"n": 0, "mag_only": 0, "kink_only": 0,
+                                       "kink_elements": 0, "worst_strict_ratio": 0.0,
                                        "comparisons": 0})
         a["n"] += r["n"]
         a["mag_only"] += r["mag_only"]
+        a["kink_only"] += r["kink_only"]
+        a["kink_elements"] += r["kink_elements"]
         a["worst_strict_ratio"] = max(a["worst_strict_ratio"], r["worst_strict_ratio"])
         a["comparisons"] += 1
     with open(path, "w") as f:

@@ -347,6 +347,48 @@ def pin_bf16_inputs(o):
     assert np.array_equal(bb["dh"], bw["dh"])
 
 
+def pin_kink_ambiguity(o):
+    """The edge 1 -> 0 of the worked example sits exactly on the LeakyReLU kink
+    (z = 0).  By hand: its weight is 1/S0 with S0 = e + 1 + e^0.25, its
+    da = dout_0 . h_1 = 0 and Delta_0 = (e + 0.25 e^0.25)/S0, so the two
+    derivatives (slope 0.2 or 1) move dz of that edge by
+    amb = 0.8 Delta_0 / S0; ds_src(1) and ds_dst(0) by amb, dh_1 by
+    amb |a_src|, dh_0 by amb |a_dst|, da_src by amb |h_1| and da_dst by
+    amb |h_0|; nothing else.  Inputs with no z near 0 give no ambiguity, and
+    the per-node and row-grouped entry points agree with the whole graph."""
+    with open(os.path.join(GOLDEN, "worked_example.json")) as f:
+        fx = json.load(f)
+    H, D = fx["H"], fx["D"]
+    rp = np.array(fx["row_ptr"], np.int32)
+    ci = np.array(fx["col_idx"], np.int32)
+    h = np.array(fx["h"], np.float32).reshape(-1, H, D)
+    dout = np.array(fx["dout"], np.float32).reshape(-1, H, D)
+    a_src = np.array(fx["a_src"], np.float32).reshape(H, D)
+    a_dst = np.array(fx["a_dst"], np.float32).reshape(H, D)
+    s0 = math.e + 1.0 + math.exp(0.25)
+    amb = 0.8 * (math.e + 0.25 * math.exp(0.25)) / s0 / s0
+    want = np.zeros((5, D))
+    want[1] = amb * np.abs(a_src[0].astype(np.float64))
+    want[0] = amb * np.abs(a_dst[0].astype(np.float64))
+    b = o.backward(rp, ci, h, a_src, a_dst, fx["slope"], dout, with_kink=True)
+    close(b["dh_kink"].reshape(-1, D), want, 1e-12, 1e-15, "kink dh")
+    close(b["da_src_kink"].ravel(), amb * np.abs(h[1, 0].astype(np.float64)), 1e-12, 1e-15,
+          "kink da_src")
+    close(b["da_dst_kink"].ravel(), amb * np.abs(h[0, 0].astype(np.float64)), 1e-12, 1e-15,
+          "kink da_dst")
+    rows = o.backward_rows(rp, ci, h, a_src, a_dst, fx["slope"], dout, [0, 1, 3], with_kink=True)
+    close(rows["dh_kink"].reshape(-1, D), want[[0, 1, 3]], 1e-12, 1e-15, "kink rows")
+    ag = o.att_grads(rp, ci, h, a_src, a_dst, fx["slope"], dout, with_kink=True)
+    close(ag["da_src_kink"], b["da_src_kink"], 1e-12, 1e-15, "kink row-grouped da_src")
+    close(ag["da_dst_kink"], b["da_dst_kink"], 1e-12, 1e-15, "kink row-grouped da_dst")
+    # random fp64 inputs: no z within rounding of 0
+    rp2, ci2 = irregular_graph(12, 5)
+    h2, as2, ad2, d2 = random_inputs(len(rp2) - 1, 2, 3, 77)
+    b2 = o.backward(rp2, ci2, h2, as2, ad2, 0.2, d2, with_kink=True)
+    assert not b2["dh_kink"].any() and not b2["da_src_kink"].any()
+
+
 ALL_PINS = [pin_worked_example, pin_dense_forward_backward, pin_dense_float32_config1,
             pin_finite_differences, pin_invariants, pin_single_neighbour, pin_equal_scores,
-            pin_hub_mean, pin_slope_one, pin_permutation, pin_sampled_modes, pin_bf16_inputs]
+            pin_hub_mean, pin_slope_one, pin_permutation, pin_sampled_modes, pin_bf16_inputs,
+            pin_kink_ambiguity]

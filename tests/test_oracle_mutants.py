@@ -29,6 +29,11 @@ MUTANTS = {
     "rows_drop_dst_term": ("row[d] += ds_src * as + sj[3] * ad;", "row[d] += ds_src * as;"),
     "rows_delta_sign": ("ds_src += alpha * (da - s[2]) * leaky_grad(zz, slope);",
                         "ds_src += alpha * (da + s[2]) * leaky_grad(zz, slope);"),
+    # the kink ambiguity
+    "kink_without_weight": ("fabs(1.0 - g->slope) * alpha[q] * fabs(da[q] - delta) : 0.0;",
+                            "fabs(1.0 - g->slope) * fabs(da[q] - delta) : 0.0;"),
+    "kink_src_to_dst_vector": ("dh_kink[x] = kink_src[j * H + k] * fabs(as) + kink_dst[j * H + k] * fabs(ad);",
+                               "dh_kink[x] = kink_src[j * H + k] * fabs(ad) + kink_dst[j * H + k] * fabs(as);"),
 }
 
 
