@@ -1040,6 +1040,29 @@ def run_layer(args, rank, world):
                          "algorithmic_bytes_fwd": b_fwd, "algorithmic_bytes_bwd": b_bwd,
                          "peak_source": peak_kind},
             "clocks": clocks}
+    if args.op == "max":
+        # the atomic-free backward on the same steps: a masked gather over the
+        # cached CSC (indices, the winners and dout rows of every out-edge's
+        # destination, dx written)
+        def bwd_ordered():
+            gnn.reduce_backward(g, arg, dout, dx=dx, ws=ws, ordered=True)
+        bwd_ordered()
+        torch.cuda.synchronize()
+        oev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for a, b in oev:
+            flush()
+            a.record(stream)
+            bwd_ordered()
+            b.record(stream)
+        torch.cuda.synchronize()
+        gnn.check_device_error(g)
+        (t_o,) = max_over_ranks([sum(a.elapsed_time(b) for a, b in oev) / K], world, dev)
+        b_o = 4 * (n + 1) + 4 * e + (4 + s) * e * F + s * n * F
+        line["bwd_ordered"] = {"ms": t_o, "vs_atomic": t_o / t_b, "algorithmic_bytes": b_o,
+                               "frac": b_o / (t_o * 1e-3) / 1e9 / peak,
+                               "what": "reduce_agg_backward_ordered: no atomics, bitwise "
+                                       "reproducible"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

@@ -482,16 +482,20 @@ def reduce_forward(g: Graph, x: torch.Tensor, op: str = "max", out=None, arg=Non
 
 
 def reduce_backward(g: Graph, arg: torch.Tensor, dout: torch.Tensor, dx=None, ws=None,
-                    stream=None):
-    """dx = the gradient of sum(out * dout) w.r.t. x, from the forward's arg."""
+                    stream=None, ordered=False):
+    """dx = the gradient of sum(out * dout) w.r.t. x, from the forward's arg.
+
+    ordered: gather the terms over the cached CSC in a fixed order instead of
+    adding them with atomics (bitwise reproducible, more bytes moved)."""
     F = _row_width(g, dout, "dout")
     _check_tensor(g, arg, "arg", dout.shape, torch.int32)
     dt = _dtype_code(dout.dtype)
     dx = _given(g, dx, "dx", dout.shape, dout.dtype, lambda: torch.empty_like(dout))
     ws = _reduce_ws(g, F, dt, _check_ws(g, ws), dout.device)
-    rc = g._lib.reduce_agg_backward(g.handle, F, dt, _ptr(arg), _ptr(dout), _ptr(dx), _ptr(ws),
-                                    ws.numel(), _stream(stream, dout.device))
-    _native.check(rc, "reduce_agg_backward")
+    fn = g._lib.reduce_agg_backward_ordered if ordered else g._lib.reduce_agg_backward
+    rc = fn(g.handle, F, dt, _ptr(arg), _ptr(dout), _ptr(dx), _ptr(ws), ws.numel(),
+            _stream(stream, dout.device))
+    _native.check(rc, "reduce_agg_backward_ordered" if ordered else "reduce_agg_backward")
     return dx
 
 

@@ -59,6 +59,7 @@ SIGNATURES = [
     ("reduce_agg_workspace_bytes", _SZ, [_P, _I32, _I32]),
     ("reduce_agg_forward", _I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     ("reduce_agg_backward", _I32, [_P, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    ("reduce_agg_backward_ordered", _I32, [_P, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     ("gnn_wait_selftest", _I32, [_P, _I32, _P]),
     ("gnn_check_device_error", _I32, [_P, _P, _P]),
     ("gnn_status_string", ctypes.c_char_p, [_I32]),

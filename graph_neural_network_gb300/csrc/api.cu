@@ -527,6 +527,22 @@ gnn_status reduce_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, const
                                                static_cast<cudaStream_t>(stream)));
 }
 
+gnn_status reduce_agg_backward_ordered(const gnn_graph* g, int F, gnn_dtype dtype,
+                                       const int32_t* arg, const void* dout, void* dx, void* ws,
+                                       size_t ws_bytes, void* stream) {
+  Shape s;
+  gnn_status r = spmm_shape(g, F, dtype, &s);
+  if (r != GNN_OK) return r;
+  if (g->n == 0) return GNN_OK;
+  if (!arg || !dout || !dx || !aligned(arg, 16) || !aligned(dout, 16) || !aligned(dx, 16))
+    return GNN_ERR_INVALID_ARG;
+  if (ws_bytes < gnn::reduce_ws_bytes(g, s)) return GNN_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned(ws, 256)) return GNN_ERR_INVALID_ARG;
+  return from_cuda(gnn::launch_reduce_backward_ordered(g, s, dtype, arg, dout, dx,
+                                                       static_cast<char*>(ws),
+                                                       static_cast<cudaStream_t>(stream)));
+}
+
 gnn_status gnn_wait_selftest(const gnn_graph* g, int polls, void* stream) {
   if (!g || !g->err || polls < 1 || polls > 1000000) return GNN_ERR_INVALID_ARG;
   return from_cuda(gnn::launch_wait_selftest(g, polls, static_cast<cudaStream_t>(stream)));

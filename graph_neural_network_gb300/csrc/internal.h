@@ -96,8 +96,11 @@ cudaError_t launch_node_scores(const Shape& s, gnn_dtype dt, const void* h, cons
 // over the CSC (transpose).  Workspace: counters, then the per-node
 // coefficients at kSpmmCoefOffset, then the hub partial sums.
 constexpr size_t kSpmmCoefOffset = 256;
+// win (optional): the masked mode of the max / min backward, edge terms kept
+// only where the gathered row's winner is the output node (norm "sum").
 cudaError_t launch_spmm(const gnn_graph* g, const Shape& s, gnn_dtype dt, int norm, bool transpose,
-                        const void* x, void* out, char* ws, cudaStream_t st);
+                        const void* x, void* out, char* ws, cudaStream_t st,
+                        const int32_t* win = nullptr);
 size_t spmm_ws_bytes(const gnn_graph* g, const Shape& s);
 
 // Max / min neighbourhood reduction (reduce.cu).  Workspace: counters,
@@ -109,6 +112,11 @@ cudaError_t launch_reduce_forward(const gnn_graph* g, const Shape& s, gnn_dtype 
 cudaError_t launch_reduce_backward(const gnn_graph* g, const Shape& s, gnn_dtype dt,
                                    const int32_t* arg, const void* dout, void* dx, char* ws,
                                    cudaStream_t st);
+// The same gradient without atomics: a gather over the cached CSC in a fixed
+// order (bitwise reproducible).
+cudaError_t launch_reduce_backward_ordered(const gnn_graph* g, const Shape& s, gnn_dtype dt,
+                                           const int32_t* arg, const void* dout, void* dx,
+                                           char* ws, cudaStream_t st);
 
 // GATv2 attention (gatv2.cu), rows of at most 512 bytes.
 size_t gatv2_ws_bytes(const gnn_graph* g, const Shape& s);

@@ -21,7 +21,9 @@
 // accumulator with atomic adds; when several destinations share a winner
 // the order of their additions, and so the last bits of dx, can vary from
 // run to run (out and arg never do).  (Splitting the features into slabs
-// whose accumulator part stays in L2 measured 2.5x slower on GB300.)
+// whose accumulator part stays in L2 measured 2.5x slower on GB300.)  The
+// ordered variant gathers the same terms over the cached CSC instead, in a
+// fixed order and without atomics.
 #include "device.cuh"
 
 namespace gnn {
@@ -363,9 +365,12 @@ unsigned grid_for(int64_t items, int sm_count) {
 
 size_t reduce_ws_bytes(const gnn_graph* g, const Shape& s) {
   const size_t row_f = size_t(s.rv) * 16 / s.esize;
-  // counters, hub keys, float32 accumulator of the backward pass
-  return 256 + align_up(size_t(g->csr.n_hub_chunks) * row_f * 8 + 1, 256) +
-         align_up(size_t(g->n) * row_f * 4 + 1, 256);
+  // counters, hub keys, float32 accumulator of the backward pass; the ordered
+  // backward lays the same bytes out as the SpMM workspace
+  const size_t own = 256 + align_up(size_t(g->csr.n_hub_chunks) * row_f * 8 + 1, 256) +
+                     align_up(size_t(g->n) * row_f * 4 + 1, 256);
+  const size_t ordered = spmm_ws_bytes(g, s);
+  return own > ordered ? own : ordered;
 }
 
 cudaError_t launch_reduce_forward(const gnn_graph* g, const Shape& s, gnn_dtype dt, int op,
@@ -435,6 +440,17 @@ cudaError_t launch_reduce_backward(const gnn_graph* g, const Shape& s, gnn_dtype
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// dx[j][f] = sum over the out-edges j -> i (cached CSC, rows ascending) of
+// dout[i][f] where arg[i][f] == j: the SpMM transpose pass with each term
+// masked by the winner, hubs chunked and merged in chunk order.  No atomics,
+// so dx is the same bit for bit on every run; it reads the winners and dout
+// rows once per edge instead of once per node.
+cudaError_t launch_reduce_backward_ordered(const gnn_graph* g, const Shape& s, gnn_dtype dt,
+                                           const int32_t* arg, const void* dout, void* dx,
+                                           char* ws, cudaStream_t st) {
+  return launch_spmm(g, s, dt, GNN_NORM_SUM, true, dout, dx, ws, st, arg);
 }
 
 }  // namespace gnn

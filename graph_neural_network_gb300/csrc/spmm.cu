@@ -37,6 +37,7 @@ struct SpmmArgs {
   void* out;
   const float* c_out;  // [N] coefficient of the output node, or null (= 1)
   const float* c_in;   // [N] coefficient of the gathered node, or null (= 1)
+  const int32_t* win;  // masked mode: [N][F] winners; edge term kept where win == node
   float* part;         // [hub chunks][row floats]
   int* ctr;            // [0] block items taken, [1] light nodes taken
   int32_t* err;
@@ -53,14 +54,28 @@ __global__ void spmm_coef(const int32_t* ptr, int64_t n, int mode, float* c) {
   }
 }
 
-// acc += c_in(j) x_j over the edges beg + g, beg + g + G, ... < end.
-template <typename T, int NV>
-__device__ __forceinline__ void spmm_edges(const SpmmArgs& A, const Lane<NV>& L,
-                                           const int32_t* cols, int colbase, int beg, int end,
-                                           int (&jn)[kUnroll], float (&acc)[NV][VecOf<T>::n]) {
+// Edges in flight per lane: kUnroll, or two in the masked mode (each edge
+// also gathers the row's winners, four bytes per feature).
+template <bool kMask>
+struct SpmmUnroll {
+  static constexpr int value = kMask ? 2 : kUnroll;
+};
+
+// acc += c_in(j) x_j over the edges beg + g, beg + g + G, ... < end.  Masked
+// mode (the max / min backward over the CSC, `self` the output node whose
+// list starts at edge `colstart`): acc[f] += x_j[f] where win[j][f] == self,
+// once per destination j -- a repeated edge (the same j right before it in
+// the ascending list) adds nothing, since a winner is counted per
+// destination, not per edge.
+template <typename T, int NV, bool kMask>
+__device__ __forceinline__ void spmm_edges(const SpmmArgs& A, const Lane<NV>& L, int self,
+                                           int colstart, const int32_t* cols, int colbase,
+                                           int beg, int end, int (&jn)[SpmmUnroll<kMask>::value],
+                                           float (&acc)[NV][VecOf<T>::n]) {
   constexpr int V = VecOf<T>::n;
-  constexpr int U = kUnroll;
+  constexpr int U = SpmmUnroll<kMask>::value;
   const int step = L.G * U;
+  const int row_f = A.s.rv * V;
   for (int base = beg; base < end; base += step) {
     int j[U];
 #pragma unroll
@@ -75,6 +90,27 @@ __device__ __forceinline__ void spmm_edges(const SpmmArgs& A, const Lane<NV>& L,
                                            : make_uint4(0, 0, 0, 0);
       w[u] = j[u] < 0 ? 0.f : (A.c_in ? __ldg(A.c_in + j[u]) : 1.f);
     }
+    int wn[kMask ? U : 1][kMask ? NV : 1][kMask ? V : 1];
+    if (kMask) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = base + u * L.G + L.g;
+        const bool repeat = j[u] >= 0 && e > colstart && __ldg(A.idx + e - 1) == j[u];
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+          for (int c4 = 0; c4 < V; c4 += 4) {
+            const int4 a = (j[u] >= 0 && !repeat && L.ok[v])
+                               ? __ldg(reinterpret_cast<const int4*>(
+                                     A.win + int64_t(j[u]) * row_f + L.q[v] * V + c4))
+                               : make_int4(-1, -1, -1, -1);
+            wn[u][v][c4] = a.x;
+            wn[u][v][c4 + 1] = a.y;
+            wn[u][v][c4 + 2] = a.z;
+            wn[u][v][c4 + 3] = a.w;
+          }
+      }
+    }
     if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -82,7 +118,12 @@ __device__ __forceinline__ void spmm_edges(const SpmmArgs& A, const Lane<NV>& L,
       for (int v = 0; v < NV; ++v) {
         float xv[V];
         unpack<T>(raw[u][v], xv);
-        axpy<V>(acc[v], w[u], xv);
+        if (kMask) {
+#pragma unroll
+          for (int c = 0; c < V; ++c) acc[v][c] += wn[u][v][c] == self ? xv[c] : 0.f;
+        } else {
+          axpy<V>(acc[v], w[u], xv);
+        }
       }
   }
 }
@@ -123,9 +164,10 @@ __device__ __forceinline__ void write_row(const SpmmArgs& A, const Lane<NV>& L, 
   }
 }
 
-template <typename T, int NV>
+template <typename T, int NV, bool kMask>
 __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(const SpmmArgs A) {
   constexpr int V = VecOf<T>::n;
+  constexpr int U = SpmmUnroll<kMask>::value;
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
   const int row_f = A.s.rv * V;
@@ -150,10 +192,11 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(
       const int per = (it.z - it.y + kWarps - 1) / kWarps;
       const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
       const int colbase = it.y & ~3;
-      int jn[kUnroll];
-      batch_ids<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
+      int jn[U];
+      batch_ids<U>(cols, colbase, wb, we, L.g, L.G, jn);
       zero<T, NV>(acc);
-      spmm_edges<T, NV>(A, L, cols, colbase, wb, we, jn, acc);
+      spmm_edges<T, NV, kMask>(A, L, it.x, kMask ? A.ptr[it.x] : 0, cols, colbase, wb, we, jn,
+                               acc);
       subgroup_sums<T, NV>(A.s, acc);
       if (L.g == 0)
 #pragma unroll
@@ -205,24 +248,24 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(
     }
     int i = __shfl_sync(kFull, my_i, 0);
     int beg = __shfl_sync(kFull, my_b, 0), end = __shfl_sync(kFull, my_e, 0);
-    int jn[kUnroll];
-    batch_ids<kUnroll>(A.idx, 0, beg, end, L.g, L.G, jn);
+    int jn[U];
+    batch_ids<U>(A.idx, 0, beg, end, L.g, L.G, jn);
     for (int q = 0; q < kGrab && i >= 0; ++q) {
       const int nq = (q + 1) & (kGrab - 1);
       const int i2 = q + 1 < kGrab ? __shfl_sync(kFull, my_i, nq) : -1;
       const int b2 = __shfl_sync(kFull, my_b, nq);
       const int e2 = __shfl_sync(kFull, my_e, nq);
-      int jn2[kUnroll];
-      batch_ids<kUnroll>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
+      int jn2[U];
+      batch_ids<U>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
       zero<T, NV>(acc);
-      spmm_edges<T, NV>(A, L, A.idx, 0, beg, end, jn, acc);
+      spmm_edges<T, NV, kMask>(A, L, i, beg, A.idx, 0, beg, end, jn, acc);
       subgroup_sums<T, NV>(A.s, acc);
       if (L.g == 0) write_row<T, NV>(A, L, i, acc);
       i = i2;
       beg = b2;
       end = e2;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) jn[u] = jn2[u];
+      for (int u = 0; u < U; ++u) jn[u] = jn2[u];
     }
   }
 }
@@ -264,14 +307,15 @@ cudaError_t launch_t(const SpmmArgs& A, int sm_count, cudaStream_t st) {
   cudaError_t e;
   if (A.n_items + A.n_light > 0) {
     const size_t smem = size_t(A.col_off) + size_t(kWarps) * A.s.rv * V * 4;
+    auto kernel = A.win ? spmm_main<T, NV, true> : spmm_main<T, NV, false>;
     if (smem > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(spmm_main<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(smem))) != cudaSuccess)
       return e;
     const int64_t work = A.n_items + (A.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
-    const int64_t cap = persistent_blocks(spmm_main<T, NV>, smem, sm_count);
+    const int64_t cap = persistent_blocks(kernel, smem, sm_count);
     const int64_t blocks = work < cap ? work : cap;
-    spmm_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
+    kernel<<<unsigned(blocks), kThreads, smem, st>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (A.n_hubs > 0) {
@@ -284,7 +328,8 @@ cudaError_t launch_t(const SpmmArgs& A, int sm_count, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_spmm(const gnn_graph* g, const Shape& s, gnn_dtype dt, int norm, bool transpose,
-                        const void* x, void* out, char* ws, cudaStream_t st) {
+                        const void* x, void* out, char* ws, cudaStream_t st,
+                        const int32_t* win) {
   const Dir& d = transpose ? g->csc : g->csr;
   SpmmArgs A{};
   A.s = s;
@@ -298,6 +343,7 @@ cudaError_t launch_spmm(const gnn_graph* g, const Shape& s, gnn_dtype dt, int no
   A.n_hubs = d.n_hubs;
   A.x = x;
   A.out = out;
+  A.win = win;
   A.ctr = reinterpret_cast<int*>(ws);
   float* coef = reinterpret_cast<float*>(ws + kSpmmCoefOffset);
   A.part = reinterpret_cast<float*>(ws + kSpmmCoefOffset + align_up(size_t(g->n) * 4, 256));

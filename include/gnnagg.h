@@ -355,7 +355,8 @@ gnn_status transformer_agg_backward(const gnn_graph* g, int H, int D, gnn_dtype 
  * 2048 bytes).  x, out, dout, dx: [N][F] dtype; arg: [N][F] int32; all
  * device, 16-byte aligned; ws 256-byte aligned, >= reduce_agg_workspace_bytes
  * (counters, N_hub_chunks * F packed keys, and N * F floats for the
- * backward's accumulator).  Asynchronous on `stream`. */
+ * backward's accumulator; at least the SpMM workspace size, which the
+ * ordered backward uses).  Asynchronous on `stream`. */
 typedef enum { GNN_REDUCE_MAX = 0, GNN_REDUCE_MIN = 1 } gnn_reduce_op;
 
 size_t reduce_agg_workspace_bytes(const gnn_graph* g, int F, gnn_dtype dtype);
@@ -368,6 +369,17 @@ gnn_status reduce_agg_forward(const gnn_graph* g, int F, gnn_dtype dtype, gnn_re
 gnn_status reduce_agg_backward(const gnn_graph* g, int F, gnn_dtype dtype, const int32_t* arg,
                                const void* dout, void* dx, void* ws, size_t ws_bytes,
                                void* stream);
+
+/* The same dx without atomics, bitwise reproducible: for each source j, the
+ * cached CSC transpose (rows ascending) is walked and dout[i][f] is added
+ * where arg[i][f] = j, with the degree-aware tiling of the SpMM backward
+ * (hub chunks summed in chunk order).  It reads the winners and dout rows
+ * once per edge rather than once per node, so it moves more bytes than
+ * reduce_agg_backward.  Arguments, workspace and errors as
+ * reduce_agg_backward. */
+gnn_status reduce_agg_backward_ordered(const gnn_graph* g, int F, gnn_dtype dtype,
+                                       const int32_t* arg, const void* dout, void* dx, void* ws,
+                                       size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, reads and clears the graph's device status word.
  * Returns GNN_OK, GNN_ERR_TIMEOUT (a bounded wait on an asynchronous copy ran

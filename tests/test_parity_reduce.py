@@ -86,3 +86,45 @@ def test_reduce_reproducible_and_autograd():
     assert np.array_equal(to_f64(y.detach()), f["out"])
     # the gradient's float32 additions may run in another order: compare values
     assert_close(to_f64(xt.grad), b["dx"], "f32", b["dx_mag"], "autograd dx")
+
+
+@pytest.mark.parametrize("tiling", TILINGS, ids=lambda t: "t%d_%d_%d" % t)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_reduce_ordered_backward(dtype, tiling):
+    """The atomic-free backward (a masked gather over the cached CSC, hubs in
+    chunk order) against the oracle, on graphs whose CSC has light, mid and
+    chunked hub sources, with ties; bitwise the same over three runs."""
+    import graph_neural_network_gb300 as gnn
+    rp, ci = testgraphs.with_in_degrees(THRESHOLD_DEGREES, n_nodes=2500, seed=67)
+    n = len(rp) - 1
+    F = 32 if dtype == "f32" else 64
+    for ties in (False, True):
+        x = features(n, F, dtype, 71, ties)
+        dy = features(n, F, dtype, 72)
+        g = device_graph(dict(row_ptr=rp, col=ci), tiling)
+        _, arg = gnn.reduce_forward(g, to_device(x, dtype), "max")
+        dyt = to_device(dy, dtype)
+        runs = [gnn.reduce_backward(g, arg, dyt, ordered=True) for _ in range(3)]
+        torch.cuda.synchronize()
+        gnn.check_device_error(g)
+        f = oracle.reduce_forward(rp, ci, x, "max")
+        b = oracle.reduce_backward(f["arg"], dy, with_mag=True)
+        assert np.array_equal(arg.cpu().numpy(), f["arg"])
+        assert_close(to_f64(runs[0]), b["dx"], dtype, b["dx_mag"], f"ordered dx {tiling} {ties}")
+        for r in runs[1:]:
+            assert torch.equal(r, runs[0])
+    assert g.stats()["csc"]["hubs"] > 0 or tiling == (64, 4096, 2048)
+
+
+def test_reduce_ordered_backward_power_law():
+    import graph_neural_network_gb300 as gnn
+    rp, ci = workload.chung_lu(50_000, 2.1, 20.0, 10_000.0, 73)
+    n = len(rp) - 1
+    x, dy = features(n, 128, "bf16", 74), features(n, 128, "bf16", 75)
+    g = device_graph(dict(row_ptr=rp, col=ci))
+    _, arg = gnn.reduce_forward(g, to_device(x, "bf16"), "min")
+    dx = gnn.reduce_backward(g, arg, to_device(dy, "bf16"), ordered=True)
+    torch.cuda.synchronize()
+    f = oracle.reduce_forward(rp, ci, x, "min")
+    b = oracle.reduce_backward(f["arg"], dy, with_mag=True)
+    assert_close(to_f64(dx), b["dx"], "bf16", b["dx_mag"], "ordered dx chung-lu")
