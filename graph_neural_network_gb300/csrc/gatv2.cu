@@ -163,13 +163,12 @@ struct V2Online {
 
 template <typename T, bool kFixed>
 __device__ __forceinline__ void fwd_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int sg, int SG,
+                                          int colbase, int beg, int end, int sg, int SG, int step,
                                           int trips, int (&jn)[kUnroll],
                                           const float (&xr)[VecOf<T>::n],
                                           const float (&a2)[VecOf<T>::n], V2Online<T>& st) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
-  const int step = SG * U;
   int base = beg;
   for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
@@ -258,15 +257,16 @@ __global__ void __launch_bounds__(kThreads, 3) v2_fwd_main(const V2Args A) {
       if (it_i >= D.n_items) break;
       const int4 it = D.items[it_i];
       if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
-      const int per = (it.z - it.y + kWarps - 1) / kWarps;
-      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      // batches of kUnroll * G edges dealt to the warps in turn
+      const int wb = it.y + wid * kUnroll * L.G;
       const int colbase = it.y & ~3;
       int jn[kUnroll];
-      batch_ids<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
+      batch_ids<kUnroll>(cols, colbase, wb, it.z, L.g, L.G, jn);
       own_row<T>(A.xr, it.x, A.s, L, xr);
       V2Online<T> st;
       st.init();
-      fwd_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, 0, jn, xr, a2, st);
+      fwd_edges<T, false>(A, L, cols, colbase, wb, it.z, L.g, L.G, kWarps * kUnroll * L.G, 0, jn,
+                          xr, a2, st);
       st.merge_subgroups(A.s);
       if (L.g == 0 && L.ok[0]) {
 #pragma unroll
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_fwd_main(const V2Args A) {
         own_row<T>(A.xr, i >= 0 ? i : 0, A.s, L, xr);
         V2Online<T> st;
         st.init();
-        fwd_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, trips, jn, xr, a2, st);
+        fwd_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, kUnroll, trips, jn, xr, a2, st);
         if (i >= 0) fwd_write<T>(A, L, i, st);
       }
     }
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_fwd_main(const V2Args A) {
       own_row<T>(A.xr, i, A.s, L, xr);
       V2Online<T> st;
       st.init();
-      fwd_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, 0, jn, xr, a2, st);
+      fwd_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, kUnroll * L.G, 0, jn, xr, a2, st);
       st.merge_subgroups(A.s);
       if (L.g == 0) fwd_write<T>(A, L, i, st);
       i = i2;
@@ -431,14 +431,13 @@ struct DstSums {
 // (which needs l = g z) and the sums (which need g alone).
 template <typename T>
 __device__ __forceinline__ void dst_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int (&jn)[kUB],
+                                          int colbase, int beg, int end, int step, int (&jn)[kUB],
                                           const float (&xr)[VecOf<T>::n],
                                           const float (&gi)[VecOf<T>::n],
                                           const float (&a2)[VecOf<T>::n], float lse2,
                                           DstSums<T>& sm) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUB;
-  const int step = L.G * U;
   for (int base = beg; base < end; base += step) {
     int j[U];
 #pragma unroll
@@ -539,17 +538,17 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
     for (int64_t it_i = blockIdx.x; it_i < D.n_items; it_i += gridDim.x) {
       const int4 it = D.items[it_i];
       if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
-      const int per = (it.z - it.y + kWarps - 1) / kWarps;
-      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      // batches of kUB * G edges dealt to the warps in turn
+      const int wb = it.y + wid * kUB * L.G;
       const int colbase = it.y & ~3;
       int jn[kUB];
-      batch_ids<kUB>(cols, colbase, wb, we, L.g, L.G, jn);
+      batch_ids<kUB>(cols, colbase, wb, it.z, L.g, L.G, jn);
       own_row<T>(A.xr, it.x, A.s, L, xr);
       own_row<T>(A.dout, it.x, A.s, L, gi);
       const float lse2 = L.ok[0] ? A.lse_in[int64_t(it.x) * H + L.k[0]] * kLog2e : 0.f;
       DstSums<T> sm;
       sm.init();
-      dst_edges<T>(A, L, cols, colbase, wb, we, jn, xr, gi, a2, lse2, sm);
+      dst_edges<T>(A, L, cols, colbase, wb, it.z, kWarps * kUB * L.G, jn, xr, gi, a2, lse2, sm);
       sm.subgroup_total(A.s);
       float* mine = wbuf + wid * (H + 2 * row_f);
       if (L.g == 0 && L.ok[0]) {
@@ -615,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
       const float lse2 = L.ok[0] ? A.lse_in[int64_t(i) * H + L.k[0]] * kLog2e : 0.f;
       DstSums<T> sm;
       sm.init();
-      dst_edges<T>(A, L, D.idx, 0, beg, end, jn, xr, gi, a2, lse2, sm);
+      dst_edges<T>(A, L, D.idx, 0, beg, end, kUB * L.G, jn, xr, gi, a2, lse2, sm);
       sm.subgroup_total(A.s);
       if (L.g == 0) dst_finish<T>(A, L, i, sm, lse2, xr, dslot);
       i = i2;
@@ -671,13 +670,12 @@ __global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
 // a batch stay in registers between the score and the sums.
 template <typename T>
 __device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int (&in)[kUB],
+                                          int colbase, int beg, int end, int step, int (&in)[kUB],
                                           const float (&xl)[VecOf<T>::n],
                                           const float (&a2)[VecOf<T>::n],
                                           float (&acc)[VecOf<T>::n], float (&w)[VecOf<T>::n]) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUB;
-  const int step = L.G * U;
   const int H = A.s.H;
   for (int base = beg; base < end; base += step) {
     int i[U];
@@ -772,15 +770,15 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
     for (int64_t it_i = blockIdx.x; it_i < D.n_items; it_i += gridDim.x) {
       const int4 it = D.items[it_i];
       if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
-      const int per = (it.z - it.y + kWarps - 1) / kWarps;
-      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      // batches of kUB * G edges dealt to the warps in turn
+      const int wb = it.y + wid * kUB * L.G;
       const int colbase = it.y & ~3;
       int in[kUB];
-      batch_ids<kUB>(cols, colbase, wb, we, L.g, L.G, in);
+      batch_ids<kUB>(cols, colbase, wb, it.z, L.g, L.G, in);
       own_row<T>(A.xl, it.x, A.s, L, xl);
       zero<V>(acc);
       zero<V>(w);
-      src_edges<T>(A, L, cols, colbase, wb, we, in, xl, a2, acc, w);
+      src_edges<T>(A, L, cols, colbase, wb, it.z, kWarps * kUB * L.G, in, xl, a2, acc, w);
       src_combine<T>(A, L, xl, acc, w, dslot);
       if (L.g == 0 && L.ok[0])
 #pragma unroll
@@ -831,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
       own_row<T>(A.xl, j, A.s, L, xl);
       zero<V>(acc);
       zero<V>(w);
-      src_edges<T>(A, L, D.idx, 0, beg, end, in, xl, a2, acc, w);
+      src_edges<T>(A, L, D.idx, 0, beg, end, kUB * L.G, in, xl, a2, acc, w);
       src_combine<T>(A, L, xl, acc, w, dslot);
       if (L.g == 0) src_write<T>(A, L, j, acc);
       j = j2;
