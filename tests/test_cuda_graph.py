@@ -1,6 +1,6 @@
 """Every compute call is capture-safe: a CUDA graph of one forward + backward
 step of each aggregation family replays to the bits of the eager calls (the
-max/min backward's float atomics aside)."""
+max/min backward's float atomics aside; its ordered variant is bitwise)."""
 import pytest
 import torch
 
@@ -24,6 +24,7 @@ def step(gnn, g, n, H, D, A, B, C, G, T, Ta, Tb):
     r["gcn_dx"] = gnn.gcn_backward(g, Y, "sym")
     r["max_out"], r["max_arg"] = gnn.reduce_forward(g, X, "max")
     r["max_dx"] = gnn.reduce_backward(g, r["max_arg"], Y)
+    r["max_dx_ordered"] = gnn.reduce_backward(g, r["max_arg"], Y, ordered=True)
     return r
 
 
