@@ -428,17 +428,22 @@ struct DstSums {
 };
 
 // The LeakyReLU slopes g of a batch stay in registers between the score
-// (which needs l = g z) and the sums (which need g alone).
-template <typename T>
+// (which needs l = g z) and the sums (which need g alone).  The batch at
+// `base` holds edges base + sg + u * SG; until end (kFixed false), or for
+// exactly `trips` batches (kFixed true, the same count on every lane of the
+// warp; batches past end add nothing).
+template <typename T, bool kFixed>
 __device__ __forceinline__ void dst_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int step, int (&jn)[kUB],
+                                          int colbase, int beg, int end, int sg, int SG,
+                                          int step, int trips, int (&jn)[kUB],
                                           const float (&xr)[VecOf<T>::n],
                                           const float (&gi)[VecOf<T>::n],
                                           const float (&a2)[VecOf<T>::n], float lse2,
                                           DstSums<T>& sm) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUB;
-  for (int base = beg; base < end; base += step) {
+  int base = beg;
+  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
@@ -447,7 +452,8 @@ __device__ __forceinline__ void dst_edges(const V2Args& A, const Lane<1>& L, con
     for (int u = 0; u < U; ++u)
       raw[u] = (j[u] >= 0 && L.ok[0]) ? ld16(row_base<T>(A.xl, j[u], A.s.rv) + 16 * L.q[0])
                                       : make_uint4(0, 0, 0, 0);
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+    if (kFixed ? t + 1 < trips : base + step < end)
+      batch_ids<U>(cols, colbase, base + step, end, sg, SG, jn);
     float red[2 * U];  // scores (base 2), then dout_i . xl_j
     float g[U][V];
 #pragma unroll
@@ -492,27 +498,30 @@ __device__ __forceinline__ void dst_finish(const V2Args& A, const Lane<1>& L, in
   if (L.head_leader(A.s, 0)) A.stats[i * A.s.H + L.k[0]] = make_float2(lse2, sm.delta);
 }
 
-// Zero this warp's datt sums (its g == 0 lanes own them).
-template <int V>
+// Zero this lane's elements of its datt slot (with kSub every sub-group has
+// a slot of its own; otherwise the g == 0 lanes own the warp's one).
+template <int V, bool kSub>
 __device__ __forceinline__ void zero_da(const Lane<1>& L, float* dslot) {
-  if (L.g == 0 && L.ok[0])
+  if ((kSub || L.g == 0) && L.ok[0])
 #pragma unroll
     for (int c = 0; c < V; ++c) dslot[L.q[0] * V + c] = 0.f;
 }
 
-// Fold the per-warp datt sums buf[kWarps][row_f] of this block (warp order)
-// into da_part[row].
-__device__ __forceinline__ void fold_da(const V2Args& A, int row_f, const float* buf,
+// Fold the datt slots buf[slots][row_f] of this block (slot order: warp, then
+// sub-group) into da_part[row].
+__device__ __forceinline__ void fold_da(const V2Args& A, int row_f, const float* buf, int slots,
                                         int64_t row) {
   __syncthreads();
   for (int t = threadIdx.x; t < row_f; t += blockDim.x) {
     double s = 0.0;
-    for (int w = 0; w < kWarps; ++w) s += double(buf[w * row_f + t]);
+    for (int w = 0; w < slots; ++w) s += double(buf[w * row_f + t]);
     A.da_part[row * row_f + t] = s;
   }
 }
 
-template <typename T>
+// kSub: light nodes take one sub-group each (rows narrower than a warp), each
+// sub-group with its own datt slot; otherwise one warp each.
+template <typename T, bool kSub>
 __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
   constexpr int V = VecOf<T>::n;
   const V2Dir& D = A.csr;
@@ -520,13 +529,14 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
   const int wid = threadIdx.x >> 5;
   const int row_f = A.s.rv * V;
   const int H = A.s.H;
+  const int nsub = kSub ? L.G : 1;
   extern __shared__ __align__(16) unsigned char smem[];
   float a2[V], xr[V], gi[V];
   att_slice<T>(A.att, L, kLog2e, a2);
   float* wbuf = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][H + 2 row_f]
-  float* dsum = wbuf + kWarps * (H + 2 * row_f);              // [kWarps][row_f] datt sums
-  float* dslot = dsum + wid * row_f;
-  zero_da<V>(L, dslot);
+  float* dsum = wbuf + kWarps * (H + 2 * row_f);              // [kWarps * nsub][row_f]
+  float* dslot = dsum + (wid * nsub + (kSub ? L.g : 0)) * row_f;
+  zero_da<V, kSub>(L, dslot);
 
   // ---- block items, assigned statically: item b, b + B, ... -------------
   if (D.n_items > 0) {
@@ -548,7 +558,8 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
       const float lse2 = L.ok[0] ? A.lse_in[int64_t(it.x) * H + L.k[0]] * kLog2e : 0.f;
       DstSums<T> sm;
       sm.init();
-      dst_edges<T>(A, L, cols, colbase, wb, it.z, kWarps * kUB * L.G, jn, xr, gi, a2, lse2, sm);
+      dst_edges<T, false>(A, L, cols, colbase, wb, it.z, L.g, L.G, kWarps * kUB * L.G, 0, jn, xr,
+                          gi, a2, lse2, sm);
       sm.subgroup_total(A.s);
       float* mine = wbuf + wid * (H + 2 * row_f);
       if (L.g == 0 && L.ok[0]) {
@@ -588,9 +599,48 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
     }
   }
 
-  // ---- light nodes, assigned statically: groups of kGrab per warp ---------
   const int64_t gw = int64_t(blockIdx.x) * kWarps + wid;
   const int64_t W = int64_t(gridDim.x) * kWarps;
+  // ---- light nodes, rows narrower than a warp: one sub-group each, groups
+  // of R * G nodes per warp assigned statically ------------------------------
+  if (kSub) {
+    const int R = L.G >= 32 ? 1 : 2;  // nodes per sub-group per group
+    const int npull = R * L.G;
+    for (int64_t t0 = gw * npull; t0 < D.n_light; t0 += W * npull) {
+      int my_i = -1, my_b = 0, my_e = 0;
+      if (L.lane < npull && t0 + L.lane < D.n_light) {
+        my_i = D.light[t0 + L.lane];
+        my_b = D.ptr[my_i];
+        my_e = D.ptr[my_i + 1];
+      }
+      for (int r = 0; r < R; ++r) {
+        const int from = r * L.G + L.g;
+        const int i = __shfl_sync(kFull, my_i, from);
+        const int beg = __shfl_sync(kFull, my_b, from);
+        const int e0 = __shfl_sync(kFull, my_e, from);  // every lane shuffles
+        const int end = i >= 0 ? e0 : beg;
+        if (!__any_sync(kFull, i >= 0)) break;
+        int trips = (end - beg + kUB - 1) / kUB;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
+        int jn[kUB];
+        batch_ids<kUB>(D.idx, 0, beg, end, 0, 1, jn);
+        const int ii = i >= 0 ? i : 0;
+        own_row<T>(A.xr, ii, A.s, L, xr);
+        own_row<T>(A.dout, ii, A.s, L, gi);
+        const float lse2 = L.ok[0] ? A.lse_in[int64_t(ii) * H + L.k[0]] * kLog2e : 0.f;
+        DstSums<T> sm;
+        sm.init();
+        dst_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, kUB, trips, jn, xr, gi, a2, lse2, sm);
+        if (i >= 0) dst_finish<T>(A, L, i, sm, lse2, xr, dslot);
+      }
+    }
+    fold_da(A, row_f, dsum, kWarps * nsub, blockIdx.x);
+    return;
+  }
+
+  // ---- light nodes, rows of a whole warp: groups of kGrab per warp,
+  // assigned statically -------------------------------------------------------
   for (int64_t t0 = gw * kGrab; t0 < D.n_light; t0 += W * kGrab) {
     int my_i = -1, my_b = 0, my_e = 0;
     if (L.lane < kGrab && t0 + L.lane < D.n_light) {
@@ -614,7 +664,8 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
       const float lse2 = L.ok[0] ? A.lse_in[int64_t(i) * H + L.k[0]] * kLog2e : 0.f;
       DstSums<T> sm;
       sm.init();
-      dst_edges<T>(A, L, D.idx, 0, beg, end, kUB * L.G, jn, xr, gi, a2, lse2, sm);
+      dst_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, kUB * L.G, 0, jn, xr, gi, a2, lse2,
+                          sm);
       sm.subgroup_total(A.s);
       if (L.g == 0) dst_finish<T>(A, L, i, sm, lse2, xr, dslot);
       i = i2;
@@ -624,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_dst_main(const V2Args A) {
       for (int u = 0; u < kUB; ++u) jn[u] = jn2[u];
     }
   }
-  fold_da(A, row_f, dsum, blockIdx.x);
+  fold_da(A, row_f, dsum, kWarps * nsub, blockIdx.x);
 }
 
 // One warp per CSR hub (static): add its chunk sums in chunk order, finish the
@@ -639,7 +690,7 @@ __global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
   const int H = A.s.H;
   __shared__ float buf[kWarps * 256];  // rows of at most 512 bytes: <= 256 floats
   float* dslot = buf + wid * row_f;
-  zero_da<V>(L, dslot);
+  zero_da<V, false>(L, dslot);
   if (t < A.csr.n_hubs && L.g == 0 && L.ok[0]) {
     const int4 hb = A.csr.hubs[t];
     DstSums<T> tot;
@@ -659,7 +710,7 @@ __global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
     const float lse2 = A.lse_in[int64_t(hb.x) * H + L.k[0]] * kLog2e;
     dst_finish<T>(A, L, hb.x, tot, lse2, xr, dslot);
   }
-  fold_da(A, row_f, buf, A.da_main_rows + blockIdx.x);
+  fold_da(A, row_f, buf, kWarps, A.da_main_rows + blockIdx.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -668,16 +719,18 @@ __global__ void __launch_bounds__(kThreads) v2_dst_merge(const V2Args A) {
 
 // acc += alpha_ij dout_i and w += de_ij g_ij over the batch; the slopes g of
 // a batch stay in registers between the score and the sums.
-template <typename T>
+template <typename T, bool kFixed>
 __device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, const int32_t* cols,
-                                          int colbase, int beg, int end, int step, int (&in)[kUB],
+                                          int colbase, int beg, int end, int sg, int SG,
+                                          int step, int trips, int (&in)[kUB],
                                           const float (&xl)[VecOf<T>::n],
                                           const float (&a2)[VecOf<T>::n],
                                           float (&acc)[VecOf<T>::n], float (&w)[VecOf<T>::n]) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUB;
   const int H = A.s.H;
-  for (int base = beg; base < end; base += step) {
+  int base = beg;
+  for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int i[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) i[u] = in[u];
@@ -690,7 +743,8 @@ __device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, con
       rg[u] = ok ? ld16(row_base<T>(A.dout, i[u], A.s.rv) + 16 * L.q[0]) : make_uint4(0, 0, 0, 0);
       st[u] = ok ? __ldg(A.stats + int64_t(i[u]) * H + L.k[0]) : make_float2(0.f, 0.f);
     }
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, in);
+    if (kFixed ? t + 1 < trips : base + step < end)
+      batch_ids<U>(cols, colbase, base + step, end, sg, SG, in);
     float red[2 * U];
     float g[U][V];
 #pragma unroll
@@ -715,17 +769,22 @@ __device__ __forceinline__ void src_edges(const V2Args& A, const Lane<1>& L, con
   }
 }
 
-// Warp totals of node j's (partial) sums: add the datt term xl_j w into this
-// warp's datt sums and turn acc into acc + att w (the lanes with g == 0).
-template <typename T>
+// Totals of node j's (partial) sums: add the datt term xl_j w into the datt
+// slot and turn acc into acc + att w.  Split (a node's edges spread over the
+// warp's sub-groups): the sub-group sums are added first and the lanes with
+// g == 0 finish; otherwise each sub-group holds a node of its own.
+template <typename T, bool kSplit>
 __device__ __forceinline__ void src_combine(const V2Args& A, const Lane<1>& L,
                                             const float (&xl)[VecOf<T>::n],
                                             float (&acc)[VecOf<T>::n],
                                             float (&w)[VecOf<T>::n], float* dslot) {
   constexpr int V = VecOf<T>::n;
-  subgroup_sums<V>(acc, A.s);
-  subgroup_sums<V>(w, A.s);
-  if (L.g != 0 || !L.ok[0]) return;
+  if (kSplit) {
+    subgroup_sums<V>(acc, A.s);
+    subgroup_sums<V>(w, A.s);
+    if (L.g != 0) return;
+  }
+  if (!L.ok[0]) return;
   float a[V];
   att_slice<T>(A.att, L, 1.f, a);
   float* d = dslot + L.q[0] * V;
@@ -746,20 +805,21 @@ __device__ __forceinline__ void src_write(const V2Args& A, const Lane<1>& L, int
 // Work is assigned statically (block items b, b + B, ...; light groups by
 // warp), so that the per-block datt sums, folded into da_part[da_src_row0 +
 // block], do not depend on timing.
-template <typename T>
+template <typename T, bool kSub>
 __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
   constexpr int V = VecOf<T>::n;
   const V2Dir& D = A.csc;
   const Lane<1> L(A.s);
   const int wid = threadIdx.x >> 5;
   const int row_f = A.s.rv * V;
+  const int nsub = kSub ? L.G : 1;
   extern __shared__ __align__(16) unsigned char smem[];
   float a2[V], xl[V], acc[V], w[V];
   att_slice<T>(A.att, L, kLog2e, a2);
   float* wacc = reinterpret_cast<float*>(smem + D.col_off);  // [kWarps][row_f]
-  float* dsum = wacc + kWarps * row_f;                        // [kWarps][row_f] datt sums
-  float* dslot = dsum + wid * row_f;
-  zero_da<V>(L, dslot);
+  float* dsum = wacc + kWarps * row_f;                        // [kWarps * nsub][row_f]
+  float* dslot = dsum + (wid * nsub + (kSub ? L.g : 0)) * row_f;
+  zero_da<V, kSub>(L, dslot);
 
   if (D.n_items > 0) {
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
@@ -778,8 +838,9 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
       own_row<T>(A.xl, it.x, A.s, L, xl);
       zero<V>(acc);
       zero<V>(w);
-      src_edges<T>(A, L, cols, colbase, wb, it.z, kWarps * kUB * L.G, in, xl, a2, acc, w);
-      src_combine<T>(A, L, xl, acc, w, dslot);
+      src_edges<T, false>(A, L, cols, colbase, wb, it.z, L.g, L.G, kWarps * kUB * L.G, 0, in, xl,
+                          a2, acc, w);
+      src_combine<T, true>(A, L, xl, acc, w, dslot);
       if (L.g == 0 && L.ok[0])
 #pragma unroll
         for (int c = 0; c < V; ++c) wacc[wid * row_f + L.q[0] * V + c] = acc[c];
@@ -805,9 +866,48 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
     }
   }
 
-  // ---- light nodes, assigned statically: groups of kGrab per warp ---------
   const int64_t gw = int64_t(blockIdx.x) * kWarps + wid;
   const int64_t W = int64_t(gridDim.x) * kWarps;
+  // ---- light nodes, rows narrower than a warp: one sub-group each, groups
+  // of R * G nodes per warp assigned statically ------------------------------
+  if (kSub) {
+    const int R = L.G >= 32 ? 1 : 2;
+    const int npull = R * L.G;
+    for (int64_t t0 = gw * npull; t0 < D.n_light; t0 += W * npull) {
+      int my_j = -1, my_b = 0, my_e = 0;
+      if (L.lane < npull && t0 + L.lane < D.n_light) {
+        my_j = D.light[t0 + L.lane];
+        my_b = D.ptr[my_j];
+        my_e = D.ptr[my_j + 1];
+      }
+      for (int r = 0; r < R; ++r) {
+        const int from = r * L.G + L.g;
+        const int j = __shfl_sync(kFull, my_j, from);
+        const int beg = __shfl_sync(kFull, my_b, from);
+        const int e0 = __shfl_sync(kFull, my_e, from);  // every lane shuffles
+        const int end = j >= 0 ? e0 : beg;
+        if (!__any_sync(kFull, j >= 0)) break;
+        int trips = (end - beg + kUB - 1) / kUB;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) trips = max(trips, __shfl_xor_sync(kFull, trips, o));
+        int in[kUB];
+        batch_ids<kUB>(D.idx, 0, beg, end, 0, 1, in);
+        own_row<T>(A.xl, j >= 0 ? j : 0, A.s, L, xl);
+        zero<V>(acc);
+        zero<V>(w);
+        src_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, kUB, trips, in, xl, a2, acc, w);
+        if (j >= 0) {
+          src_combine<T, false>(A, L, xl, acc, w, dslot);
+          src_write<T>(A, L, j, acc);
+        }
+      }
+    }
+    fold_da(A, row_f, dsum, kWarps * nsub, A.da_src_row0 + blockIdx.x);
+    return;
+  }
+
+  // ---- light nodes, rows of a whole warp: groups of kGrab per warp,
+  // assigned statically -------------------------------------------------------
   for (int64_t t0 = gw * kGrab; t0 < D.n_light; t0 += W * kGrab) {
     int my_j = -1, my_b = 0, my_e = 0;
     if (L.lane < kGrab && t0 + L.lane < D.n_light) {
@@ -829,8 +929,8 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
       own_row<T>(A.xl, j, A.s, L, xl);
       zero<V>(acc);
       zero<V>(w);
-      src_edges<T>(A, L, D.idx, 0, beg, end, kUB * L.G, in, xl, a2, acc, w);
-      src_combine<T>(A, L, xl, acc, w, dslot);
+      src_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, kUB * L.G, 0, in, xl, a2, acc, w);
+      src_combine<T, true>(A, L, xl, acc, w, dslot);
       if (L.g == 0) src_write<T>(A, L, j, acc);
       j = j2;
       beg = b2;
@@ -839,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 3) v2_src_main(const V2Args A) {
       for (int u = 0; u < kUB; ++u) in[u] = in2[u];
     }
   }
-  fold_da(A, row_f, dsum, A.da_src_row0 + blockIdx.x);
+  fold_da(A, row_f, dsum, kWarps * nsub, A.da_src_row0 + blockIdx.x);
 }
 
 template <typename T>
@@ -909,16 +1009,22 @@ cudaError_t bwd_t(V2Args A, int sm_count, cudaStream_t st) {
   constexpr int V = VecOf<T>::n;
   const int row_f = A.s.rv * V;
   const int64_t cap = int64_t(sm_count > 0 ? sm_count : 1) * 8;
+  // rows narrower than a warp: light nodes one sub-group each, with a datt
+  // slot per sub-group
+  const bool sub = A.s.lpr < 32;
+  const int nsub = sub ? 32 / A.s.lpr : 1;
   cudaError_t e;
   // pass 1: a fixed grid (static work assignment), one da_part row per block
   {
     const V2Dir& D = A.csr;
-    const size_t smem = size_t(D.col_off) + size_t(kWarps) * (A.s.H + 3 * row_f) * 4;
-    if ((e = set_smem(v2_dst_main<T>, smem)) != cudaSuccess) return e;
-    int64_t blocks = persistent_blocks(v2_dst_main<T>, smem, sm_count);
+    const size_t smem =
+        size_t(D.col_off) + size_t(kWarps) * (A.s.H + 2 * row_f + nsub * row_f) * 4;
+    auto kernel = sub ? v2_dst_main<T, true> : v2_dst_main<T, false>;
+    if ((e = set_smem(kernel, smem)) != cudaSuccess) return e;
+    int64_t blocks = persistent_blocks(kernel, smem, sm_count);
     if (blocks > cap) blocks = cap;
     A.da_main_rows = int(blocks);
-    v2_dst_main<T><<<unsigned(blocks), kThreads, smem, st>>>(A);
+    kernel<<<unsigned(blocks), kThreads, smem, st>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t mblocks = (D.n_hubs + kWarps - 1) / kWarps;
     if (mblocks > 0) {
@@ -930,11 +1036,12 @@ cudaError_t bwd_t(V2Args A, int sm_count, cudaStream_t st) {
   // pass 2: likewise a fixed grid, one da_part row per block
   {
     const V2Dir& D = A.csc;
-    const size_t smem = size_t(D.col_off) + size_t(kWarps) * 2 * row_f * 4;
-    if ((e = set_smem(v2_src_main<T>, smem)) != cudaSuccess) return e;
-    int64_t blocks = persistent_blocks(v2_src_main<T>, smem, sm_count);
+    const size_t smem = size_t(D.col_off) + size_t(kWarps) * (1 + nsub) * row_f * 4;
+    auto kernel = sub ? v2_src_main<T, true> : v2_src_main<T, false>;
+    if ((e = set_smem(kernel, smem)) != cudaSuccess) return e;
+    int64_t blocks = persistent_blocks(kernel, smem, sm_count);
     if (blocks > cap) blocks = cap;
-    v2_src_main<T><<<unsigned(blocks), kThreads, smem, st>>>(A);
+    kernel<<<unsigned(blocks), kThreads, smem, st>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (D.n_hubs > 0) {
       v2_src_merge<T><<<unsigned((D.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
