@@ -21,9 +21,10 @@ constexpr int kUnroll = 4;     // edges in flight per lane and batch
 // Resident blocks per SM the main kernels are compiled for (register cap).
 // Rows up to 512 bytes: 4 blocks (32 warps, <= 64 registers) for the
 // kernels that gather one row per edge and keep little state, 3 blocks
-// (24 warps, <= 80 registers) for the source-side backward pass, which
-// gathers a row and a statistics record and keeps a row accumulator (at 64
-// registers it spills).  Measured on GB300 over the power-law workloads.
+// (24 warps, <= 80 registers) for the source-side backward pass with
+// 16-byte vectors, which gathers a row and a statistics record and keeps a
+// row accumulator (at 64 registers it spills and runs slower).  Measured on
+// GB300 over the power-law workloads.
 template <int NV>
 struct MinBlocks {
   static constexpr int value = NV == 1 ? 3 : (NV == 2 ? 2 : 1);
