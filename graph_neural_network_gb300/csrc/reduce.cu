@@ -105,10 +105,9 @@ struct Best {
 template <typename T, int NV>
 __device__ __forceinline__ void red_edges(const RedArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
-                                          int (&jn)[kUnroll], Best<T, NV>& b) {
+                                          int step, int (&jn)[kUnroll], Best<T, NV>& b) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
-  const int step = L.G * U;
   for (int base = beg; base < end; base += step) {
     int j[U];
 #pragma unroll
@@ -183,13 +182,13 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_ma
       if (it_i >= A.n_items) break;
       const int4 it = A.items[it_i];
       if (!stage_edges(cols, A.idx, it.y, it.z, bar, parity, A.err)) return;
-      const int per = (it.z - it.y + kWarps - 1) / kWarps;
-      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      // batches of kUnroll * G edges dealt to the warps in turn
+      const int wb = it.y + wid * kUnroll * L.G;
       const int colbase = it.y & ~3;
       int jn[kUnroll];
-      batch_ids<kUnroll>(cols, colbase, wb, we, L.g, L.G, jn);
+      batch_ids<kUnroll>(cols, colbase, wb, it.z, L.g, L.G, jn);
       b.init();
-      red_edges<T, NV>(A, L, cols, colbase, wb, we, jn, b);
+      red_edges<T, NV>(A, L, cols, colbase, wb, it.z, kWarps * kUnroll * L.G, jn, b);
       b.merge_subgroups(A.s);
       if (L.g == 0)
 #pragma unroll
@@ -254,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_ma
       int jn2[kUnroll];
       batch_ids<kUnroll>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
       b.init();
-      red_edges<T, NV>(A, L, A.idx, 0, beg, end, jn, b);
+      red_edges<T, NV>(A, L, A.idx, 0, beg, end, kUnroll * L.G, jn, b);
       b.merge_subgroups(A.s);
       if (L.g == 0) write_best<T, NV>(A, L, i, b);
       i = i2;

@@ -70,11 +70,11 @@ struct SpmmUnroll {
 template <typename T, int NV, bool kMask>
 __device__ __forceinline__ void spmm_edges(const SpmmArgs& A, const Lane<NV>& L, int self,
                                            int colstart, const int32_t* cols, int colbase,
-                                           int beg, int end, int (&jn)[SpmmUnroll<kMask>::value],
+                                           int beg, int end, int step,
+                                           int (&jn)[SpmmUnroll<kMask>::value],
                                            float (&acc)[NV][VecOf<T>::n]) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = SpmmUnroll<kMask>::value;
-  const int step = L.G * U;
   const int row_f = A.s.rv * V;
   for (int base = beg; base < end; base += step) {
     int j[U];
@@ -189,14 +189,14 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(
       if (it_i >= A.n_items) break;
       const int4 it = A.items[it_i];
       if (!stage_edges(cols, A.idx, it.y, it.z, bar, parity, A.err)) return;
-      const int per = (it.z - it.y + kWarps - 1) / kWarps;
-      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      // batches of U * G edges dealt to the warps in turn
+      const int wb = it.y + wid * U * L.G;
       const int colbase = it.y & ~3;
       int jn[U];
-      batch_ids<U>(cols, colbase, wb, we, L.g, L.G, jn);
+      batch_ids<U>(cols, colbase, wb, it.z, L.g, L.G, jn);
       zero<T, NV>(acc);
-      spmm_edges<T, NV, kMask>(A, L, it.x, kMask ? A.ptr[it.x] : 0, cols, colbase, wb, we, jn,
-                               acc);
+      spmm_edges<T, NV, kMask>(A, L, it.x, kMask ? A.ptr[it.x] : 0, cols, colbase, wb, it.z,
+                               kWarps * U * L.G, jn, acc);
       subgroup_sums<T, NV>(A.s, acc);
       if (L.g == 0)
 #pragma unroll
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(
       int jn2[U];
       batch_ids<U>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
       zero<T, NV>(acc);
-      spmm_edges<T, NV, kMask>(A, L, i, beg, A.idx, 0, beg, end, jn, acc);
+      spmm_edges<T, NV, kMask>(A, L, i, beg, A.idx, 0, beg, end, U * L.G, jn, acc);
       subgroup_sums<T, NV>(A.s, acc);
       if (L.g == 0) write_row<T, NV>(A, L, i, acc);
       i = i2;

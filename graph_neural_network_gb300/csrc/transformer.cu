@@ -113,11 +113,10 @@ struct GtOnline {
 template <typename T, bool kFixed>
 __device__ __forceinline__ void fwd_edges(const GtArgs& A, const Lane<1>& L, const int32_t* cols,
                                           int colbase, int beg, int end, int sg, int SG,
-                                          int trips, int (&jn)[kU],
+                                          int step, int trips, int (&jn)[kU],
                                           const float (&qs)[VecOf<T>::n], GtOnline<T>& st) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kU;
-  const int step = SG * U;
   int base = beg;
   for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
@@ -212,15 +211,15 @@ __global__ void __launch_bounds__(kThreads, 3) gt_fwd_main(const GtArgs A) {
       if (it_i >= D.n_items) break;
       const int4 it = D.items[it_i];
       if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
-      const int per = (it.z - it.y + kWarps - 1) / kWarps;
-      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      // batches of kU * G edges dealt to the warps in turn
+      const int wb = it.y + wid * kU * L.G, we = it.z;
       const int colbase = it.y & ~3;
       int jn[kU];
       batch_ids<kU>(cols, colbase, wb, we, L.g, L.G, jn);
       query<T>(A, L, it.x, qs);
       GtOnline<T> st;
       st.init();
-      fwd_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, 0, jn, qs, st);
+      fwd_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, kWarps * kU * L.G, 0, jn, qs, st);
       st.merge_subgroups(A.s);
       if (L.g == 0 && L.ok[0]) {
 #pragma unroll
@@ -284,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_fwd_main(const GtArgs A) {
       query<T>(A, L, i, qs);
       GtOnline<T> st;
       st.init();
-      fwd_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, 0, jn, qs, st);
+      fwd_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, kU * L.G, 0, jn, qs, st);
       st.merge_subgroups(A.s);
       if (L.g == 0) fwd_write<T>(A, L, i, st);
       i = i2;
@@ -347,13 +346,12 @@ struct GtDst {
 template <typename T, bool kFixed>
 __device__ __forceinline__ void dst_edges(const GtArgs& A, const Lane<1>& L, const int32_t* cols,
                                           int colbase, int beg, int end, int sg, int SG,
-                                          int trips, int (&jn)[kU],
+                                          int step, int trips, int (&jn)[kU],
                                           const float (&qs)[VecOf<T>::n],
                                           const float (&gi)[VecOf<T>::n], float lse2,
                                           GtDst<T>& sm) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kU;
-  const int step = SG * U;
   int base = beg;
   for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
     int j[U];
@@ -428,8 +426,8 @@ __global__ void __launch_bounds__(kThreads, 3) gt_dst_main(const GtArgs A) {
       if (it_i >= D.n_items) break;
       const int4 it = D.items[it_i];
       if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
-      const int per = (it.z - it.y + kWarps - 1) / kWarps;
-      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      // batches of kU * G edges dealt to the warps in turn
+      const int wb = it.y + wid * kU * L.G, we = it.z;
       const int colbase = it.y & ~3;
       int jn[kU];
       batch_ids<kU>(cols, colbase, wb, we, L.g, L.G, jn);
@@ -438,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_dst_main(const GtArgs A) {
       const float lse2 = L.ok[0] ? A.lse_in[int64_t(it.x) * H + L.k[0]] * kLog2e : 0.f;
       GtDst<T> sm;
       sm.init();
-      dst_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, 0, jn, qs, gi, lse2, sm);
+      dst_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, kWarps * kU * L.G, 0, jn, qs, gi, lse2, sm);
       sm.subgroup_total(A.s);
       float* mine = wbuf + wid * (H + 2 * row_f);
       if (L.g == 0 && L.ok[0]) {
@@ -511,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_dst_main(const GtArgs A) {
         const float lse2 = L.ok[0] ? A.lse_in[int64_t(ii) * H + L.k[0]] * kLog2e : 0.f;
         GtDst<T> sm;
         sm.init();
-        dst_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, trips, jn, qs, gi, lse2, sm);
+        dst_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, kU, trips, jn, qs, gi, lse2, sm);
         if (i >= 0) dst_finish<T>(A, L, i, sm, lse2);
       }
     }
@@ -546,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_dst_main(const GtArgs A) {
       const float lse2 = L.ok[0] ? A.lse_in[int64_t(i) * H + L.k[0]] * kLog2e : 0.f;
       GtDst<T> sm;
       sm.init();
-      dst_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, 0, jn, qs, gi, lse2, sm);
+      dst_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, kU * L.G, 0, jn, qs, gi, lse2, sm);
       sm.subgroup_total(A.s);
       if (L.g == 0) dst_finish<T>(A, L, i, sm, lse2);
       i = i2;
@@ -589,13 +587,12 @@ __global__ void __launch_bounds__(kThreads) gt_dst_merge(const GtArgs A) {
 template <typename T, bool kFixed>
 __device__ __forceinline__ void src_edges(const GtArgs& A, const Lane<1>& L, const int32_t* cols,
                                           int colbase, int beg, int end, int sg, int SG,
-                                          int trips, int (&in)[kU],
+                                          int step, int trips, int (&in)[kU],
                                           const float (&ks)[VecOf<T>::n],
                                           const float (&vj)[VecOf<T>::n],
                                           float (&dk)[VecOf<T>::n], float (&dv)[VecOf<T>::n]) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kU;
-  const int step = SG * U;
   const int H = A.s.H;
   int base = beg;
   for (int t = 0; kFixed ? t < trips : base < end; ++t, base += step) {
@@ -671,8 +668,8 @@ __global__ void __launch_bounds__(kThreads, 3) gt_src_main(const GtArgs A) {
       if (it_i >= D.n_items) break;
       const int4 it = D.items[it_i];
       if (!stage_edges(cols, D.idx, it.y, it.z, bar, parity, A.err)) return;
-      const int per = (it.z - it.y + kWarps - 1) / kWarps;
-      const int wb = min(it.z, it.y + wid * per), we = min(it.z, wb + per);
+      // batches of kU * G edges dealt to the warps in turn
+      const int wb = it.y + wid * kU * L.G, we = it.z;
       const int colbase = it.y & ~3;
       int in[kU];
       batch_ids<kU>(cols, colbase, wb, we, L.g, L.G, in);
@@ -681,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_src_main(const GtArgs A) {
       own_row<T>(A.val, it.x, A.s, L, vj);
       zero<V>(dk);
       zero<V>(dv);
-      src_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, 0, in, ks, vj, dk, dv);
+      src_edges<T, false>(A, L, cols, colbase, wb, we, L.g, L.G, kWarps * kU * L.G, 0, in, ks, vj, dk, dv);
       subgroup_sums<V>(dk, A.s);
       subgroup_sums<V>(dv, A.s);
       if (L.g == 0 && L.ok[0])
@@ -750,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_src_main(const GtArgs A) {
         own_row<T>(A.val, jj, A.s, L, vj);
         zero<V>(dk);
         zero<V>(dv);
-        src_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, trips, in, ks, vj, dk, dv);
+        src_edges<T, true>(A, L, D.idx, 0, beg, end, 0, 1, kU, trips, in, ks, vj, dk, dv);
         if (j >= 0) src_write<T>(A, L, j, dk, dv);
       }
     }
@@ -785,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 3) gt_src_main(const GtArgs A) {
       own_row<T>(A.val, j, A.s, L, vj);
       zero<V>(dk);
       zero<V>(dv);
-      src_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, 0, in, ks, vj, dk, dv);
+      src_edges<T, false>(A, L, D.idx, 0, beg, end, L.g, L.G, kU * L.G, 0, in, ks, vj, dk, dv);
       subgroup_sums<V>(dk, A.s);
       subgroup_sums<V>(dv, A.s);
       if (L.g == 0) src_write<T>(A, L, j, dk, dv);
