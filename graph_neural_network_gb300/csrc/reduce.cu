@@ -11,8 +11,9 @@
 // s = +1 for max and -1 for min: a total order, so the winner does not
 // depend on the order edges are visited and every merge below is exact and
 // reproducible.  Degree-aware tiling as on the page: light nodes get a warp
-// (feature-parallel lanes, edges split over sub-groups), mid nodes a thread
-// block, and hubs are split into edge chunks whose winners are merged with
+// (feature-parallel lanes, edges split over sub-groups), or a sub-group of
+// their own where a row is narrower than a warp, mid nodes a thread block,
+// and hubs are split into edge chunks whose winners are merged with
 // 64-bit atomicMax on packed (value, source) keys -- the page's atomic merge
 // of packed (value, index) pairs -- then decoded by a small kernel.
 //
@@ -102,10 +103,13 @@ struct Best {
   }
 };
 
+// b takes the edges beg + sg, beg + sg + SG, ... < end (sg, SG: this lane's
+// sub-group and the sub-groups sharing the node; 0, 1 for a node of its own).
 template <typename T, int NV>
 __device__ __forceinline__ void red_edges(const RedArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
-                                          int step, int (&jn)[kUnroll], Best<T, NV>& b) {
+                                          int sg, int SG, int step, int (&jn)[kUnroll],
+                                          Best<T, NV>& b) {
   constexpr int V = VecOf<T>::n;
   constexpr int U = kUnroll;
   for (int base = beg; base < end; base += step) {
@@ -119,7 +123,7 @@ __device__ __forceinline__ void red_edges(const RedArgs& A, const Lane<NV>& L,
       for (int a = 0; a < NV; ++a)
         raw[u][a] = (j[u] >= 0 && L.ok[a]) ? ld16(row_base<T>(A.x, j[u], A.s.rv) + 16 * L.q[a])
                                            : make_uint4(0, 0, 0, 0);
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, sg, SG, jn);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (j[u] < 0) continue;
@@ -158,7 +162,7 @@ __device__ __forceinline__ void write_best(const RedArgs& A, const Lane<NV>& L, 
   }
 }
 
-template <typename T, int NV>
+template <typename T, int NV, bool kSub>
 __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_main(const RedArgs A) {
   constexpr int V = VecOf<T>::n;
   const Lane<NV> L(A.s);
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_ma
       int jn[kUnroll];
       batch_ids<kUnroll>(cols, colbase, wb, it.z, L.g, L.G, jn);
       b.init();
-      red_edges<T, NV>(A, L, cols, colbase, wb, it.z, kWarps * kUnroll * L.G, jn, b);
+      red_edges<T, NV>(A, L, cols, colbase, wb, it.z, L.g, L.G, kWarps * kUnroll * L.G, jn, b);
       b.merge_subgroups(A.s);
       if (L.g == 0)
 #pragma unroll
@@ -230,6 +234,34 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_ma
     }
   }
 
+  // ---- light nodes, rows narrower than a warp: one sub-group each --------
+  if constexpr (kSub) {
+    // two nodes per sub-group per pull; no shuffles in the edge loop, so the
+    // sub-groups run their own trip counts
+    constexpr int R = 2;
+    const int npull = R * L.G;
+    for (;;) {
+      int t0 = 0;
+      if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, npull);
+      t0 = __shfl_sync(kFull, t0, 0);
+      if (t0 >= A.n_light) break;
+#pragma unroll 1
+      for (int r = 0; r < R; ++r) {
+        const int64_t t = int64_t(t0) + r * L.G + L.g;
+        if (t >= A.n_light) break;
+        const int i = __ldg(A.light + t);
+        const int beg = __ldg(A.ptr + i), end = __ldg(A.ptr + i + 1);
+        int jn[kUnroll];
+        batch_ids<kUnroll>(A.idx, 0, beg, end, 0, 1, jn);
+        b.init();
+        red_edges<T, NV>(A, L, A.idx, 0, beg, end, 0, 1, kUnroll, jn, b);
+        write_best<T, NV>(A, L, i, b);
+      }
+    }
+    return;
+  }
+
+  // ---- light nodes, rows of a whole warp: one warp each --------------------
   for (;;) {
     int t0 = 0;
     if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
@@ -253,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_ma
       int jn2[kUnroll];
       batch_ids<kUnroll>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
       b.init();
-      red_edges<T, NV>(A, L, A.idx, 0, beg, end, kUnroll * L.G, jn, b);
+      red_edges<T, NV>(A, L, A.idx, 0, beg, end, L.g, L.G, kUnroll * L.G, jn, b);
       b.merge_subgroups(A.s);
       if (L.g == 0) write_best<T, NV>(A, L, i, b);
       i = i2;
@@ -335,15 +367,17 @@ cudaError_t launch_fwd_t(const RedArgs& A, int sm_count, cudaStream_t st) {
   cudaError_t e;
   if (A.n_items + A.n_light > 0) {
     const size_t smem = size_t(A.col_off) + size_t(kWarps) * A.s.rv * V * 8;
+    void (*kernel)(const RedArgs) = red_fwd_main<T, NV, false>;
+    if constexpr (NV == 1)
+      if (A.s.lpr < 32) kernel = red_fwd_main<T, NV, true>;
     if (smem > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(red_fwd_main<T, NV>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) !=
-            cudaSuccess)
+        (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(smem))) != cudaSuccess)
       return e;
     const int64_t work = A.n_items + (A.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
-    const int64_t cap = persistent_blocks(red_fwd_main<T, NV>, smem, sm_count);
+    const int64_t cap = persistent_blocks(kernel, smem, sm_count);
     const int64_t blocks = work < cap ? work : cap;
-    red_fwd_main<T, NV><<<unsigned(blocks), kThreads, smem, st>>>(A);
+    kernel<<<unsigned(blocks), kThreads, smem, st>>>(A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (A.n_hubs > 0) {

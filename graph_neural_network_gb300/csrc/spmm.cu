@@ -13,9 +13,12 @@
 // A~ factors as diag(c_out) A diag(c_in) with per-node coefficients (1/deg
 // or deg^-1/2) computed once per call from row_ptr; each edge gathers one
 // feature row and one float.  Degree-aware tiling as in the attention
-// kernels: light nodes get a warp, mid nodes a block (edge list staged in
-// shared memory by a bulk copy), hubs are split into edge chunks whose
-// partial sums a second kernel adds in chunk order.
+// kernels: light nodes get a warp, or a sub-group of their own where a row is
+// narrower than a warp, mid nodes a block (edge list staged in shared memory
+// by a bulk copy), hubs are split into edge chunks whose partial sums a
+// second kernel adds in chunk order.  Rows that start on 32-byte boundaries
+// and hold an even number of 16-byte vectors (up to 1024 bytes) are read as
+// 32-byte lane vectors.
 #include "device.cuh"
 
 namespace gnn {
@@ -54,47 +57,51 @@ __global__ void spmm_coef(const int32_t* ptr, int64_t n, int mode, float* c) {
   }
 }
 
-// Edges in flight per lane: kUnroll, or two in the masked mode (each edge
-// also gathers the row's winners, four bytes per feature).
-template <bool kMask>
+// Edges in flight per lane: 64 bytes of rows (4 edges of 16-byte lane
+// vectors, 2 of 32-byte ones), or two in the masked mode (each edge also
+// gathers the row's winners, four bytes per feature; 16-byte vectors only).
+template <bool kMask, int VB>
 struct SpmmUnroll {
-  static constexpr int value = kMask ? 2 : kUnroll;
+  static constexpr int value = kMask ? 2 : UnrollOf<VB>::value;
 };
 
-// acc += c_in(j) x_j over the edges beg + g, beg + g + G, ... < end.  Masked
-// mode (the max / min backward over the CSC, `self` the output node whose
-// list starts at edge `colstart`): acc[f] += x_j[f] where win[j][f] == self,
-// once per destination j -- a repeated edge (the same j right before it in
-// the ascending list) adds nothing, since a winner is counted per
-// destination, not per edge.
-template <typename T, int NV, bool kMask>
+// acc += c_in(j) x_j over the edges beg + sg, beg + sg + SG, ... < end
+// (sg, SG: this lane's sub-group and the sub-groups sharing the node; 0, 1
+// when a sub-group has the node to itself).  Masked mode (the max / min
+// backward over the CSC, `self` the output node whose list starts at edge
+// `colstart`): acc[f] += x_j[f] where win[j][f] == self, once per destination
+// j -- a repeated edge (the same j right before it in the ascending list)
+// adds nothing, since a winner is counted per destination, not per edge.
+template <typename T, int NV, int VB, bool kMask>
 __device__ __forceinline__ void spmm_edges(const SpmmArgs& A, const Lane<NV>& L, int self,
                                            int colstart, const int32_t* cols, int colbase,
-                                           int beg, int end, int step,
-                                           int (&jn)[SpmmUnroll<kMask>::value],
-                                           float (&acc)[NV][VecOf<T>::n]) {
-  constexpr int V = VecOf<T>::n;
-  constexpr int U = SpmmUnroll<kMask>::value;
+                                           int beg, int end, int sg, int SG, int step,
+                                           int (&jn)[SpmmUnroll<kMask, VB>::value],
+                                           float (&acc)[NV][ElemsOf<T, VB>::n]) {
+  static_assert(!kMask || VB == 16, "masked mode uses 16-byte lane vectors");
+  constexpr int V = ElemsOf<T, VB>::n;
+  constexpr int U = SpmmUnroll<kMask, VB>::value;
   const int row_f = A.s.rv * V;
   for (int base = beg; base < end; base += step) {
     int j[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) j[u] = jn[u];
-    uint4 raw[U][NV];
+    RawV<VB> raw[U][NV];
     float w[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
 #pragma unroll
       for (int v = 0; v < NV; ++v)
-        raw[u][v] = (j[u] >= 0 && L.ok[v]) ? ld16(row_base<T>(A.x, j[u], A.s.rv) + 16 * L.q[v])
-                                           : make_uint4(0, 0, 0, 0);
+        raw[u][v] = (j[u] >= 0 && L.ok[v])
+                        ? ldv<VB>(row_at<VB>(A.x, j[u], A.s.rv) + VB * L.q[v])
+                        : zero_raw<VB>();
       w[u] = j[u] < 0 ? 0.f : (A.c_in ? __ldg(A.c_in + j[u]) : 1.f);
     }
     int wn[kMask ? U : 1][kMask ? NV : 1][kMask ? V : 1];
-    if (kMask) {
+    if constexpr (kMask) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int e = base + u * L.G + L.g;
+        const int e = base + u * SG + sg;
         const bool repeat = j[u] >= 0 && e > colstart && __ldg(A.idx + e - 1) == j[u];
 #pragma unroll
         for (int v = 0; v < NV; ++v)
@@ -111,14 +118,14 @@ __device__ __forceinline__ void spmm_edges(const SpmmArgs& A, const Lane<NV>& L,
           }
       }
     }
-    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, L.g, L.G, jn);
+    if (base + step < end) batch_ids<U>(cols, colbase, base + step, end, sg, SG, jn);
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         float xv[V];
-        unpack<T>(raw[u][v], xv);
-        if (kMask) {
+        unpackv<T, VB>(raw[u][v], xv);
+        if constexpr (kMask) {
 #pragma unroll
           for (int c = 0; c < V; ++c) acc[v][c] += wn[u][v][c] == self ? xv[c] : 0.f;
         } else {
@@ -128,46 +135,44 @@ __device__ __forceinline__ void spmm_edges(const SpmmArgs& A, const Lane<NV>& L,
   }
 }
 
-template <typename T, int NV>
-__device__ __forceinline__ void zero(float (&acc)[NV][VecOf<T>::n]) {
+template <typename T, int NV, int VB>
+__device__ __forceinline__ void zero(float (&acc)[NV][ElemsOf<T, VB>::n]) {
 #pragma unroll
   for (int v = 0; v < NV; ++v)
 #pragma unroll
-    for (int c = 0; c < VecOf<T>::n; ++c) acc[v][c] = 0.f;
+    for (int c = 0; c < ElemsOf<T, VB>::n; ++c) acc[v][c] = 0.f;
 }
 
 // Sum the accumulators of the warp's sub-groups (every lane ends with the total).
-template <typename T, int NV>
-__device__ __forceinline__ void subgroup_sums(const Shape& s, float (&acc)[NV][VecOf<T>::n]) {
+template <typename T, int NV, int VB>
+__device__ __forceinline__ void subgroup_sums(const Shape& s,
+                                              float (&acc)[NV][ElemsOf<T, VB>::n]) {
   for (int o = s.lpr; o < 32; o <<= 1)
 #pragma unroll
     for (int v = 0; v < NV; ++v)
 #pragma unroll
-      for (int c = 0; c < VecOf<T>::n; ++c) acc[v][c] += __shfl_xor_sync(kFull, acc[v][c], o);
+      for (int c = 0; c < ElemsOf<T, VB>::n; ++c)
+        acc[v][c] += __shfl_xor_sync(kFull, acc[v][c], o);
 }
 
 // out_node = c_out(node) * acc.
-template <typename T, int NV>
+template <typename T, int NV, int VB>
 __device__ __forceinline__ void write_row(const SpmmArgs& A, const Lane<NV>& L, int64_t node,
-                                          const float (&acc)[NV][VecOf<T>::n]) {
-  constexpr int V = VecOf<T>::n;
+                                          float (&acc)[NV][ElemsOf<T, VB>::n]) {
   const float c = A.c_out ? __ldg(A.c_out + node) : 1.f;
-  char* orow = reinterpret_cast<char*>(A.out) + node * int64_t(A.s.rv) * 16;
+  char* orow = reinterpret_cast<char*>(A.out) + node * int64_t(A.s.rv) * VB;
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     if (!L.ok[v]) continue;
-    float y[V];
-#pragma unroll
-    for (int k = 0; k < V; ++k) y[k] = acc[v][k];
-    scale<V>(y, c);
-    st16(orow + 16 * L.q[v], pack<T>(y));
+    scale<ElemsOf<T, VB>::n>(acc[v], c);
+    storev<T, VB>(orow + VB * L.q[v], acc[v]);
   }
 }
 
-template <typename T, int NV, bool kMask>
+template <typename T, int NV, int VB, bool kMask, bool kSub>
 __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(const SpmmArgs A) {
-  constexpr int V = VecOf<T>::n;
-  constexpr int U = SpmmUnroll<kMask>::value;
+  constexpr int V = ElemsOf<T, VB>::n;
+  constexpr int U = SpmmUnroll<kMask, VB>::value;
   const Lane<NV> L(A.s);
   const int wid = threadIdx.x >> 5;
   const int row_f = A.s.rv * V;
@@ -194,10 +199,10 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(
       const int colbase = it.y & ~3;
       int jn[U];
       batch_ids<U>(cols, colbase, wb, it.z, L.g, L.G, jn);
-      zero<T, NV>(acc);
-      spmm_edges<T, NV, kMask>(A, L, it.x, kMask ? A.ptr[it.x] : 0, cols, colbase, wb, it.z,
-                               kWarps * U * L.G, jn, acc);
-      subgroup_sums<T, NV>(A.s, acc);
+      zero<T, NV, VB>(acc);
+      spmm_edges<T, NV, VB, kMask>(A, L, it.x, kMask ? A.ptr[it.x] : 0, cols, colbase, wb, it.z,
+                                   L.g, L.G, kWarps * U * L.G, jn, acc);
+      subgroup_sums<T, NV, VB>(A.s, acc);
       if (L.g == 0)
 #pragma unroll
         for (int v = 0; v < NV; ++v)
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(
             acc[v][c] = t;
           }
         if (it.w < 0) {
-          write_row<T, NV>(A, L, it.x, acc);
+          write_row<T, NV, VB>(A, L, it.x, acc);
         } else {
 #pragma unroll
           for (int v = 0; v < NV; ++v) {
@@ -234,7 +239,35 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(
     }
   }
 
-  // ---- light nodes: one warp each, pulled kGrab at a time ----------------
+  // ---- light nodes, rows narrower than a warp: one sub-group each --------
+  if constexpr (kSub) {
+    // a pull takes two nodes per sub-group; the edge loop has no shuffles, so
+    // the sub-groups of a warp run their own trip counts (the light list is
+    // sorted by degree, so they are nearly equal)
+    constexpr int R = 2;
+    const int npull = R * L.G;
+    for (;;) {
+      int t0 = 0;
+      if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, npull);
+      t0 = __shfl_sync(kFull, t0, 0);
+      if (t0 >= A.n_light) break;
+#pragma unroll 1
+      for (int r = 0; r < R; ++r) {
+        const int64_t t = int64_t(t0) + r * L.G + L.g;
+        if (t >= A.n_light) break;
+        const int i = __ldg(A.light + t);
+        const int beg = __ldg(A.ptr + i), end = __ldg(A.ptr + i + 1);
+        int jn[U];
+        batch_ids<U>(A.idx, 0, beg, end, 0, 1, jn);
+        zero<T, NV, VB>(acc);
+        spmm_edges<T, NV, VB, kMask>(A, L, i, beg, A.idx, 0, beg, end, 0, 1, U, jn, acc);
+        write_row<T, NV, VB>(A, L, i, acc);
+      }
+    }
+    return;
+  }
+
+  // ---- light nodes, rows of a whole warp: one warp each, kGrab at a time --
   for (;;) {
     int t0 = 0;
     if (L.lane == 0) t0 = atomicAdd(A.ctr + 1, kGrab);
@@ -257,10 +290,10 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) spmm_main(
       const int e2 = __shfl_sync(kFull, my_e, nq);
       int jn2[U];
       batch_ids<U>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
-      zero<T, NV>(acc);
-      spmm_edges<T, NV, kMask>(A, L, i, beg, A.idx, 0, beg, end, U * L.G, jn, acc);
-      subgroup_sums<T, NV>(A.s, acc);
-      if (L.g == 0) write_row<T, NV>(A, L, i, acc);
+      zero<T, NV, VB>(acc);
+      spmm_edges<T, NV, VB, kMask>(A, L, i, beg, A.idx, 0, beg, end, L.g, L.G, U * L.G, jn, acc);
+      subgroup_sums<T, NV, VB>(A.s, acc);
+      if (L.g == 0) write_row<T, NV, VB>(A, L, i, acc);
       i = i2;
       beg = b2;
       end = e2;
@@ -280,8 +313,8 @@ __global__ void __launch_bounds__(kThreads) spmm_merge(const SpmmArgs A) {
   const int4 hb = A.hubs[t];
   const int row_f = A.s.rv * V;
   float acc[NV][V], cmp[NV][V];
-  zero<T, NV>(acc);
-  zero<T, NV>(cmp);
+  zero<T, NV, 16>(acc);
+  zero<T, NV, 16>(cmp);
   for (int c = 0; c < hb.z; ++c) {
     const int64_t slot = int64_t(hb.y) + c;
 #pragma unroll
@@ -298,31 +331,89 @@ __global__ void __launch_bounds__(kThreads) spmm_merge(const SpmmArgs A) {
       }
     }
   }
-  write_row<T, NV>(A, L, hb.x, acc);
+  write_row<T, NV, 16>(A, L, hb.x, acc);
 }
 
-template <typename T, int NV>
-cudaError_t launch_t(const SpmmArgs& A, int sm_count, cudaStream_t st) {
-  constexpr int V = VecOf<T>::n;
+// The persistent kernel for A's shape: a sub-group per light node where a
+// row is narrower than a warp.
+template <typename T, int NV, int VB>
+cudaError_t launch_main(const SpmmArgs& A, int sm_count, cudaStream_t st) {
+  constexpr int V = ElemsOf<T, VB>::n;
+  if (A.n_items + A.n_light <= 0) return cudaSuccess;
+  const bool sub = A.s.lpr < 32;
+  void (*kernel)(const SpmmArgs);
+  if constexpr (VB == 32) {
+    kernel = sub ? spmm_main<T, NV, VB, false, true> : spmm_main<T, NV, VB, false, false>;
+  } else if constexpr (NV == 1) {
+    if (A.win)
+      kernel = sub ? spmm_main<T, NV, VB, true, true> : spmm_main<T, NV, VB, true, false>;
+    else
+      kernel = sub ? spmm_main<T, NV, VB, false, true> : spmm_main<T, NV, VB, false, false>;
+  } else {
+    kernel = A.win ? spmm_main<T, NV, VB, true, false> : spmm_main<T, NV, VB, false, false>;
+  }
+  const size_t smem = size_t(A.col_off) + size_t(kWarps) * A.s.rv * V * 4;
   cudaError_t e;
-  if (A.n_items + A.n_light > 0) {
-    const size_t smem = size_t(A.col_off) + size_t(kWarps) * A.s.rv * V * 4;
-    auto kernel = A.win ? spmm_main<T, NV, true> : spmm_main<T, NV, false>;
-    if (smem > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(smem))) != cudaSuccess)
-      return e;
-    const int64_t work = A.n_items + (A.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
-    const int64_t cap = persistent_blocks(kernel, smem, sm_count);
-    const int64_t blocks = work < cap ? work : cap;
-    kernel<<<unsigned(blocks), kThreads, smem, st>>>(A);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (smem > 48 * 1024 &&
+      (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(smem))) != cudaSuccess)
+    return e;
+  const int64_t work = A.n_items + (A.n_light + kWarps * kGrab - 1) / (kWarps * kGrab);
+  const int64_t cap = persistent_blocks(kernel, smem, sm_count);
+  const int64_t blocks = work < cap ? work : cap;
+  kernel<<<unsigned(blocks), kThreads, smem, st>>>(A);
+  return cudaGetLastError();
+}
+
+// Hub merge over the 16-byte-vector shape of the row (the chunk partials are
+// plain float rows whatever lane vectors the main kernel used).
+template <typename T>
+cudaError_t launch_merge(const SpmmArgs& A16, cudaStream_t st) {
+  if (A16.n_hubs <= 0) return cudaSuccess;
+  const unsigned grid = unsigned((A16.n_hubs + kWarps - 1) / kWarps);
+  switch (A16.s.nv) {
+    case 1: spmm_merge<T, 1><<<grid, kThreads, 0, st>>>(A16); break;
+    case 2: spmm_merge<T, 2><<<grid, kThreads, 0, st>>>(A16); break;
+    case 4: spmm_merge<T, 4><<<grid, kThreads, 0, st>>>(A16); break;
+    default: return cudaErrorInvalidValue;
   }
-  if (A.n_hubs > 0) {
-    spmm_merge<T, NV><<<unsigned((A.n_hubs + kWarps - 1) / kWarps), kThreads, 0, st>>>(A);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// 32-byte lane vectors: rows of an even number of 16-byte vectors up to
+// 1024 bytes, one vector per lane.
+bool spmm_wide_shape(const Shape& s, Shape* w) {
+  if (s.rv % 2 || s.rv > 64) return false;
+  *w = s;
+  w->rv = s.rv / 2;
+  w->hv = 1;
+  w->hv_log2 = 0;
+  w->nv = 1;
+  w->lpr = 1;
+  while (w->lpr < w->rv) w->lpr <<= 1;
+  w->lpr_log2 = 0;
+  while ((1 << w->lpr_log2) < w->lpr) ++w->lpr_log2;
+  return true;
+}
+
+template <typename T>
+cudaError_t launch_all(const SpmmArgs& A16, int sm_count, cudaStream_t st) {
+  cudaError_t e;
+  Shape w;
+  if (!A16.win && spmm_wide_shape(A16.s, &w) && aligned32(A16.x)) {
+    SpmmArgs A = A16;
+    A.s = w;
+    e = launch_main<T, 1, 32>(A, sm_count, st);
+  } else {
+    switch (A16.s.nv) {
+      case 1: e = launch_main<T, 1, 16>(A16, sm_count, st); break;
+      case 2: e = launch_main<T, 2, 16>(A16, sm_count, st); break;
+      case 4: e = launch_main<T, 4, 16>(A16, sm_count, st); break;
+      default: return cudaErrorInvalidValue;
+    }
   }
-  return cudaSuccess;
+  if (e != cudaSuccess) return e;
+  return launch_merge<T>(A16, st);
 }
 
 }  // namespace
@@ -366,20 +457,8 @@ cudaError_t launch_spmm(const gnn_graph* g, const Shape& s, gnn_dtype dt, int no
                                                      norm == GNN_NORM_MEAN ? 1 : 2, coef);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (dt == GNN_F32) {
-    switch (s.nv) {
-      case 1: return launch_t<float, 1>(A, g->sm_count, st);
-      case 2: return launch_t<float, 2>(A, g->sm_count, st);
-      case 4: return launch_t<float, 4>(A, g->sm_count, st);
-    }
-  } else {
-    switch (s.nv) {
-      case 1: return launch_t<__nv_bfloat16, 1>(A, g->sm_count, st);
-      case 2: return launch_t<__nv_bfloat16, 2>(A, g->sm_count, st);
-      case 4: return launch_t<__nv_bfloat16, 4>(A, g->sm_count, st);
-    }
-  }
-  return cudaErrorInvalidValue;
+  if (dt == GNN_F32) return launch_all<float>(A, g->sm_count, st);
+  return launch_all<__nv_bfloat16>(A, g->sm_count, st);
 }
 
 size_t spmm_ws_bytes(const gnn_graph* g, const Shape& s) {

@@ -66,6 +66,42 @@ def test_spmm_power_law_default_tiling(dtype):
     check(rp, ci, 128, dtype, "sym", what="chung-lu")
 
 
+def _offset_copy(x, dtype):
+    """x on the device at an address 16 bytes past a 32-byte boundary."""
+    t = to_device(x, dtype)
+    pad = 16 // t.element_size()
+    buf = torch.empty(t.numel() + pad, dtype=t.dtype, device="cuda")
+    view = buf[pad:].view(t.shape)
+    view.copy_(t)
+    assert view.data_ptr() % 32 == 16
+    return view
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_spmm_rows_off_32_byte_boundaries(dtype):
+    """Rows of an even number of 16-byte vectors run with 32-byte lane vectors
+    when they start on 32-byte boundaries, else with 16-byte ones; both
+    against the oracle, light nodes one per sub-group, mid nodes and hubs."""
+    import graph_neural_network_gb300 as gnn
+    rp, ci = testgraphs.with_in_degrees(THRESHOLD_DEGREES, n_nodes=2500, seed=61)
+    n = len(rp) - 1
+    F = 64 if dtype == "f32" else 128
+    x = features(n, F, dtype, 61)
+    g_out = features(n, F, dtype, 62)
+    g = device_graph(dict(row_ptr=np.asarray(rp, np.int32), col=np.asarray(ci, np.int32)),
+                     (8, 64, 16))
+    f = oracle.spmm_forward(rp, ci, x, "sym", with_mag=True)
+    b = oracle.spmm_backward(rp, ci, g_out, "sym", with_mag=True)
+    for xd, gd in ((to_device(x, dtype), to_device(g_out, dtype)),
+                   (_offset_copy(x, dtype), _offset_copy(g_out, dtype))):
+        out = gnn.gcn_forward(g, xd, "sym")
+        dx = gnn.gcn_backward(g, gd, "sym")
+        torch.cuda.synchronize()
+        what = f"offset {xd.data_ptr() % 32}"
+        assert_close(to_f64(out), f["out"], dtype, f["out_mag"], f"{what} sym out")
+        assert_close(to_f64(dx), b["dx"], dtype, b["dx_mag"], f"{what} sym dx")
+
+
 def test_spmm_reproducible_and_autograd():
     import graph_neural_network_gb300 as gnn
     rp, ci = workload.chung_lu(20_000, 2.1, 20.0, 5_000.0, 29)
