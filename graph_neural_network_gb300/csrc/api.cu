@@ -94,8 +94,18 @@ namespace {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool tiling_ok(const gnn_tiling& t) {
-  return t.light_max_deg >= 0 && t.cta_max_deg >= t.light_max_deg && t.cta_max_deg <= 16384 &&
-         t.hub_chunk >= 1 && t.hub_chunk <= 16384;
+  return t.light_max_deg >= GNN_LIGHT_AUTO && t.cta_max_deg >= 0 &&
+         t.cta_max_deg >= t.light_max_deg && t.cta_max_deg <= 16384 && t.hub_chunk >= 1 &&
+         t.hub_chunk <= 16384;
+}
+
+// The tiling that bounds the prepared graph's buffers: an automatic light
+// threshold is never below its floor (or cta_max_deg), and fewer light nodes
+// only mean more block items, which the bound covers.
+gnn_tiling bound_tiling(gnn_tiling t) {
+  if (t.light_max_deg == GNN_LIGHT_AUTO)
+    t.light_max_deg = t.cta_max_deg < gnn::kLightAutoMin ? t.cta_max_deg : gnn::kLightAutoMin;
+  return t;
 }
 
 gnn_tiling resolve_tiling(const gnn_tiling* t) {
@@ -125,7 +135,7 @@ extern "C" {
 
 void gnn_default_tiling(gnn_tiling* t) {
   if (!t) return;
-  t->light_max_deg = 64;
+  t->light_max_deg = GNN_LIGHT_AUTO;
   t->cta_max_deg = 4096;
   t->hub_chunk = 2048;
 }
@@ -149,7 +159,7 @@ const char* gnn_status_string(gnn_status s) {
 size_t gnn_graph_buffer_bytes(int64_t n_nodes, int64_t n_edges, const gnn_tiling* tiling) {
   const gnn_tiling t = resolve_tiling(tiling);
   if (!sizes_ok(n_nodes, n_edges) || !tiling_ok(t)) return 0;
-  return gnn::graph_buffer_bytes(n_nodes, n_edges, t);
+  return gnn::graph_buffer_bytes(n_nodes, n_edges, bound_tiling(t));
 }
 
 size_t gnn_graph_scratch_bytes(int64_t n_nodes, int64_t n_edges) {
@@ -170,7 +180,7 @@ gnn_status gnn_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t* ro
   if (!aligned(row_ptr_d, 4) || !aligned(col_idx_d, 16) || !aligned(buffer_d, 256) ||
       !aligned(scratch_d, 256))
     return GNN_ERR_INVALID_ARG;
-  if (buffer_bytes < gnn::graph_buffer_bytes(n_nodes, n_edges, t) ||
+  if (buffer_bytes < gnn::graph_buffer_bytes(n_nodes, n_edges, bound_tiling(t)) ||
       scratch_bytes < gnn::graph_scratch_bytes(n_nodes, n_edges))
     return GNN_ERR_WORKSPACE_TOO_SMALL;
   gnn_graph* g = new (std::nothrow) gnn_graph;
@@ -184,6 +194,8 @@ gnn_status gnn_graph_prepare(int64_t n_nodes, int64_t n_edges, const int32_t* ro
     delete g;
     return GNN_ERR_CUDA;
   }
+  if (t.light_max_deg == GNN_LIGHT_AUTO)
+    g->tiling.light_max_deg = gnn::auto_light_max(n_edges, g->sm_count, t.cta_max_deg);
   const gnn_status s =
       gnn::prepare_graph(g, row_ptr_d, col_idx_d, static_cast<char*>(buffer_d), buffer_bytes,
                          static_cast<char*>(scratch_d), scratch_bytes,

@@ -69,6 +69,25 @@ struct WsLayout {
 // before the persistent kernels pull work from them.
 constexpr int kCounters = 8;
 
+// Automatic light-node threshold.  A light node runs on one warp or
+// sub-group with no barrier and no merge, while a block item pays a work
+// pull, the staging of its edge list and a block-wide merge; so as many
+// nodes as possible should be light, as long as the largest light node (its
+// edges walked by one sub-group) stays short beside the work of one resident
+// warp.  With 32 resident warps per SM, E / (SMs * 32) edges per warp, the
+// threshold is a sixteenth of that, rounded to a power of two, within
+// [kLightAutoMin, kLightAutoMax] and at most cta_max_deg.  On GB300 this is
+// 256 for 18.7M edges and 1024 for 118M or more.
+constexpr int kLightAutoMin = 64;
+constexpr int kLightAutoMax = 1024;
+inline int auto_light_max(int64_t e, int sm_count, int cta_max_deg) {
+  const double per = double(e) / (double(sm_count > 0 ? sm_count : 1) * 32.0 * 16.0);
+  int t = kLightAutoMin;
+  // nearest power of two on a log scale: double while per >= t * sqrt(2)
+  while (t < kLightAutoMax && per >= double(t) * 1.4142135623730951) t *= 2;
+  return t < cta_max_deg ? t : cta_max_deg;
+}
+
 bool make_shape(int H, int D, gnn_dtype dt, Shape* s);
 // The geometry of 32-byte lane vectors for the same rows (false when a head
 // spans less than 32 bytes or a row more than 1024).

@@ -73,18 +73,25 @@ typedef enum {
 typedef enum { GNN_F32 = 0, GNN_BF16 = 1 } gnn_dtype;
 
 /* Degree-aware tiling thresholds (in edges).  A node of in-degree (CSR) or
- * out-degree (CSC) d is "light" when d <= light_max_deg and gets one warp;
- * "mid" when light_max_deg < d <= cta_max_deg and gets one thread block;
- * a "hub" otherwise, split into chunks of hub_chunk edges, one thread block
- * each.  Constraints: 0 <= light_max_deg <= cta_max_deg <= 16384,
+ * out-degree (CSC) d is "light" when d <= light_max_deg and gets one warp
+ * (or a sub-group of one, for rows narrower than a warp); "mid" when
+ * light_max_deg < d <= cta_max_deg and gets one thread block; a "hub"
+ * otherwise, split into chunks of hub_chunk edges, one thread block each.
+ * light_max_deg = GNN_LIGHT_AUTO lets gnn_graph_prepare choose it from the
+ * edge count and the device's SM count: E / (SMs * 512) rounded to a power of
+ * two, within [64, 1024] and at most cta_max_deg (gnn_graph_stats reports the
+ * value chosen).  Constraints: light_max_deg = GNN_LIGHT_AUTO or
+ * 0 <= light_max_deg <= cta_max_deg; cta_max_deg <= 16384;
  * 1 <= hub_chunk <= 16384. */
+#define GNN_LIGHT_AUTO (-1)
 typedef struct {
   int32_t light_max_deg;
   int32_t cta_max_deg;
   int32_t hub_chunk;
 } gnn_tiling;
 
-/* Fills *t with the default thresholds. */
+/* Fills *t with the default thresholds: an automatic light threshold,
+ * cta_max_deg 4096, hub_chunk 2048. */
 void gnn_default_tiling(gnn_tiling* t);
 
 typedef struct gnn_graph gnn_graph; /* opaque; immutable after prepare */

@@ -50,7 +50,17 @@ def test_version_and_status_strings(lib):
 def test_sizes_are_host_only(lib):
     from graph_neural_network_gb300 import _native
     t = _native.default_tiling()
-    assert (t.light_max_deg, t.cta_max_deg, t.hub_chunk) == (64, 4096, 2048)
+    assert (t.light_max_deg, t.cta_max_deg, t.hub_chunk) == (-1, 4096, 2048)   # automatic
+    # an automatic light threshold is bounded by the buffer of its floor, 64
+    for n, e in ((1000, 20000), (50_000, 3_000_000)):
+        floor = _native.Tiling(64, 4096, 2048)
+        assert lib.gnn_graph_buffer_bytes(n, e, None) == \
+            lib.gnn_graph_buffer_bytes(n, e, ctypes.byref(floor))
+        auto_low = _native.Tiling(-1, 16, 8)              # floor above cta_max_deg: 16
+        low = _native.Tiling(16, 16, 8)
+        assert lib.gnn_graph_buffer_bytes(n, e, ctypes.byref(auto_low)) == \
+            lib.gnn_graph_buffer_bytes(n, e, ctypes.byref(low))
+    assert lib.gnn_graph_buffer_bytes(10, 10, ctypes.byref(_native.Tiling(-2, 64, 8))) == 0
     b1 = lib.gnn_graph_buffer_bytes(1000, 20000, None)
     b2 = lib.gnn_graph_buffer_bytes(1000, 40000, None)
     assert 0 < b1 < b2

@@ -105,3 +105,34 @@ def test_empty_graph():
                   torch.zeros(0, dtype=torch.int32, device="cuda"))
     st = g.stats()
     assert st["n"] == 0 and st["e"] == 0
+
+
+def auto_light_max(e, sm_count, cta_max):
+    """The automatic light threshold as documented for gnn_tiling: E / (SMs * 512)
+    rounded to a power of two (on a log scale), within [64, 1024], at most
+    cta_max_deg."""
+    per = e / (sm_count * 512.0)
+    t = 64
+    while t < 1024 and per >= t * 2 ** 0.5:
+        t *= 2
+    return min(t, cta_max)
+
+
+@pytest.mark.parametrize("scale,ef", [(10, 8), (16, 16), (19, 32)])
+def test_automatic_light_threshold(scale, ef):
+    """The default tiling picks the light threshold from the edge count and the
+    SM count, and the buckets follow it exactly."""
+    rp, ci = workload.rmat(scale, ef, 0.57, 0.19, 0.19, scale)
+    case = make_case(rp, ci, 1, 16, "f32", 1)
+    g = device_graph(case)                       # default tiling: automatic threshold
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    want = auto_light_max(len(ci), sm, 4096)
+    st = g.stats()
+    assert st["light_max_deg"] == want and st["cta_max_deg"] == 4096
+    arr = {k: v.cpu().numpy() for k, v in g.arrays().items()}
+    col_ptr, _ = host_csc(rp, ci)
+    for d, ptr in (("csr", rp), ("csc", col_ptr)):
+        light, items, hubs = host_buckets(ptr, (want, 4096, 2048))
+        assert np.array_equal(arr[f"{d}_light"], light)
+        assert np.array_equal(arr[f"{d}_items"].astype(np.int64), items)
+        assert np.array_equal(arr[f"{d}_hubs"].astype(np.int64), hubs)
