@@ -212,3 +212,53 @@ def test_rows_off_32_byte_boundaries_take_16_byte_vectors(dtype):
         gpu = dict(out=to_f64(out), lse=to_f64(lse), dh=to_f64(dh), da_src=to_f64(da_s),
                    da_dst=to_f64(da_d))
         compare(gpu, ref, dtype, what=f"offset {h.data_ptr() % 32}")
+
+
+def _positive(seed, stream, shape):
+    """Values in (0.75, 1.25): 1 + tanh(x) / 4 of seeded normals."""
+    return (1.0 + 0.25 * np.tanh(workload.normal_f32(seed, stream, shape, 1.0))).astype(np.float32)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_attention_gradients_without_cancellation(dtype):
+    """da_src and da_dst held to the plain atol + rtol bound, with no float32
+    summation term, on inputs whose sums do not cancel.  Every destination
+    has two in-edges: from an A node with a positive row and from a B node
+    with a zero row.  Rows, dout and a_src are positive and a_dst negative,
+    so z > 0 on the A edge and z < 0 on the B edge, at least 0.25 from the
+    kink; then de > 0 on every A edge and the terms of da_src (de h_a) are all
+    positive, and those of da_dst (de (1 - slope) h_i per destination) too.
+    The A nodes' out-degrees follow a Zipf law, so the source pass runs CSC
+    hubs of several chunks as well as light and mid nodes.  A dropped or
+    doubled contribution to either sum fails the plain bound."""
+    n_a, n_b, n_c = 2000, 2000, 30000
+    rp, ci = testgraphs.paired_sources(n_a, n_b, n_c, seed=71)
+    n = len(rp) - 1
+    H, D = 2, (16 if dtype == "f32" else 32)
+    h = _positive(71, 1, (n, H, D))
+    h[n_a:n_a + n_b] = 0.0
+    dout = _positive(71, 4, (n, H, D))
+    a_s = np.full((H, D), 2.0 / D, np.float32)     # a_src . h_a in (1.5, 2.5)
+    a_d = np.full((H, D), -0.5 / D, np.float32)    # a_dst . h_i in (-0.625, -0.375)
+    if dtype == "bf16":
+        h = workload.f32_to_bf16_bits(h)
+        dout = workload.f32_to_bf16_bits(dout)
+    case = dict(row_ptr=rp, col=ci, h=h, dout=dout, a_src=a_s, a_dst=a_d, H=H, D=D,
+                dtype=dtype, slope=0.2)
+    # the construction, in float64: z = a_dst.h_i + a_src.h_j is at least 0.25 on every
+    # A edge and at most -0.25 on every B edge (per head)
+    hf = workload.bf16_bits_to_f32(h) if dtype == "bf16" else h
+    sc_src = np.einsum("nkd,kd->nk", hf.astype(np.float64), a_s.astype(np.float64))
+    sc_dst = np.einsum("nkd,kd->nk", hf.astype(np.float64), a_d.astype(np.float64))
+    dst = np.repeat(np.arange(n), np.diff(rp))
+    z = sc_dst[dst] + sc_src[ci]
+    assert np.all(z[0::2] >= 0.25) and np.all(z[1::2] <= -0.25)
+    ref = run_oracle(case)
+    assert np.all(ref["da_src"] > 0) and np.all(ref["da_dst"] > 0)
+    assert not np.any(ref["da_src_kink"]) and not np.any(ref["da_dst_kink"])
+    g = device_graph(case, None)
+    assert g.stats()["csc"]["hubs"] >= 2
+    gpu = run_gpu(case, graph=g)
+    compare(gpu, ref, dtype, what=f"no cancellation {dtype}")
+    for k in ("da_src", "da_dst"):
+        assert_close(gpu[k], ref[k], dtype, None, f"no cancellation {dtype} {k}", strict=True)

@@ -62,3 +62,21 @@ def star_out(n, extra=1):
     in-edges from node 1 (a multi-edge when extra > 1)."""
     rows = [[0] + [1] * extra for _ in range(n)]
     return csr_from_rows(rows)
+
+
+def paired_sources(n_a, n_b, n_c, seed=0, skew=1.6):
+    """Three node groups: A = [0, n_a), B = [n_a, n_a + n_b) and the
+    destinations C after them.  Each destination has exactly two in-edges,
+    from one A node (Zipf law of exponent `skew` over A, so A's first node
+    is a large out-degree hub) and from one B node (uniform); A and B nodes
+    have none."""
+    rng = np.random.default_rng(seed)
+    a_of = np.minimum(rng.zipf(skew, n_c) - 1, n_a - 1).astype(np.int32)
+    b_of = (n_a + rng.integers(0, n_b, n_c)).astype(np.int32)
+    n = n_a + n_b + n_c
+    row_ptr = np.zeros(n + 1, np.int32)
+    row_ptr[n_a + n_b + 1:] = 2 * np.arange(1, n_c + 1, dtype=np.int32)
+    col = np.empty(2 * n_c, np.int32)
+    col[0::2] = a_of
+    col[1::2] = b_of
+    return row_ptr, col
