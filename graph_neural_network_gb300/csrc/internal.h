@@ -40,6 +40,7 @@ struct gnn_graph {
   gnn_tiling tiling{};
   gnn::Dir csr, csc;
   int32_t* err = nullptr;  // device status word (in the caller's buffer)
+  bool csr_sorted = true;  // every CSR row lists its sources in non-decreasing order
   int device = 0;
   int sm_count = 0;
 };

@@ -26,7 +26,8 @@ constexpr int kSortTile = kSortWarps * kSortSteps * 32;  // 2048 edges per block
 // Counters the host reads back at the end of prepare.
 struct Counters {
   int32_t err;
-  int32_t pad[3];
+  int32_t unsorted;  // some CSR row lists a source after a larger one
+  int32_t pad[2];
   int32_t csr[8];  // light, mid, hubs, hub chunks, max degree
   int32_t csc[8];
 };
@@ -57,6 +58,14 @@ __global__ void k_out_degree(const int32_t* col, int64_t e, int32_t* deg) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t x = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; x < e; x += stride)
     atomicAdd(deg + col[x], 1);
+}
+
+// Flags a CSR row whose sources are not in non-decreasing order (rows[x]:
+// the row of position x).
+__global__ void k_row_order(const int32_t* rows, const int32_t* col, int64_t e, int32_t* flag) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t x = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; x + 1 < e; x += stride)
+    if (rows[x] == rows[x + 1] && col[x] > col[x + 1]) atomicOr(flag, 1);
 }
 
 // row id of every CSR position: the last r with row_ptr[r] <= x
@@ -446,6 +455,8 @@ gnn_status prepare_graph(gnn_graph* g, const int32_t* row_ptr, const int32_t* co
     int32_t* v0 = s.k2;  // row id per CSR position; consumed by pass 0
     k_expand_rows<<<grid_for(e, 256), 256, 0, st>>>(row_ptr, n, e, v0);
     if (cuda_fail(cudaGetLastError())) return GNN_ERR_CUDA;
+    k_row_order<<<grid_for(e, 256), 256, 0, st>>>(v0, col, e, &cnt->unsorted);
+    if (cuda_fail(cudaGetLastError())) return GNN_ERR_CUDA;
     if (cuda_fail(radix_sort_pairs(col, v0, e, bits, row_idx, s, st))) return GNN_ERR_CUDA;
   }
 
@@ -457,6 +468,7 @@ gnn_status prepare_graph(gnn_graph* g, const int32_t* row_ptr, const int32_t* co
     return GNN_ERR_CUDA;
 
   g->err = &cnt->err;
+  g->csr_sorted = host.unsorted == 0;
   auto fill = [&](Dir& d, const int32_t* ptr, const int32_t* idx, const DirBuffers& b,
                   const int32_t* c) {
     d.ptr = ptr;

@@ -74,7 +74,9 @@ struct Best {
   static constexpr int V = VecOf<T>::n;
   float v[NV][V];  // sign * value
   int j[NV][V];
+  bool have;       // a candidate has been taken (ascending streams only)
   __device__ __forceinline__ void init() {
+    have = false;
 #pragma unroll
     for (int a = 0; a < NV; ++a)
 #pragma unroll
@@ -105,7 +107,12 @@ struct Best {
 
 // b takes the edges beg + sg, beg + sg + SG, ... < end (sg, SG: this lane's
 // sub-group and the sub-groups sharing the node; 0, 1 for a node of its own).
-template <typename T, int NV>
+// kAsc: the CSR rows list their sources in non-decreasing order, so a lane
+// meets its candidates by ascending source and an equal value never displaces
+// the one it holds: after the lane's first candidate (taken whole), one
+// strict comparison per element decides.  Otherwise the full order (value,
+// then source) is compared.  kMin: the values enter negated.
+template <typename T, int NV, bool kMin, bool kAsc>
 __device__ __forceinline__ void red_edges(const RedArgs& A, const Lane<NV>& L,
                                           const int32_t* cols, int colbase, int beg, int end,
                                           int sg, int SG, int step, int (&jn)[kUnroll],
@@ -127,13 +134,25 @@ __device__ __forceinline__ void red_edges(const RedArgs& A, const Lane<NV>& L,
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (j[u] < 0) continue;
+      const bool first = kAsc && !b.have;
 #pragma unroll
       for (int a = 0; a < NV; ++a) {
         float xv[V];
         unpack<T>(raw[u][a], xv);
 #pragma unroll
-        for (int c = 0; c < V; ++c) b.take(a, c, A.sign * xv[c], j[u]);
+        for (int c = 0; c < V; ++c) {
+          const float sv = kMin ? -xv[c] : xv[c];
+          if (kAsc) {
+            if (first || sv > b.v[a][c]) {
+              b.v[a][c] = sv;
+              b.j[a][c] = j[u];
+            }
+          } else {
+            b.take(a, c, sv, j[u]);
+          }
+        }
       }
+      if (kAsc) b.have = true;
     }
   }
 }
@@ -162,7 +181,7 @@ __device__ __forceinline__ void write_best(const RedArgs& A, const Lane<NV>& L, 
   }
 }
 
-template <typename T, int NV, bool kSub>
+template <typename T, int NV, bool kSub, bool kMin, bool kAsc>
 __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_main(const RedArgs A) {
   constexpr int V = VecOf<T>::n;
   const Lane<NV> L(A.s);
@@ -192,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_ma
       int jn[kUnroll];
       batch_ids<kUnroll>(cols, colbase, wb, it.z, L.g, L.G, jn);
       b.init();
-      red_edges<T, NV>(A, L, cols, colbase, wb, it.z, L.g, L.G, kWarps * kUnroll * L.G, jn, b);
+      red_edges<T, NV, kMin, kAsc>(A, L, cols, colbase, wb, it.z, L.g, L.G,
+                                   kWarps * kUnroll * L.G, jn, b);
       b.merge_subgroups(A.s);
       if (L.g == 0)
 #pragma unroll
@@ -254,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_ma
         int jn[kUnroll];
         batch_ids<kUnroll>(A.idx, 0, beg, end, 0, 1, jn);
         b.init();
-        red_edges<T, NV>(A, L, A.idx, 0, beg, end, 0, 1, kUnroll, jn, b);
+        red_edges<T, NV, kMin, kAsc>(A, L, A.idx, 0, beg, end, 0, 1, kUnroll, jn, b);
         write_best<T, NV>(A, L, i, b);
       }
     }
@@ -285,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_ma
       int jn2[kUnroll];
       batch_ids<kUnroll>(A.idx, 0, b2, i2 >= 0 ? e2 : b2, L.g, L.G, jn2);
       b.init();
-      red_edges<T, NV>(A, L, A.idx, 0, beg, end, L.g, L.G, kUnroll * L.G, jn, b);
+      red_edges<T, NV, kMin, kAsc>(A, L, A.idx, 0, beg, end, L.g, L.G, kUnroll * L.G, jn, b);
       b.merge_subgroups(A.s);
       if (L.g == 0) write_best<T, NV>(A, L, i, b);
       i = i2;
@@ -362,14 +382,26 @@ __global__ void red_bwd_convert(const float* acc, int64_t n8, void* dx) {
 }
 
 template <typename T, int NV>
-cudaError_t launch_fwd_t(const RedArgs& A, int sm_count, cudaStream_t st) {
+cudaError_t launch_fwd_t(const RedArgs& A, bool asc, int sm_count, cudaStream_t st) {
   constexpr int V = VecOf<T>::n;
   cudaError_t e;
   if (A.n_items + A.n_light > 0) {
     const size_t smem = size_t(A.col_off) + size_t(kWarps) * A.s.rv * V * 8;
-    void (*kernel)(const RedArgs) = red_fwd_main<T, NV, false>;
-    if constexpr (NV == 1)
-      if (A.s.lpr < 32) kernel = red_fwd_main<T, NV, true>;
+    const bool mn = A.sign < 0.f;
+    void (*kernel)(const RedArgs);
+    if constexpr (NV == 1) {
+      // a sub-group per light node where the row is narrower than a warp;
+      // the strict comparison where the CSR rows are in ascending order
+      const bool sub = A.s.lpr < 32;
+      if (asc)
+        kernel = sub ? (mn ? red_fwd_main<T, NV, true, true, true> : red_fwd_main<T, NV, true, false, true>)
+                     : (mn ? red_fwd_main<T, NV, false, true, true> : red_fwd_main<T, NV, false, false, true>);
+      else
+        kernel = sub ? (mn ? red_fwd_main<T, NV, true, true, false> : red_fwd_main<T, NV, true, false, false>)
+                     : (mn ? red_fwd_main<T, NV, false, true, false> : red_fwd_main<T, NV, false, false, false>);
+    } else {
+      kernel = mn ? red_fwd_main<T, NV, false, true, false> : red_fwd_main<T, NV, false, false, false>;
+    }
     if (smem > 48 * 1024 &&
         (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(smem))) != cudaSuccess)
@@ -437,15 +469,15 @@ cudaError_t launch_reduce_forward(const gnn_graph* g, const Shape& s, gnn_dtype 
     return e;
   if (dt == GNN_F32) {
     switch (s.nv) {
-      case 1: return launch_fwd_t<float, 1>(A, g->sm_count, st);
-      case 2: return launch_fwd_t<float, 2>(A, g->sm_count, st);
-      case 4: return launch_fwd_t<float, 4>(A, g->sm_count, st);
+      case 1: return launch_fwd_t<float, 1>(A, g->csr_sorted, g->sm_count, st);
+      case 2: return launch_fwd_t<float, 2>(A, g->csr_sorted, g->sm_count, st);
+      case 4: return launch_fwd_t<float, 4>(A, g->csr_sorted, g->sm_count, st);
     }
   } else {
     switch (s.nv) {
-      case 1: return launch_fwd_t<__nv_bfloat16, 1>(A, g->sm_count, st);
-      case 2: return launch_fwd_t<__nv_bfloat16, 2>(A, g->sm_count, st);
-      case 4: return launch_fwd_t<__nv_bfloat16, 4>(A, g->sm_count, st);
+      case 1: return launch_fwd_t<__nv_bfloat16, 1>(A, g->csr_sorted, g->sm_count, st);
+      case 2: return launch_fwd_t<__nv_bfloat16, 2>(A, g->csr_sorted, g->sm_count, st);
+      case 4: return launch_fwd_t<__nv_bfloat16, 4>(A, g->csr_sorted, g->sm_count, st);
     }
   }
   return cudaErrorInvalidValue;

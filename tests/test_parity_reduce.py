@@ -54,6 +54,23 @@ def test_reduce_bucket_thresholds(dtype, tiling, op):
     check(rp, ci, 16, dtype, op, tiling, ties=True, what=f"ties {tiling}")
 
 
+@pytest.mark.parametrize("op", ["max", "min"])
+@pytest.mark.parametrize("tiling", TILINGS, ids=lambda t: "t%d_%d_%d" % t)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_reduce_rows_in_any_order(dtype, tiling, op):
+    """Rows that list their sources in no particular order take the full
+    (value, source) comparison; rows in ascending order take the strict one.
+    With many equal values the winner is the smallest source id either way."""
+    for sort_rows in (False, True):
+        rp, ci = testgraphs.with_in_degrees(THRESHOLD_DEGREES, n_nodes=2500, seed=17,
+                                            sort_rows=sort_rows)
+        if not sort_rows:
+            rows = np.split(ci, rp[1:-1])
+            assert any(np.any(np.diff(r) < 0) for r in rows)
+        for F in ((16, 64) if dtype == "f32" else (16, 128)):
+            check(rp, ci, F, dtype, op, tiling, ties=True, what=f"sorted={sort_rows} F={F}")
+
+
 @pytest.mark.parametrize("F,dtype", [(4, "f32"), (12, "f32"), (128, "f32"), (512, "f32"),
                                      (8, "bf16"), (24, "bf16"), (256, "bf16"), (1024, "bf16")])
 def test_reduce_row_widths(F, dtype):
