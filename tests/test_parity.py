@@ -16,7 +16,7 @@ SHAPES = [  # (H, D, dtype): row vectors rv = H * D * size / 16
     (8, 64, "f32"), (2, 8, "bf16"), (6, 8, "bf16"), (8, 16, "bf16"), (1, 128, "bf16"),
     (4, 64, "bf16"), (12, 32, "bf16"), (1, 256, "bf16"),
 ]
-TILINGS = [(64, 4096, 2048), (8, 64, 16), (0, 0, 1)]
+TILINGS = [(64, 4096, 2048), (1024, 4096, 2048), (8, 64, 16), (0, 0, 1)]
 THRESHOLD_DEGREES = [0, 1, 2, 3, 7, 8, 9, 15, 16, 17, 63, 64, 65, 127, 128, 129, 257, 1000, 2049,
                      4096, 4097]
 

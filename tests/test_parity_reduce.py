@@ -13,7 +13,7 @@ from gpu_util import assert_close, device_graph, to_device, to_f64
 
 pytestmark = pytest.mark.gpu
 
-TILINGS = [(64, 4096, 2048), (8, 64, 16), (0, 0, 1)]
+TILINGS = [(64, 4096, 2048), (1024, 4096, 2048), (8, 64, 16), (0, 0, 1)]
 THRESHOLD_DEGREES = [0, 1, 2, 3, 7, 8, 9, 15, 16, 17, 63, 64, 65, 127, 128, 129, 257, 1000, 2049,
                      4096, 4097]
 
@@ -130,7 +130,7 @@ def test_reduce_ordered_backward(dtype, tiling):
         assert_close(to_f64(runs[0]), b["dx"], dtype, b["dx_mag"], f"ordered dx {tiling} {ties}")
         for r in runs[1:]:
             assert torch.equal(r, runs[0])
-    assert g.stats()["csc"]["hubs"] > 0 or tiling == (64, 4096, 2048)
+    assert g.stats()["csc"]["hubs"] > 0 or tiling[1] == 4096
 
 
 def test_reduce_ordered_backward_power_law():

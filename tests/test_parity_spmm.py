@@ -14,7 +14,7 @@ from gpu_util import assert_close, device_graph, to_device, to_f64
 pytestmark = pytest.mark.gpu
 
 NORMS = ["sum", "mean", "sym"]
-TILINGS = [(64, 4096, 2048), (8, 64, 16), (0, 0, 1)]
+TILINGS = [(64, 4096, 2048), (1024, 4096, 2048), (8, 64, 16), (0, 0, 1)]
 THRESHOLD_DEGREES = [0, 1, 2, 3, 7, 8, 9, 15, 16, 17, 63, 64, 65, 127, 128, 129, 257, 1000, 2049,
                      4096, 4097]
 

@@ -48,7 +48,7 @@ GRAPHS = {
     "star_out": lambda: testgraphs.star_out(5000, extra=2),
     "rmat12": lambda: workload.rmat(12, 16, 0.57, 0.19, 0.19, 9),
 }
-TILINGS = [(64, 4096, 2048), (8, 64, 16), (0, 0, 1)]
+TILINGS = [(64, 4096, 2048), (1024, 4096, 2048), (8, 64, 16), (0, 0, 1)]
 
 
 @pytest.mark.parametrize("tiling", TILINGS, ids=lambda t: "t%d_%d_%d" % t)
