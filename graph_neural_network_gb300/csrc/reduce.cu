@@ -256,9 +256,10 @@ __global__ void __launch_bounds__(kThreads, MinBlocksLean<NV>::value) red_fwd_ma
 
   // ---- light nodes, rows narrower than a warp: one sub-group each --------
   if constexpr (kSub) {
-    // two nodes per sub-group per pull; no shuffles in the edge loop, so the
-    // sub-groups run their own trip counts
-    constexpr int R = 2;
+    // two nodes per sub-group per pull, four where a warp holds two
+    // sub-groups; no shuffles in the edge loop, so the sub-groups run their
+    // own trip counts
+    const int R = L.G == 2 ? 4 : 2;
     const int npull = R * L.G;
     for (;;) {
       int t0 = 0;

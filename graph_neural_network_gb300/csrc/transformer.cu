@@ -478,7 +478,9 @@ __global__ void __launch_bounds__(kThreads, 3) gt_dst_main(const GtArgs A) {
 
   // ---- light nodes, rows narrower than a warp: one sub-group each --------
   if (kSub) {
-    const int R = L.G >= 32 ? 1 : 2;  // nodes per sub-group per pull
+    // nodes per sub-group per pull: four where a warp holds two sub-groups,
+    // two otherwise
+    const int R = L.G >= 32 ? 1 : (L.G == 2 ? 4 : 2);
     const int npull = R * L.G;
     for (;;) {
       int t0 = 0;
@@ -716,7 +718,9 @@ __global__ void __launch_bounds__(kThreads, 3) gt_src_main(const GtArgs A) {
 
   // ---- light nodes, rows narrower than a warp: one sub-group each --------
   if (kSub) {
-    const int R = L.G >= 32 ? 1 : 2;  // nodes per sub-group per pull
+    // nodes per sub-group per pull: four where a warp holds two sub-groups,
+    // two otherwise
+    const int R = L.G >= 32 ? 1 : (L.G == 2 ? 4 : 2);
     const int npull = R * L.G;
     for (;;) {
       int t0 = 0;
