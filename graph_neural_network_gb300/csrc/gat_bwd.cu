@@ -882,13 +882,21 @@ cudaError_t launch_t(const BwdArgs& A, const Shape& s16, gnn_dtype dt, int sm_co
       return e;
     mark(5);
   }
-  // attention-vector gradients
+  // attention-vector gradients: as many blocks as are resident at once (at
+  // most the workspace's rows), so that no second partial wave trails
   {
     const size_t smem = size_t(kWarps) * (32 / s16.lpr) * 2 * row_f * 4;
-    if ((e = launch16<T, DaPartial>(M, unsigned(A.da_blocks), smem, st)) != cudaSuccess) return e;
+    void (*dk)(const BwdArgs) =
+        M.s.nv == 1 ? da_partial<T, 1> : (M.s.nv == 2 ? da_partial<T, 2> : da_partial<T, 4>);
+    if ((e = set_smem(dk, smem)) != cudaSuccess) return e;
+    BwdArgs Md = M;
+    const int64_t resident = persistent_blocks(dk, smem, sm_count);
+    if (resident < Md.da_blocks) Md.da_blocks = int(resident);
+    if ((e = launch16<T, DaPartial>(Md, unsigned(Md.da_blocks), smem, st)) != cudaSuccess)
+      return e;
     mark(6);
     da_final<<<unsigned((2 * row_f + kWarps - 1) / kWarps), kThreads, 0, st>>>(
-        A.da_part, A.da_blocks, row_f, A.da_src, A.da_dst);
+        A.da_part, Md.da_blocks, row_f, A.da_src, A.da_dst);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark(7);
   }

@@ -64,7 +64,8 @@ cudaError_t launch_t(const Shape& s, const void* h, const float* a_src, const fl
   if (n <= 0) return cudaSuccess;
   const int64_t per_block = int64_t(kWarps) * (32 >> s.lpr_log2) * (kNodesPerIter * 16 / VB);
   int64_t blocks = (n + per_block - 1) / per_block;
-  const int64_t cap = int64_t(sm_count > 0 ? sm_count : 1) * 8;
+  // as many blocks as are resident at once: one wave, no trailing partial one
+  const int64_t cap = persistent_blocks(node_scores<T, NV, VB>, 0, sm_count);
   if (blocks > cap) blocks = cap;
   node_scores<T, NV, VB><<<unsigned(blocks), kThreads, 0, st>>>(s, h, a_src, a_dst, n, ssrc,
                                                                 sdst);
