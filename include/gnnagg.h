@@ -135,7 +135,8 @@ gnn_status gnn_graph_destroy(gnn_graph* g);
  *   [2..7]  CSR (by in-degree):  light nodes, block items, hubs, hub chunks,
  *           max in-degree, longest block item
  *   [8..13] CSC (by out-degree): the same six
- *   [14] light_max_deg [15] cta_max_deg
+ *   [14] light_max_deg in use (the chosen value when it was GNN_LIGHT_AUTO)
+ *   [15] cta_max_deg
  * n must be >= 16. */
 gnn_status gnn_graph_stats(const gnn_graph* g, int64_t* stats, int n);
 
