@@ -136,3 +136,19 @@ def test_automatic_light_threshold(scale, ef):
         assert np.array_equal(arr[f"{d}_light"], light)
         assert np.array_equal(arr[f"{d}_items"].astype(np.int64), items)
         assert np.array_equal(arr[f"{d}_hubs"].astype(np.int64), hubs)
+
+
+def test_automatic_light_threshold_capped_by_cta_bound():
+    """An automatic light threshold never exceeds cta_max_deg."""
+    rp, ci = testgraphs.with_in_degrees([0, 1, 7, 8, 9, 15, 16, 17, 40, 100], n_nodes=1500, seed=5)
+    case = make_case(rp, ci, 1, 16, "f32", 1)
+    g = device_graph(case, (-1, 16, 8))
+    st = g.stats()
+    assert st["light_max_deg"] == 16 and st["cta_max_deg"] == 16
+    arr = {k: v.cpu().numpy() for k, v in g.arrays().items()}
+    col_ptr, _ = host_csc(rp, ci)
+    for d, ptr in (("csr", rp), ("csc", col_ptr)):
+        light, items, hubs = host_buckets(ptr, (16, 16, 8))
+        assert np.array_equal(arr[f"{d}_light"], light)
+        assert np.array_equal(arr[f"{d}_items"].astype(np.int64), items)
+        assert np.array_equal(arr[f"{d}_hubs"].astype(np.int64), hubs)
